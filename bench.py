@@ -1,0 +1,500 @@
+#!/usr/bin/env python
+"""Benchmark of the block-wise Sparse GQA prefill (merge + index + top-k +
+union + attention) on GB300.
+
+One step = one sgqa_prefill call over the whole workload (by default the
+Step-5-shaped 128K prefill: 131072 queries, 64 query / 8 KV heads, d = 128,
+B = 8, k = 4096, union tile 64).  Prints one JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   (the CPU oracle, timed on the host)
+
+Timing: W untimed steps, then exactly K steps between CUDA events on the
+launch stream, bracketed by a barrier and a device synchronise; the maximum
+over ranks is reported.  The inputs (several GB) are larger than the 129 MB
+L2, so no flush is needed between steps.  Multi-GPU runs are independent
+replicas (each rank prefills its own copy of the workload; the path has no
+exchange step), so scaling is weak and the value is the total over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Sparse-GQA prefill tokens/s at 128K (merge+index+topk+attn) and % of roofline"
+UNIT = "tokens/s"
+
+
+# ----------------------------------------------------------------------------- setup
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="step5_128k")
+    ap.add_argument("--rho-q", type=float, default=None,
+                    help="AR(1) correlation of the query noise (0 = i.i.d. stress case)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29531")
+        dist.init_process_group(backend)
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Maximum of a float over all ranks (the identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        return {"hbm_gbs": m["hbm_gbs"], "bf16_tflops": m["bf16_tflops"],
+                "bf16_tflops_sustained": m.get("bf16_tflops_sustained", m["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9 or not parts[0].isdigit():
+                    continue
+                if int(parts[0]) != self.gpu_index:
+                    continue
+                rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows),
+                "power_w_max": max((float(r[3]) for r in rows if _isnum(r[3])), default=None)}
+
+
+def _isnum(s):
+    try:
+        float(s)
+        return True
+    except ValueError:
+        return False
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+def algorithmic(wl, chunk: int):
+    """Closed-form algorithmic work of one prefill (mode A):
+      indexer FLOPs  = Hkv * sum_t nh(t) * 2d          (each scored pair once)
+      attention FLOPs = H * sum_t (min(Ks, nh(t)) * B + pos(t) mod B + 1) * 4d
+                        (QK^T and PV over each query's own keys, not the union)
+      compulsory bytes = Q + O + lse + K read by the merge + Kbar write + read
+                        + K and V read once.
+    Also per-chunk attention and indexer FLOPs (one attention / indexer
+    launch per chunk of `chunk` queries) and per-chunk top-k bytes."""
+    T, off, B, d = wl.seq_q, wl.q_offset, wl.block_size, wl.head_dim
+    H, Hkv, Ks = wl.n_q_heads, wl.n_kv_heads, wl.k_blocks
+    t = np.arange(T, dtype=np.int64)
+    pos = off + t
+    nh = np.minimum(pos // B, wl.n_blocks)
+    keys = np.minimum(Ks, nh) * B + pos % B + 1
+    attn = H * keys * 4.0 * d
+    idx = Hkv * nh * 2.0 * d
+    topk_bytes = Hkv * nh * 4.0
+    e = 2 if wl.dtype == "bf16" else 4
+    new_blocks = wl.n_blocks - off // B  # the prefix's block keys are cached (chunked prefill)
+    byts = (2 * T * H * d * e + H * T * 4 + new_blocks * B * Hkv * d * e
+            + 2 * wl.n_blocks * Hkv * d * 4 + 2 * wl.seq_kv * Hkv * d * e)
+    nch = (T + chunk - 1) // chunk
+    per_chunk = lambda a: [float(a[i * chunk:(i + 1) * chunk].sum()) for i in range(nch)]
+    return {"attn_flops": float(attn.sum()), "index_flops": float(idx.sum()),
+            "bytes": float(byts), "attn_flops_chunks": per_chunk(attn),
+            "index_flops_chunks": per_chunk(idx), "topk_bytes_chunks": per_chunk(topk_bytes)}
+
+
+def traffic_from_profiles(kernel_file: str, workload: str):
+    """dram bytes per launch recorded by a committed ncu summary, if the kernel
+    source has not changed since (the summary carries the source's sha256)."""
+    prof = os.path.join(ROOT, "profiles", f"{os.path.splitext(kernel_file)[0]}_{workload}.md")
+    src = os.path.join(ROOT, "block_sparse_long_sgqa_gb300", "csrc", kernel_file)
+    if not (os.path.exists(prof) and os.path.exists(src)):
+        return None
+    text = open(prof).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not (m and h):
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != h.group(1):
+        return None
+    return float(m.group(1))
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(wl, inp, budget_s: float):
+    """Time the CPU oracle on a bounded sample of the workload: the full block
+    merge, plus the per-query pipeline (index query, scores, top-k, attention)
+    for a few spread contiguous query ranges.  Returns (tokens/s extrapolated
+    to the whole workload, sample description, seconds spent)."""
+    import oracle
+    from block_sparse_long_sgqa_gb300 import synth
+
+    Q = synth.widen(inp["Q"])
+    K = synth.widen(inp["K"])
+    V = synth.widen(inp["V"])
+    t0 = time.perf_counter()
+    Kbar = oracle.merge_f64(K, wl.block_size)
+    t_merge = time.perf_counter() - t0
+
+    def run_rows(n_ranges, per):
+        T = wl.seq_q
+        starts = np.linspace(0, T - per, n_ranges).astype(np.int64) if T > per else [0]
+        t1 = time.perf_counter()
+        n = 0
+        for s0 in starts:
+            s0 = int(s0)
+            rows = np.arange(s0, min(T, s0 + per), dtype=np.int32)
+            qt = oracle.index_query(Q, wl.n_kv_heads, rows)
+            S = oracle.scores(qt, Kbar, wl.block_size, wl.q_offset, rows)
+            sel = oracle.select(S, wl.block_size, wl.q_offset, rows, wl.k_blocks)
+            # attention for these rows: a sub-problem with the same positions
+            sub_off = wl.q_offset + s0
+            oracle.sparse_attn(Q[s0:s0 + len(rows)], K, V, sub_off, wl.block_size, sel, 0,
+                               W=wl.tile_q)
+            n += len(rows)
+        return n, time.perf_counter() - t1
+
+    n, dt = run_rows(4, 1)  # probe
+    per_row = dt / max(n, 1)
+    per = max(1, int(budget_s / per_row / 8))
+    n, dt = run_rows(8, per)
+    total = t_merge + wl.seq_q * dt / n
+    desc = (f"full block merge ({t_merge:.2f} s) + {n} queries in 8 spread ranges "
+            f"({dt:.2f} s), extrapolated to {wl.seq_q} queries")
+    return wl.seq_q / total, desc, t_merge + dt
+
+
+# ----------------------------------------------------------------------------- main
+def run_reference(args, wl, rank):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    from block_sparse_long_sgqa_gb300 import synth
+
+    if rank != 0:
+        return None
+    inp = synth.make_inputs(wl, rho_q=args.rho_q)
+    cores = len(os.sched_getaffinity(0))
+    vals, desc = [], ""
+    per_step = max(2.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup + args.steps):
+        v, desc, _ = oracle_sample(wl, inp, per_step)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": wl.seq_q / value * 1000.0, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl, args),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    return line
+
+
+def config_of(wl, args):
+    return {"workload": wl.name, "seq_q": wl.seq_q, "seq_kv": wl.seq_kv, "q_offset": wl.q_offset,
+            "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
+            "block_size": wl.block_size, "topk_tokens": wl.topk_tokens, "tile_q": wl.tile_q,
+            "page_size": wl.page_size, "union_mode": "masked",
+            "inputs": f"seeded {wl.dist}" + (f", AR(1) query noise rho={wl.rho_q if args.rho_q is None else args.rho_q}"
+                                              if wl.dist == "clustered" else "")
+                      + (f", {wl.needles} needle blocks per tile" if wl.needles else ""),
+            "l2": "inputs larger than L2 (no flush between steps)",
+            "parallelism": f"replicas x{args.gpus}"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    from block_sparse_long_sgqa_gb300 import synth
+
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        line = run_reference(args, wl, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+
+    from block_sparse_long_sgqa_gb300 import sgqa
+
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    dev = torch.device("cuda", local)
+    p = sgqa.params_for(wl)
+    chunk, launches = sgqa.sgqa_prefill_plan(p)
+
+    t_gen = time.perf_counter()
+    inp = synth.make_inputs(wl, rho_q=args.rho_q)
+    t_gen = time.perf_counter() - t_gen
+
+    def to_dev(x):
+        t = torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x)
+        t = t.to(dev)
+        return t.view(torch.bfloat16) if x.dtype == np.uint16 else t
+
+    Kh, Vh = inp["K"], inp["V"]
+    if wl.page_size:
+        Kh = synth.to_paged(Kh, inp["page_table"], wl.page_size)
+        Vh = synth.to_paged(Vh, inp["page_table"], wl.page_size)
+    Q, K, V = to_dev(inp["Q"]), to_dev(Kh), to_dev(Vh)
+    pt = torch.from_numpy(inp["page_table"]).to(dev) if wl.page_size else None
+    O, lse = sgqa.alloc_outputs(p, dev)
+    ws = sgqa.alloc_workspace(p, sgqa.WS_PREFILL, dev)
+    st = sgqa.new_status(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # a chunked prefill at 1M: the block keys of the cached prefix exist already
+    kvalid = 0
+    Kbar = sgqa.kbar_empty(p, dev)
+    if wl.q_offset > 0:
+        kvalid = wl.q_offset // wl.block_size
+        sgqa.sgqa_block_merge(p, K, Kbar, 0, kvalid, page_table=pt)
+
+    def step():
+        sgqa.sgqa_prefill(p, Q, K, V, Kbar, O, lse, ws, page_table=pt, kbar_valid_blocks=kvalid,
+                          status=st)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    code, detail = sgqa.read_status(st)
+    if code != 0:
+        raise RuntimeError(f"device status after warm-up: {sgqa.status_string(code)} ({detail})")
+
+    # ---------------- timed region (device-resident inputs)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x for x in vis.split(",") if x.strip().isdigit()]
+    gpu_index = int(ids[local]) if local < len(ids) else local
+    log = sgqa.launch_log(args.steps * (launches + 4))
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_index) as clk, log:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    code, detail = sgqa.read_status(st)
+    if code != 0:
+        raise RuntimeError(f"device status after timing: {sgqa.status_string(code)} ({detail})")
+    ms_max = reduce_max(ms, dev)
+    n_launch = int(reduce_sum(log.count, dev))
+    clocks = clk.summary()
+
+    # ---------------- per-kernel durations from the launch log
+    alg = algorithmic(wl, chunk)
+    peaks = measured_peaks()
+    per_kind = {}
+    for kind, t_ms in log.entries():
+        per_kind.setdefault(kind, []).append(t_ms)
+    total_logged = sum(sum(v) for v in per_kind.values())
+    kernels = {}
+    for kind, ts in per_kind.items():
+        name = sgqa.KERNEL_NAMES.get(kind, str(kind))
+        kernels[name] = {"launches_per_step": len(ts) / args.steps,
+                         "ms_per_step": sum(ts) / args.steps,
+                         "share": sum(ts) / total_logged if total_logged else None}
+    tensor_peak = peaks["bf16_tflops_sustained"]
+    if sgqa.K_ATTN in per_kind:
+        k = kernels["sparse_attn"]
+        k["achieved_tflops"] = alg["attn_flops"] / (k["ms_per_step"] * 1e-3) / 1e12
+        k["frac"] = k["achieved_tflops"] / tensor_peak
+    if sgqa.K_INDEX_SCORES in per_kind:
+        k = kernels["index_scores"]
+        k["achieved_tflops"] = alg["index_flops"] / (k["ms_per_step"] * 1e-3) / 1e12
+        k["frac"] = k["achieved_tflops"] / tensor_peak
+    if sgqa.K_TOPK_UNION in per_kind:
+        k = kernels["topk_union"]
+        k["achieved_gbs"] = sum(alg["topk_bytes_chunks"]) / (k["ms_per_step"] * 1e-3) / 1e9
+        k["frac"] = k["achieved_gbs"] / peaks["hbm_gbs"]
+    dominant = max(kernels, key=lambda n: kernels[n]["ms_per_step"])
+    dk = kernels[dominant]
+    src_of = {"sparse_attn": "attn.cu", "index_scores": "index_gemm.cu",
+              "topk_union": "topk_union.cu", "merge": "merge.cu"}
+    traffic = traffic_from_profiles(src_of.get(dominant, ""), wl.name)
+    if dominant in ("sparse_attn", "index_scores"):
+        roofline = {"kernel": dominant, "bound": "tensor", "achieved": dk["achieved_tflops"],
+                    "peak": tensor_peak, "unit": "TFLOP/s", "frac": dk["frac"],
+                    "traffic": traffic,
+                    "peak_source": f"bf16_tflops_sustained of {peaks['source']}"}
+    else:
+        ach = dk.get("achieved_gbs")
+        roofline = {"kernel": dominant, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": (ach / peaks["hbm_gbs"]) if ach else None,
+                    "traffic": traffic, "peak_source": f"hbm_gbs of {peaks['source']}"}
+    f_alg = alg["attn_flops"] + alg["index_flops"]
+    t_roof = max(f_alg / (tensor_peak * 1e12), alg["bytes"] / (peaks["hbm_gbs"] * 1e9))
+    step_roof = {"flops_alg": f_alg, "bytes_alg": alg["bytes"], "t_roof_ms": t_roof * 1e3,
+                 "frac": t_roof * 1e3 / ms, "peak_tflops": tensor_peak,
+                 "peak_gbs": peaks["hbm_gbs"], "of": peaks["source"]}
+
+    # ---------------- end to end through the C ABI from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        hQ = torch.from_numpy(inp["Q"].view(np.int16) if inp["Q"].dtype == np.uint16
+                              else inp["Q"]).pin_memory()
+        hK = torch.from_numpy(Kh.view(np.int16) if Kh.dtype == np.uint16 else Kh).pin_memory()
+        hV = torch.from_numpy(Vh.view(np.int16) if Vh.dtype == np.uint16 else Vh).pin_memory()
+        hO = torch.empty(O.numel(), dtype=torch.int16 if O.dtype == torch.bfloat16 else torch.float32).pin_memory()
+        hl = torch.empty(lse.numel(), dtype=torch.float32).pin_memory()
+        Qv, Kv, Vv = (Q.view(torch.int16) if Q.dtype == torch.bfloat16 else Q,
+                      K.view(torch.int16) if K.dtype == torch.bfloat16 else K,
+                      V.view(torch.int16) if V.dtype == torch.bfloat16 else V)
+        Ov = O.view(torch.int16) if O.dtype == torch.bfloat16 else O
+
+        def e2e_step():
+            Qv.view(-1).copy_(hQ.view(-1), non_blocking=True)
+            Kv.view(-1).copy_(hK.view(-1), non_blocking=True)
+            Vv.view(-1).copy_(hV.view(-1), non_blocking=True)
+            step()
+            hO.copy_(Ov.view(-1), non_blocking=True)
+            hl.copy_(lse.view(-1), non_blocking=True)
+
+        for _ in range(max(1, min(args.warmup, 2))):
+            e2e_step()
+        barrier()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e2e_ms = reduce_max(ev0.elapsed_time(ev1) / args.steps, dev)
+        h2d = (hQ.numel() + hK.numel() + hV.numel()) * hQ.element_size()
+        d2h = hO.numel() * hO.element_size() + hl.numel() * 4
+        e2e = {"value": world * wl.seq_q / (e2e_ms * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_ms}
+
+    # ---------------- CPU baseline (rank 0, single GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, desc, _ = oracle_sample(wl, inp, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": desc}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": world * wl.seq_q / (ms_max * 1e-3), "unit": UNIT,
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+                "data": "synthetic", "config": config_of(wl, args), "clocks": clocks,
+                "e2e": e2e, "gpu_launches": n_launch, "roofline": roofline,
+                "step_roofline": step_roof, "kernels": kernels, "cpu_baseline": cpu,
+                "input_gen_s": round(t_gen, 2)}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,484 @@
+// C ABI of libsgqa.so: validation, workspace layout and orchestration.
+// Every entry point is declared and documented in include/sgqa.h.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace sgqa {
+
+// launchers with an explicit slot layout (defined next to their kernels)
+int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begin, int64_t q_end,
+                             int32_t* sel, int64_t* union_off, int32_t* union_len,
+                             int32_t* union_blk, uint64_t* union_mask, int64_t union_cap,
+                             int64_t lay_tau0, int64_t lay_ntiles, int64_t capG,
+                             int32_t* status, cudaStream_t st);
+int launch_sparse_attn_layout(const Dims& dm, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                              const __nv_bfloat16* V, const int32_t* page_table,
+                              const int64_t* union_off, const int32_t* union_len,
+                              const int32_t* union_blk, const uint64_t* union_mask, void* O,
+                              float* lse, int64_t tau_begin, int64_t tau_end, int64_t lay_tau0,
+                              int64_t lay_ntiles, int32_t* status, cudaStream_t st);
+
+// ---------------------------------------------------------------- launch log
+static sgqa_launch_log* g_log = nullptr;
+
+void log_begin(int kind, cudaStream_t st) {
+  sgqa_launch_log* l = g_log;
+  if (l == nullptr || l->count >= l->capacity) return;
+  cudaEventRecord(static_cast<cudaEvent_t>(l->start[l->count]), st);
+  l->kind[l->count] = kind;
+}
+
+void log_end(cudaStream_t st) {
+  sgqa_launch_log* l = g_log;
+  if (l == nullptr || l->count >= l->capacity) return;
+  cudaEventRecord(static_cast<cudaEvent_t>(l->stop[l->count]), st);
+  ++l->count;
+}
+
+int derive(const sgqa_params* p, Dims* dm) {
+  if (p == nullptr || dm == nullptr) return SGQA_ERR_INVALID_ARG;
+  if (p->seq_q < 1 || p->q_offset < 0 || p->seq_kv < 1 ||
+      (int64_t)p->q_offset + p->seq_q > p->seq_kv)
+    return SGQA_ERR_INVALID_ARG;
+  if (p->n_kv_heads < 1 || p->n_q_heads < 1 || p->n_q_heads % p->n_kv_heads)
+    return SGQA_ERR_INVALID_ARG;
+  if (p->block_size < 1 || p->topk_tokens < 0 || p->topk_tokens % p->block_size)
+    return SGQA_ERR_INVALID_ARG;
+  if (p->tile_q < 1 || p->dtype < 0 || p->dtype > 1 || p->union_mode < 0 || p->union_mode > 1)
+    return SGQA_ERR_INVALID_ARG;
+  if (!(p->softmax_scale >= 0.0f) || !std::isfinite(p->softmax_scale))
+    return SGQA_ERR_INVALID_ARG;
+  if (p->page_size < 0) return SGQA_ERR_INVALID_ARG;
+  const int B = p->block_size;
+  if (B != 1 && B != 2 && B != 4 && B != 8 && B != 16) return SGQA_ERR_UNSUPPORTED;
+  if (p->head_dim != 64 && p->head_dim != 128) return SGQA_ERR_UNSUPPORTED;
+  if (p->tile_q > 64) return SGQA_ERR_UNSUPPORTED;
+  if (p->n_q_heads / p->n_kv_heads > 128) return SGQA_ERR_UNSUPPORTED;
+  if (p->page_size > 0 &&
+      (p->page_size % B || p->page_size % 8 || p->seq_kv % p->page_size))
+    return SGQA_ERR_UNSUPPORTED;
+  dm->T = p->seq_q;
+  dm->Tkv = p->seq_kv;
+  dm->off = p->q_offset;
+  dm->H = p->n_q_heads;
+  dm->Hkv = p->n_kv_heads;
+  dm->G = p->n_q_heads / p->n_kv_heads;
+  dm->d = p->head_dim;
+  dm->B = B;
+  dm->Ks = p->topk_tokens / B;
+  dm->W = p->tile_q;
+  dm->nblk = p->seq_kv / B;
+  dm->ntiles = (p->seq_q + p->tile_q - 1) / p->tile_q;
+  dm->ps = p->page_size;
+  dm->dtype = p->dtype;
+  dm->mode = p->union_mode;
+  dm->scale = p->softmax_scale > 0.0f ? p->softmax_scale : 1.0f / std::sqrt((float)p->head_dim);
+  dm->elem = p->dtype == SGQA_BF16 ? 2 : 4;
+  return SGQA_OK;
+}
+
+int64_t tile_cap(const Dims& dm, int64_t tau) {
+  const int64_t first = tau * dm.W;
+  const int64_t len = std::min<int64_t>(dm.W, dm.T - first);
+  const int64_t nh = std::min<int64_t>((dm.off + first + len - 1) / dm.B, dm.nblk);
+  return std::min<int64_t>(len * dm.Ks, nh);
+}
+
+static int64_t caps_between(const Dims& dm, int64_t tau0, int64_t tau1) {
+  int64_t s = 0;
+  for (int64_t t = tau0; t < tau1; ++t) s += tile_cap(dm, t);
+  return s;
+}
+
+int64_t group_cap(const Dims& dm) { return caps_between(dm, 0, dm.ntiles); }
+
+// ------------------------------------------------------------------ TMA encode
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                       uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ workspace plans
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Carve {  // bump allocator over a caller-owned workspace
+  uint8_t* p;
+  size_t used = 0;
+  explicit Carve(void* base) : p(static_cast<uint8_t*>(base)) {}
+  template <typename T>
+  T* take(size_t n) {
+    T* r = p ? reinterpret_cast<T*>(p + used) : nullptr;
+    used += up(n * sizeof(T));
+    return r;
+  }
+};
+
+// Queries handled per prefill chunk: bounded so the chunk's fp32 scores stay
+// near 2 GiB, and a multiple of lcm(tile_q, 128).
+int64_t prefill_chunk(const Dims& dm) {
+  int64_t a = dm.W, b = 128;
+  while (b) {
+    const int64_t t = a % b;
+    a = b;
+    b = t;
+  }
+  const int64_t L = dm.W / a * 128;
+  const int64_t per_q = std::max<int64_t>(1, (int64_t)dm.Hkv * dm.nblk * 4);
+  int64_t c = (int64_t(1) << 31) / per_q / L * L;
+  if (c < L) c = L;
+  const int64_t tl = (dm.T + L - 1) / L * L;
+  return std::min(c, tl);
+}
+
+struct IndexWs {
+  __nv_bfloat16 *khi, *klo, *qhi, *qlo;
+};
+IndexWs carve_index(Carve& c, const Dims& dm, int64_t nq) {
+  IndexWs w;
+  const size_t nk = (size_t)dm.Hkv * dm.nblk * dm.d, nqe = (size_t)dm.Hkv * nq * dm.d;
+  w.khi = c.take<__nv_bfloat16>(nk);
+  w.klo = c.take<__nv_bfloat16>(nk);
+  w.qhi = c.take<__nv_bfloat16>(nqe);
+  w.qlo = c.take<__nv_bfloat16>(nqe);
+  return w;
+}
+
+struct AttnWs {
+  __nv_bfloat16 *Q, *K, *V;  // bf16 copies of fp32 inputs (null for bf16 inputs)
+};
+AttnWs carve_attn(Carve& c, const Dims& dm) {
+  AttnWs w{nullptr, nullptr, nullptr};
+  if (dm.dtype == SGQA_FP32) {
+    w.Q = c.take<__nv_bfloat16>((size_t)dm.T * dm.H * dm.d);
+    w.K = c.take<__nv_bfloat16>((size_t)dm.Tkv * dm.Hkv * dm.d);
+    w.V = c.take<__nv_bfloat16>((size_t)dm.Tkv * dm.Hkv * dm.d);
+  }
+  return w;
+}
+
+struct PrefillWs {
+  IndexWs ix;
+  AttnWs at;
+  float* scores;
+  int32_t* sel;
+  int64_t* uoff;
+  int32_t* ulen;
+  int32_t* ublk;
+  uint64_t* umask;
+  int64_t ucap, chunk, chunk_tiles, capG;
+};
+PrefillWs carve_prefill(Carve& c, const Dims& dm) {
+  PrefillWs w;
+  w.chunk = prefill_chunk(dm);
+  w.chunk_tiles = w.chunk / dm.W;
+  w.ix = carve_index(c, dm, w.chunk);
+  w.at = carve_attn(c, dm);
+  w.scores = c.take<float>((size_t)dm.Hkv * w.chunk * std::max<int64_t>(dm.nblk, 1));
+  w.sel = c.take<int32_t>((size_t)dm.Hkv * w.chunk * std::max(dm.Ks, 1));
+  // slot layout of one chunk: the largest chunk's caps
+  int64_t capG = 0;
+  for (int64_t t0 = 0; t0 < dm.ntiles; t0 += w.chunk_tiles)
+    capG = std::max(capG, caps_between(dm, t0, std::min(dm.ntiles, t0 + w.chunk_tiles)));
+  w.capG = capG;
+  w.ucap = capG * dm.Hkv;
+  w.uoff = c.take<int64_t>((size_t)dm.Hkv * w.chunk_tiles);
+  w.ulen = c.take<int32_t>((size_t)dm.Hkv * w.chunk_tiles);
+  w.ublk = c.take<int32_t>((size_t)std::max<int64_t>(w.ucap, 1));
+  w.umask = c.take<uint64_t>((size_t)std::max<int64_t>(w.ucap, 1));
+  return w;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA; }
+
+cudaError_t stage_bf16(const Dims& dm, const void* Q, const void* K, const void* V,
+                       const AttnWs& w, cudaStream_t st) {
+  cudaError_t e = launch_to_bf16(static_cast<const float*>(Q), w.Q, dm.T * dm.H * dm.d, st);
+  if (e == cudaSuccess)
+    e = launch_to_bf16(static_cast<const float*>(K), w.K, dm.Tkv * dm.Hkv * dm.d, st);
+  if (e == cudaSuccess)
+    e = launch_to_bf16(static_cast<const float*>(V), w.V, dm.Tkv * dm.Hkv * dm.d, st);
+  return e;
+}
+
+}  // namespace
+}  // namespace sgqa
+
+using namespace sgqa;
+
+extern "C" {
+
+SGQA_API int sgqa_version(void) { return 100; }
+
+SGQA_API const char* sgqa_status_string(int code) {
+  switch (code) {
+    case SGQA_OK: return "ok";
+    case SGQA_ERR_INVALID_ARG: return "invalid argument";
+    case SGQA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SGQA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case SGQA_ERR_WORKSPACE: return "workspace missing or too small";
+    case SGQA_ERR_CUDA: return "CUDA call or launch failed";
+    case SGQA_ERR_CAPACITY: return "union list exceeded its capacity";
+    case SGQA_ERR_TIMEOUT: return "pipeline wait timed out";
+    case SGQA_ERR_BOUNDS: return "index check failed";
+    default: return "unknown status";
+  }
+}
+
+SGQA_API size_t sgqa_workspace_bytes(const sgqa_params* p, int which) {
+  Dims dm;
+  if (derive(p, &dm) != SGQA_OK) return 0;
+  Carve c(nullptr);
+  switch (which) {
+    case SGQA_WS_INDEX_SCORES: carve_index(c, dm, dm.T); break;
+    case SGQA_WS_TOPK_UNION: c.take<int32_t>(topk_union_ws_bytes(dm, dm.T) / 4); break;
+    case SGQA_WS_SPARSE_ATTN: carve_attn(c, dm); break;
+    case SGQA_WS_PREFILL: carve_prefill(c, dm); break;
+    default: return 0;
+  }
+  return c.used + kAlign;  // slack to align the caller's base
+}
+
+SGQA_API int64_t sgqa_union_capacity(const sgqa_params* p) {
+  Dims dm;
+  if (derive(p, &dm) != SGQA_OK) return -1;
+  return group_cap(dm) * dm.Hkv;
+}
+
+static void* align_ws(void* ws) {
+  return reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(ws) + kAlign - 1) &
+                                 ~static_cast<uintptr_t>(kAlign - 1));
+}
+
+SGQA_API int sgqa_block_merge(const sgqa_params* p, const void* K, const int32_t* page_table,
+                              int32_t blk_begin, int32_t blk_end, float* Kbar, int32_t* status,
+                              sgqa_stream_t stream) {
+  Dims dm;
+  int rc = derive(p, &dm);
+  if (rc != SGQA_OK) return rc;
+  if (K == nullptr || Kbar == nullptr || blk_begin < 0 || blk_end < blk_begin ||
+      blk_end > dm.nblk || ((dm.ps > 0) != (page_table != nullptr)))
+    return SGQA_ERR_INVALID_ARG;
+  if (!aligned16(K) || !aligned16(Kbar)) return SGQA_ERR_ALIGNMENT;
+  (void)status;
+  return cuda_rc(launch_block_merge(dm, K, page_table, blk_begin, blk_end, Kbar, nullptr, nullptr,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+SGQA_API int sgqa_index_scores(const sgqa_params* p, const void* Q, const float* Kbar,
+                               int32_t q_begin, int32_t q_end, float* scores, void* ws,
+                               size_t ws_bytes, int32_t* status, sgqa_stream_t stream) {
+  Dims dm;
+  int rc = derive(p, &dm);
+  if (rc != SGQA_OK) return rc;
+  if (Q == nullptr || Kbar == nullptr || scores == nullptr || q_begin < 0 || q_end < q_begin ||
+      q_end > dm.T)
+    return SGQA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(Kbar) || !aligned16(scores)) return SGQA_ERR_ALIGNMENT;
+  if (ws == nullptr || ws_bytes < sgqa_workspace_bytes(p, SGQA_WS_INDEX_SCORES))
+    return SGQA_ERR_WORKSPACE;
+  if (q_end == q_begin || dm.nblk == 0) return SGQA_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Carve c(align_ws(ws));
+  IndexWs w = carve_index(c, dm, q_end - q_begin);
+  cudaError_t e = launch_split_kbar(dm, Kbar, w.khi, w.klo, st);
+  if (e == cudaSuccess) e = launch_index_query(dm, Q, q_begin, q_end, w.qhi, w.qlo, st);
+  if (e != cudaSuccess) return SGQA_ERR_CUDA;
+  return launch_index_scores(dm, w.qhi, w.qlo, w.khi, w.klo, q_begin, q_end, scores, status, st);
+}
+
+SGQA_API int sgqa_topk_union(const sgqa_params* p, const float* scores, int32_t q_begin,
+                             int32_t q_end, int32_t* topk_idx, int64_t* union_off,
+                             int32_t* union_len, int32_t* union_blk, uint64_t* union_mask,
+                             int64_t union_cap, void* ws, size_t ws_bytes, int32_t* status,
+                             sgqa_stream_t stream) {
+  Dims dm;
+  int rc = derive(p, &dm);
+  if (rc != SGQA_OK) return rc;
+  if (q_begin < 0 || q_end < q_begin || q_end > dm.T || q_begin % dm.W ||
+      (q_end % dm.W && q_end != dm.T))
+    return SGQA_ERR_INVALID_ARG;
+  if ((dm.nblk > 0 && scores == nullptr) || union_off == nullptr || union_len == nullptr ||
+      union_blk == nullptr || union_mask == nullptr)
+    return SGQA_ERR_INVALID_ARG;
+  if (scores && !aligned16(scores)) return SGQA_ERR_ALIGNMENT;
+  if (union_cap < sgqa_union_capacity(p)) return SGQA_ERR_WORKSPACE;
+  int32_t* sel = topk_idx;
+  if (sel == nullptr) {
+    if (ws == nullptr || ws_bytes < sgqa_workspace_bytes(p, SGQA_WS_TOPK_UNION))
+      return SGQA_ERR_WORKSPACE;
+    sel = static_cast<int32_t*>(align_ws(ws));
+  }
+  return launch_topk_union(dm, scores, q_begin, q_end, sel, union_off, union_len, union_blk,
+                           union_mask, union_cap, status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+SGQA_API int sgqa_sparse_attn_fwd(const sgqa_params* p, const void* Q, const void* K,
+                                  const void* V, const int32_t* page_table,
+                                  const int64_t* union_off, const int32_t* union_len,
+                                  const int32_t* union_blk, const uint64_t* union_mask, void* O,
+                                  float* lse, void* ws, size_t ws_bytes, int32_t* status,
+                                  sgqa_stream_t stream) {
+  Dims dm;
+  int rc = derive(p, &dm);
+  if (rc != SGQA_OK) return rc;
+  if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr || lse == nullptr ||
+      union_off == nullptr || union_len == nullptr || union_blk == nullptr ||
+      union_mask == nullptr || ((dm.ps > 0) != (page_table != nullptr)))
+    return SGQA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+    return SGQA_ERR_ALIGNMENT;
+  const size_t need = sgqa_workspace_bytes(p, SGQA_WS_SPARSE_ATTN);
+  if (dm.dtype == SGQA_FP32 && (ws == nullptr || ws_bytes < need)) return SGQA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const __nv_bfloat16 *q = static_cast<const __nv_bfloat16*>(Q),
+                      *k = static_cast<const __nv_bfloat16*>(K),
+                      *v = static_cast<const __nv_bfloat16*>(V);
+  if (dm.dtype == SGQA_FP32) {
+    Carve c(align_ws(ws));
+    AttnWs w = carve_attn(c, dm);
+    if (stage_bf16(dm, Q, K, V, w, st) != cudaSuccess) return SGQA_ERR_CUDA;
+    q = w.Q;
+    k = w.K;
+    v = w.V;
+  }
+  return launch_sparse_attn(dm, q, k, v, page_table, union_off, union_len, union_blk, union_mask,
+                            O, lse, 0, dm.ntiles, status, st);
+}
+
+SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, const void* V,
+                          const int32_t* page_table, float* Kbar, int32_t kbar_valid_blocks,
+                          void* O, float* lse, void* ws, size_t ws_bytes, int32_t* status,
+                          sgqa_stream_t stream) {
+  Dims dm;
+  int rc = derive(p, &dm);
+  if (rc != SGQA_OK) return rc;
+  if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr || lse == nullptr ||
+      Kbar == nullptr || kbar_valid_blocks < 0 || kbar_valid_blocks > dm.nblk ||
+      ((dm.ps > 0) != (page_table != nullptr)))
+    return SGQA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(Kbar))
+    return SGQA_ERR_ALIGNMENT;
+  if (ws == nullptr || ws_bytes < sgqa_workspace_bytes(p, SGQA_WS_PREFILL))
+    return SGQA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Carve c(align_ws(ws));
+  PrefillWs w = carve_prefill(c, dm);
+
+  // step 1: merge the blocks not yet in the cache (and split all of them for the indexer)
+  cudaError_t e = launch_block_merge(dm, K, page_table, kbar_valid_blocks, dm.nblk, Kbar, w.ix.khi,
+                                     w.ix.klo, st);
+  if (e == cudaSuccess && kbar_valid_blocks > 0) {
+    Dims part = dm;  // split the cached prefix: per group, blocks [0, kbar_valid_blocks)
+    for (int g = 0; g < dm.Hkv && e == cudaSuccess; ++g) {
+      part.Hkv = 1;
+      part.nblk = kbar_valid_blocks;
+      const size_t o = (size_t)g * dm.nblk * dm.d;
+      e = launch_split_kbar(part, Kbar + o, w.ix.khi + o, w.ix.klo + o, st);
+    }
+  }
+  const __nv_bfloat16 *q = static_cast<const __nv_bfloat16*>(Q),
+                      *k = static_cast<const __nv_bfloat16*>(K),
+                      *v = static_cast<const __nv_bfloat16*>(V);
+  if (e == cudaSuccess && dm.dtype == SGQA_FP32) {
+    e = stage_bf16(dm, Q, K, V, w.at, st);
+    q = w.at.Q;
+    k = w.at.K;
+    v = w.at.V;
+  }
+  if (e != cudaSuccess) return SGQA_ERR_CUDA;
+
+  for (int64_t q0 = 0; q0 < dm.T; q0 += w.chunk) {
+    const int64_t q1 = std::min<int64_t>(dm.T, q0 + w.chunk);
+    const int64_t tau0 = q0 / dm.W, tau1 = (q1 + dm.W - 1) / dm.W;
+    if (dm.nblk > 0) {
+      e = launch_index_query(dm, Q, q0, q1, w.ix.qhi, w.ix.qlo, st);
+      if (e != cudaSuccess) return SGQA_ERR_CUDA;
+      rc = launch_index_scores(dm, w.ix.qhi, w.ix.qlo, w.ix.khi, w.ix.klo, q0, q1, w.scores,
+                               status, st);
+      if (rc != SGQA_OK) return rc;
+    }
+    rc = launch_topk_union_layout(dm, w.scores, q0, q1, w.sel, w.uoff, w.ulen, w.ublk, w.umask,
+                                  w.ucap, tau0, w.chunk_tiles, w.capG, status, st);
+    if (rc != SGQA_OK) return rc;
+    rc = launch_sparse_attn_layout(dm, q, k, v, page_table, w.uoff, w.ulen, w.ublk, w.umask, O,
+                                   lse, tau0, tau1, tau0, w.chunk_tiles, status, st);
+    if (rc != SGQA_OK) return rc;
+  }
+  return SGQA_OK;
+}
+
+SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int32_t* launches) {
+  Dims dm;
+  const int rc = derive(p, &dm);
+  if (rc != SGQA_OK) return rc;
+  const int64_t chunk = prefill_chunk(dm);
+  if (chunk_queries) *chunk_queries = chunk;
+  if (launches) {
+    // with an empty block-key cache: merge, fp32 staging, then per chunk the
+    // index query and indexer GEMM (when there are blocks), top-k/union, attention
+    const int64_t nchunks = (dm.T + chunk - 1) / chunk;
+    int64_t n = (dm.nblk > 0 ? 1 : 0) + (dm.dtype == SGQA_FP32 ? 3 : 0);
+    n += nchunks * ((dm.nblk > 0 ? 2 : 0) + 2);
+    *launches = (int32_t)n;
+  }
+  return SGQA_OK;
+}
+
+SGQA_API int sgqa_set_launch_log(sgqa_launch_log* log) {
+  if (log != nullptr && (log->capacity < 0 || (log->capacity > 0 &&
+                         (log->start == nullptr || log->stop == nullptr || log->kind == nullptr))))
+    return SGQA_ERR_INVALID_ARG;
+  g_log = log;
+  return SGQA_OK;
+}
+
+SGQA_API int sgqa_reset_status(int32_t* status, sgqa_stream_t stream) {
+  if (status == nullptr) return SGQA_ERR_INVALID_ARG;
+  return cuda_rc(cudaMemsetAsync(status, 0, 4 * sizeof(int32_t),
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+SGQA_API int sgqa_read_status(const int32_t* status, int32_t* detail, sgqa_stream_t stream) {
+  if (status == nullptr) return SGQA_ERR_INVALID_ARG;
+  int32_t h[4] = {0, 0, 0, 0};
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(h, status, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return SGQA_ERR_CUDA;
+  if (detail) *detail = h[1];
+  return h[0];
+}
+
+}  // extern "C"

@@ -1,0 +1,76 @@
+// Host-side definitions shared by the translation units of libsgqa.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sgqa.h"
+
+namespace sgqa {
+
+// Parameters of one call, validated and derived once on the host.
+struct Dims {
+  int64_t T, Tkv, off;       // queries, keys, position of query 0
+  int H, Hkv, G, d;          // heads, KV groups, heads per group, head dim
+  int B, Ks, W;              // block size, blocks selected per query, union tile
+  int64_t nblk, ntiles;      // complete blocks, union tiles of the call
+  int ps;                    // page size (0 = contiguous)
+  int dtype, mode;           // enum sgqa_dtype, enum sgqa_union_mode
+  float scale;               // softmax scale
+  int elem;                  // bytes per Q/K/V element
+};
+
+// Validate `p` and fill `dm`; returns SGQA_OK or an error code.
+int derive(const sgqa_params* p, Dims* dm);
+
+// nh of query t (absolute index within the call): historical complete blocks.
+inline int64_t nh_of(const Dims& dm, int64_t t) {
+  int64_t nh = (dm.off + t) / dm.B;
+  return nh < dm.nblk ? nh : dm.nblk;
+}
+
+// Union slot capacity of tile tau of one group, and of one whole group.
+int64_t tile_cap(const Dims& dm, int64_t tau);
+int64_t group_cap(const Dims& dm);
+
+// Encode a tiled TMA descriptor (2-D, 128-byte swizzle, bf16) through the
+// driver entry point; returns false on failure.
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                       uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// Launch-log hooks (see sgqa_set_launch_log): called immediately around every
+// kernel launch of the library.
+void log_begin(int kind, cudaStream_t st);
+void log_end(cudaStream_t st);
+
+// ---- launchers (all asynchronous on `st`; return cudaSuccess or the launch error)
+cudaError_t launch_block_merge(const Dims& dm, const void* K, const int32_t* page_table,
+                               int64_t blk_begin, int64_t blk_end, float* Kbar,
+                               __nv_bfloat16* khi, __nv_bfloat16* klo, cudaStream_t st);
+cudaError_t launch_split_kbar(const Dims& dm, const float* Kbar, __nv_bfloat16* khi,
+                              __nv_bfloat16* klo, cudaStream_t st);
+cudaError_t launch_index_query(const Dims& dm, const void* Q, int64_t q_begin, int64_t q_end,
+                               __nv_bfloat16* qhi, __nv_bfloat16* qlo, cudaStream_t st);
+cudaError_t launch_to_bf16(const float* in, __nv_bfloat16* out, int64_t n, cudaStream_t st);
+
+// scores [Hkv][q_end-q_begin][nblk]; qhi/qlo are [Hkv][q_end-q_begin][d].
+int launch_index_scores(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* qlo,
+                        const __nv_bfloat16* khi, const __nv_bfloat16* klo, int64_t q_begin,
+                        int64_t q_end, float* scores, int32_t* status, cudaStream_t st);
+
+size_t topk_union_ws_bytes(const Dims& dm, int64_t nq);
+int launch_topk_union(const Dims& dm, const float* scores, int64_t q_begin, int64_t q_end,
+                      int32_t* sel, int64_t* union_off, int32_t* union_len, int32_t* union_blk,
+                      uint64_t* union_mask, int64_t union_cap, int32_t* status, cudaStream_t st);
+
+// Attention over the tiles [tau_begin, tau_end) of the call.  Q/K/V are bf16.
+int launch_sparse_attn(const Dims& dm, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                       const __nv_bfloat16* V, const int32_t* page_table,
+                       const int64_t* union_off, const int32_t* union_len,
+                       const int32_t* union_blk, const uint64_t* union_mask, void* O,
+                       float* lse, int64_t tau_begin, int64_t tau_end, int32_t* status,
+                       cudaStream_t st);
+
+}  // namespace sgqa

@@ -1,0 +1,236 @@
+// Streaming kernels of the path (HBM-bound, no tensor cores):
+//  - block merge: the block representation of "Reducing indexer's cost"
+//    (Inside Step 5 Preview, section Sparse GQA), the mean of B adjacent keys;
+//  - the bf16 hi/lo split of the block keys and of the group index queries
+//    that feeds the tensor-core indexer;
+//  - fp32 -> bf16 staging of attention operands.
+#include "common.cuh"
+#include "internal.h"
+
+namespace sgqa {
+namespace {
+
+template <typename T>
+struct Vec8;  // 8 consecutive elements loaded as one 16- or 32-byte access
+
+template <>
+struct Vec8<__nv_bfloat16> {
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&v)[8]) {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f = __bfloat1622float2(h[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+};
+template <>
+struct Vec8<float> {
+  static __device__ __forceinline__ void load(const float* p, float (&v)[8]) {
+    float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
+__device__ __forceinline__ void split_store8(const float (&v)[8], __nv_bfloat16* hi,
+                                             __nv_bfloat16* lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]);
+    __nv_bfloat16 h1 = __float2bfloat16_rn(v[2 * i + 1]);
+    float r0 = __fsub_rn(v[2 * i], __bfloat162float(h0));  // exact in fp32
+    float r1 = __fsub_rn(v[2 * i + 1], __bfloat162float(h1));
+    __nv_bfloat162 hh(h0, h1);
+    h[i] = *reinterpret_cast<uint32_t*>(&hh);
+    l[i] = pack_bf16x2(r0, r1);
+  }
+  *reinterpret_cast<uint4*>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// One thread = 8 consecutive head-dim lanes of one (block, group).
+// Sum of the B rows as adjacent pairs level by level, then times 1/B.
+template <typename T, int B>
+__global__ void __launch_bounds__(256) k_block_merge(const T* __restrict__ K,
+                                                     const int32_t* __restrict__ page_table,
+                                                     int64_t blk_begin, int64_t nblocks, int Hkv,
+                                                     int d, int ps, int64_t nblk,
+                                                     float* __restrict__ Kbar,
+                                                     __nv_bfloat16* __restrict__ khi,
+                                                     __nv_bfloat16* __restrict__ klo) {
+  const int chunks = d / 8;
+  const int64_t total = nblocks * Hkv * chunks;
+  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
+       x += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(x % chunks);
+    const int g = (int)((x / chunks) % Hkv);
+    const int64_t j = blk_begin + x / ((int64_t)chunks * Hkv);
+    float v[B][8];
+#pragma unroll
+    for (int r = 0; r < B; ++r) {
+      const int64_t p = j * B + r;
+      const T* row;
+      if (ps > 0) {
+        const int64_t phys = page_table[p / ps];
+        row = K + ((phys * Hkv + g) * ps + (p % ps)) * (int64_t)d;
+      } else {
+        row = K + (p * Hkv + g) * (int64_t)d;
+      }
+      Vec8<T>::load(row + c * 8, v[r]);
+    }
+#pragma unroll
+    for (int w = B; w > 1; w /= 2)
+#pragma unroll
+      for (int r = 0; r < w / 2; ++r)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[r][i] = __fadd_rn(v[2 * r][i], v[2 * r + 1][i]);
+    const float inv = 1.0f / (float)B;  // exact: B is a power of two
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[0][i] = __fmul_rn(v[0][i], inv);
+    const int64_t o = ((int64_t)g * nblk + j) * d + c * 8;
+    float4* dst = reinterpret_cast<float4*>(Kbar + o);
+    dst[0] = make_float4(v[0][0], v[0][1], v[0][2], v[0][3]);
+    dst[1] = make_float4(v[0][4], v[0][5], v[0][6], v[0][7]);
+    if (khi != nullptr) split_store8(v[0], khi + o, klo + o);
+  }
+}
+
+__global__ void __launch_bounds__(256) k_split_kbar(const float* __restrict__ Kbar, int64_t n8,
+                                                    __nv_bfloat16* __restrict__ khi,
+                                                    __nv_bfloat16* __restrict__ klo) {
+  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < n8;
+       x += (int64_t)gridDim.x * blockDim.x) {
+    float v[8];
+    Vec8<float>::load(Kbar + x * 8, v);
+    split_store8(v, khi + x * 8, klo + x * 8);
+  }
+}
+
+// Group index query: qt[g][t] = (1/G) * sum of the G heads of group g, summed
+// in head order in fp32, then split into bf16 hi/lo.  Output [Hkv][nq][d].
+template <typename T>
+__global__ void __launch_bounds__(256) k_index_query(const T* __restrict__ Q, int64_t q_begin,
+                                                     int64_t nq, int H, int Hkv, int G, int d,
+                                                     __nv_bfloat16* __restrict__ qhi,
+                                                     __nv_bfloat16* __restrict__ qlo) {
+  const int chunks = d / 8;
+  const int64_t total = nq * Hkv * chunks;
+  const float invG = 1.0f / (float)G;
+  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
+       x += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(x % chunks);
+    const int g = (int)((x / chunks) % Hkv);
+    const int64_t tl = x / ((int64_t)chunks * Hkv);
+    float acc[8], v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int h = 0; h < G; ++h) {
+      Vec8<T>::load(Q + ((q_begin + tl) * H + g * G + h) * (int64_t)d + c * 8, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], v[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = __fmul_rn(acc[i], invG);
+    const int64_t o = ((int64_t)g * nq + tl) * d + c * 8;
+    split_store8(acc, qhi + o, qlo + o);
+  }
+}
+
+__global__ void __launch_bounds__(256) k_to_bf16(const float* __restrict__ in, int64_t n8,
+                                                 __nv_bfloat16* __restrict__ out) {
+  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < n8;
+       x += (int64_t)gridDim.x * blockDim.x) {
+    float v[8];
+    Vec8<float>::load(in + x * 8, v);
+    uint4 u = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                         pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+    *reinterpret_cast<uint4*>(out + x * 8) = u;
+  }
+}
+
+int grid_for(int64_t work) {
+  // enough CTAs to cover every SM several times; grid-stride loops do the rest
+  int64_t g = (work + 255) / 256;
+  const int64_t cap = 152 * 16;
+  return (int)(g < 1 ? 1 : (g > cap ? cap : g));
+}
+
+template <typename T>
+cudaError_t merge_dispatch(const Dims& dm, const T* K, const int32_t* pt, int64_t b0, int64_t nb,
+                           float* Kbar, __nv_bfloat16* khi, __nv_bfloat16* klo, cudaStream_t st) {
+  const int grid = grid_for(nb * dm.Hkv * (dm.d / 8));
+  log_begin(SGQA_K_MERGE, st);
+#define SGQA_MERGE_CASE(BB)                                                                   \
+  case BB:                                                                                    \
+    k_block_merge<T, BB><<<grid, 256, 0, st>>>(K, pt, b0, nb, dm.Hkv, dm.d, dm.ps, dm.nblk,  \
+                                               Kbar, khi, klo);                               \
+    break;
+  switch (dm.B) {
+    SGQA_MERGE_CASE(1)
+    SGQA_MERGE_CASE(2)
+    SGQA_MERGE_CASE(4)
+    SGQA_MERGE_CASE(8)
+    SGQA_MERGE_CASE(16)
+    default:
+      log_end(st);
+      return cudaErrorInvalidValue;
+  }
+#undef SGQA_MERGE_CASE
+  log_end(st);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_block_merge(const Dims& dm, const void* K, const int32_t* page_table,
+                               int64_t blk_begin, int64_t blk_end, float* Kbar,
+                               __nv_bfloat16* khi, __nv_bfloat16* klo, cudaStream_t st) {
+  const int64_t nb = blk_end - blk_begin;
+  if (nb <= 0) return cudaSuccess;
+  if (dm.dtype == SGQA_BF16)
+    return merge_dispatch(dm, static_cast<const __nv_bfloat16*>(K), page_table, blk_begin, nb,
+                          Kbar, khi, klo, st);
+  return merge_dispatch(dm, static_cast<const float*>(K), page_table, blk_begin, nb, Kbar, khi,
+                        klo, st);
+}
+
+cudaError_t launch_split_kbar(const Dims& dm, const float* Kbar, __nv_bfloat16* khi,
+                              __nv_bfloat16* klo, cudaStream_t st) {
+  const int64_t n8 = (int64_t)dm.Hkv * dm.nblk * dm.d / 8;
+  if (n8 == 0) return cudaSuccess;
+  log_begin(SGQA_K_SPLIT, st);
+  k_split_kbar<<<grid_for(n8), 256, 0, st>>>(Kbar, n8, khi, klo);
+  log_end(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_index_query(const Dims& dm, const void* Q, int64_t q_begin, int64_t q_end,
+                               __nv_bfloat16* qhi, __nv_bfloat16* qlo, cudaStream_t st) {
+  const int64_t nq = q_end - q_begin;
+  if (nq <= 0) return cudaSuccess;
+  const int grid = grid_for(nq * dm.Hkv * (dm.d / 8));
+  log_begin(SGQA_K_INDEX_QUERY, st);
+  if (dm.dtype == SGQA_BF16)
+    k_index_query<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(Q), q_begin, nq, dm.H,
+                                        dm.Hkv, dm.G, dm.d, qhi, qlo);
+  else
+    k_index_query<<<grid, 256, 0, st>>>(static_cast<const float*>(Q), q_begin, nq, dm.H, dm.Hkv,
+                                        dm.G, dm.d, qhi, qlo);
+  log_end(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_bf16(const float* in, __nv_bfloat16* out, int64_t n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  log_begin(SGQA_K_STAGE, st);
+  k_to_bf16<<<grid_for(n / 8), 256, 0, st>>>(in, n / 8, out);
+  log_end(st);
+  return cudaGetLastError();
+}
+
+}  // namespace sgqa

@@ -1,0 +1,440 @@
+// Top-k block selection and tile union.
+//
+// "Inside Step 5 Preview" (StepFun blog), section Sparse GQA: each query keeps
+// its k/B best historical blocks (paragraph "Trade-off between top-k and block
+// size"), and the selections of adjacent queries are unioned so one gathered
+// block list serves a whole tile (paragraph "Efficient implementation of
+// sparse attention").
+//
+// One CTA per (KV group, tile).  Each warp owns rows (queries) of the tile and
+// runs an exact radix select on the row's fp32 scores, compared through the
+// order-preserving map of their bit patterns: an 11-bit histogram of the top
+// key bits finds the bucket of the k-th largest key, the bucket's members are
+// compacted into shared memory, two more histogram levels (11 + 10 bits) pin
+// the k-th key exactly, and a final pass in ascending block order emits every
+// block above it plus the lowest-indexed blocks equal to it.  Emission uses
+// warp ballots, so each list comes out sorted and each 32-block word of the
+// tile's union bitmask is OR-ed in one shared atomic.  The union is then the
+// set bits of that bitmask (ranks by a prefix sum of word popcounts), and a
+// member mask per union slot is built from the rows' lists with shared (or,
+// for very long unions, global) atomic ORs.
+#include "common.cuh"
+#include "internal.h"
+
+namespace sgqa {
+namespace {
+
+constexpr int NB0 = 2048;        // bins of the level-0 and level-1 histograms (11 bits)
+constexpr int CAND_CAP = 1024;   // bucket members kept in shared memory per warp
+constexpr int WARP_BYTES = NB0 * 4 + CAND_CAP * 8;
+constexpr unsigned FULL = 0xffffffffu;
+
+struct TUArgs {
+  const float* scores;  // [Hkv][nq][nblk], rows q_begin .. q_end-1 of the call
+  int64_t nq, q_begin, q_end, T, off, nblk;
+  int B, Ks, W;
+  int32_t* sel;         // [Hkv][nq][Ks]
+  int64_t* uoff;        // [Hkv][lay_ntiles]
+  int32_t* ulen;
+  int32_t* ublk;
+  uint64_t* umask;
+  int64_t ucap;         // slots available
+  int64_t lay_tau0;     // first tile of the slot layout
+  int64_t lay_ntiles;   // tiles in the slot layout
+  int64_t capG;         // slots per group in the layout
+  int64_t tau_begin;    // first tile of this launch
+  int nwords;           // ceil(nblk / 32)
+  int nw;               // warps per CTA
+  int32_t* status;
+};
+
+__device__ __forceinline__ int64_t cap_of_tile(const TUArgs& a, int64_t tau) {
+  const int64_t first = tau * a.W;
+  int64_t len = a.T - first;
+  if (len > a.W) len = a.W;
+  int64_t nh = (a.off + first + len - 1) / a.B;
+  if (nh > a.nblk) nh = a.nblk;
+  const int64_t k = len * a.Ks;
+  return k < nh ? k : nh;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Warp-wide: in `hist` (nbins, a multiple of 32), find the bin holding the
+// need-th largest element counting from the top bin down.  Returns the bin,
+// the count strictly above it and the bin's count.
+__device__ void find_bin(const uint32_t* hist, int nbins, uint32_t need, uint32_t& bin,
+                         uint32_t& above, uint32_t& cnt) {
+  const int lane = lane_id();
+  const int per = nbins / 32;
+  const int lo = lane * per;
+  uint32_t s = 0;
+  for (int i = 0; i < per; ++i) s += hist[lo + ((i + lane) & (per - 1))];  // rotated: no bank conflicts
+  uint32_t incl = s;  // sum over lanes >= lane
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_down_sync(FULL, incl, o);
+    if (lane + o < 32) incl += v;
+  }
+  const uint32_t excl = incl - s;
+  const uint32_t who_m = __ballot_sync(FULL, excl < need && need <= incl);
+  const int who = who_m ? __ffs(who_m) - 1 : 0;
+  uint32_t b = 0, ab = 0, c = 0;
+  if (lane == who) {
+    uint32_t acc = excl;
+    for (int i = per - 1; i >= 0; --i) {
+      const uint32_t h = hist[lo + i];
+      if (acc + h >= need) {
+        b = lo + i;
+        ab = acc;
+        c = h;
+        break;
+      }
+      acc += h;
+    }
+  }
+  bin = __shfl_sync(FULL, b, who);
+  above = __shfl_sync(FULL, ab, who);
+  cnt = __shfl_sync(FULL, c, who);
+}
+
+__device__ __forceinline__ void zero_hist(uint32_t* hist, int nbins) {
+  for (int i = lane_id() * 4; i < nbins; i += 128)
+    *reinterpret_cast<uint4*>(hist + i) = make_uint4(0, 0, 0, 0);
+  __syncwarp();
+}
+
+// Histogram of (key >> shift) & (nbins-1) over row keys whose key >> pshift == pval
+// (no filter when pshift == 32).
+__device__ void hist_row(const float* __restrict__ row, int64_t nh, bool vec, uint32_t* hist,
+                         int shift, int nbins, int pshift, uint32_t pval) {
+  const int lane = lane_id();
+  const uint32_t bm = nbins - 1;
+  if (vec) {
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    const int64_t n4 = nh / 4;
+    int64_t x = lane;
+    for (; x + 7 * 32 < n4; x += 8 * 32) {  // 8 loads in flight per lane
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldg(r4 + x + u * 32);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t key = order_key(e[k]);
+          if (pshift == 32 || (key >> pshift) == pval) atomicAdd(&hist[(key >> shift) & bm], 1u);
+        }
+      }
+    }
+    for (; x < n4; x += 32) {
+      const float4 v = __ldg(r4 + x);
+      const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t key = order_key(e[k]);
+        if (pshift == 32 || (key >> pshift) == pval) atomicAdd(&hist[(key >> shift) & bm], 1u);
+      }
+    }
+    for (int64_t j = n4 * 4 + lane; j < nh; j += 32) {
+      const uint32_t key = order_key(__ldg(row + j));
+      if (pshift == 32 || (key >> pshift) == pval) atomicAdd(&hist[(key >> shift) & bm], 1u);
+    }
+  } else {
+    for (int64_t j = lane; j < nh; j += 32) {
+      const uint32_t key = order_key(__ldg(row + j));
+      if (pshift == 32 || (key >> pshift) == pval) atomicAdd(&hist[(key >> shift) & bm], 1u);
+    }
+  }
+  __syncwarp();
+}
+
+__device__ void hist_cand(const uint32_t* ck, int n, uint32_t* hist, int shift, int nbins,
+                          int pshift, uint32_t pval) {
+  const uint32_t bm = nbins - 1;
+  for (int i = lane_id(); i < n; i += 32) {
+    const uint32_t key = ck[i];
+    if ((key >> pshift) == pval) atomicAdd(&hist[(key >> shift) & bm], 1u);
+  }
+  __syncwarp();
+}
+
+// Select row t of group g, write its ascending list and OR it into the tile
+// bitmask.  Returns nothing; all lanes participate.
+__device__ void select_row(const TUArgs& a, int g, int64_t t, uint32_t* hist, uint32_t* ck,
+                           int32_t* ci, uint32_t* tile_bits) {
+  const int lane = lane_id();
+  const int64_t tl = t - a.q_begin;
+  int64_t nh = (a.off + t) / a.B;
+  if (nh > a.nblk) nh = a.nblk;
+  const uint32_t need = (uint32_t)(nh < a.Ks ? nh : a.Ks);
+  const float* row = a.scores + ((int64_t)g * a.nq + tl) * a.nblk;
+  int32_t* out = a.sel + ((int64_t)g * a.nq + tl) * a.Ks;
+  const bool vec = (a.nblk & 3) == 0;
+  if (need == 0) {
+    for (int64_t x = lane; x < a.Ks; x += 32) out[x] = -1;
+    return;
+  }
+
+  bool take_all = (int64_t)need == nh;
+  uint32_t Tp = 0, rem = need;
+  int shift = 0;
+  if (!take_all) {
+    uint32_t b, above, cnt;
+    zero_hist(hist, NB0);
+    hist_row(row, nh, vec, hist, 21, NB0, 32, 0);
+    find_bin(hist, NB0, rem, b, above, cnt);
+    rem -= above;
+    Tp = b;
+    shift = 21;
+    if (cnt != rem) {
+      const bool use_cand = cnt <= (uint32_t)CAND_CAP;
+      int n = 0;
+      if (use_cand) {  // compact the bucket's members, in block order
+        for (int64_t base = 0; base < nh; base += 32) {
+          const int64_t j = base + lane;
+          const uint32_t key = j < nh ? order_key(__ldg(row + j)) : 0u;
+          const bool in = j < nh && (key >> 21) == b;
+          const uint32_t m = __ballot_sync(FULL, in);
+          if (in) {
+            const int p = n + __popc(m & lanemask_lt());
+            ck[p] = key;
+            ci[p] = (int32_t)j;
+          }
+          n += __popc(m);
+        }
+        __syncwarp();
+      }
+      // level 1: bits 20..10
+      zero_hist(hist, NB0);
+      if (use_cand) hist_cand(ck, n, hist, 10, NB0, 21, Tp);
+      else hist_row(row, nh, vec, hist, 10, NB0, 21, Tp);
+      find_bin(hist, NB0, rem, b, above, cnt);
+      rem -= above;
+      Tp = (Tp << 11) | b;
+      shift = 10;
+      if (cnt != rem) {
+        // level 2: bits 9..0
+        zero_hist(hist, 1024);
+        if (use_cand) hist_cand(ck, n, hist, 0, 1024, 10, Tp);
+        else hist_row(row, nh, vec, hist, 0, 1024, 10, Tp);
+        find_bin(hist, 1024, rem, b, above, cnt);
+        rem -= above;
+        Tp = (Tp << 10) | b;
+        shift = 0;
+      }
+    }
+  }
+
+  // emission in ascending block order
+  uint32_t eq_seen = 0, n_out = 0;
+  for (int64_t base = 0; base < nh; base += 32) {
+    const int64_t j = base + lane;
+    const bool valid = j < nh;
+    bool take;
+    uint32_t meq = 0;
+    if (take_all) {
+      take = valid;
+    } else {
+      const uint32_t kp = valid ? (order_key(__ldg(row + j)) >> shift) : 0u;
+      const bool above = valid && kp > Tp;
+      const bool eq = valid && kp == Tp;
+      meq = __ballot_sync(FULL, eq);
+      const uint32_t rank = eq_seen + __popc(meq & lanemask_lt());
+      take = above || (eq && rank < rem);
+    }
+    const uint32_t mt = __ballot_sync(FULL, take);
+    if (take) out[n_out + __popc(mt & lanemask_lt())] = (int32_t)j;
+    if (lane == 0 && mt) atomicOr(&tile_bits[base >> 5], mt);
+    n_out += __popc(mt);
+    eq_seen += __popc(meq);
+  }
+  for (int64_t x = n_out + lane; x < a.Ks; x += 32) out[x] = -1;
+  if (lane == 0 && n_out != need) report(a.status, SGQA_ERR_BOUNDS, (int)t);
+}
+
+__global__ void k_topk_union(TUArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int g = blockIdx.y;
+  const int64_t tau = a.tau_begin + blockIdx.x;
+  const int nthr = blockDim.x;
+  const int tid = threadIdx.x, warp = warp_id(), lane = lane_id();
+  uint32_t* tile_bits = reinterpret_cast<uint32_t*>(smem);
+  uint32_t* wprefix = tile_bits + ((a.nwords + 3) & ~3);          // nwords + 1 entries
+  uint8_t* wbase = reinterpret_cast<uint8_t*>(wprefix + ((a.nwords + 1 + 3) & ~3));
+  __shared__ int64_t s_red[32];
+  __shared__ int64_t s_base;
+
+  for (int i = tid; i < a.nwords; i += nthr) tile_bits[i] = 0;
+
+  // slot base of this tile: g * capG + sum of the caps of the layout's earlier tiles
+  int64_t part = 0;
+  for (int64_t x = a.lay_tau0 + tid; x < tau; x += nthr) part += cap_of_tile(a, x);
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_down_sync(FULL, part, o);
+  if (lane == 0) s_red[warp] = part;
+  __syncthreads();
+  if (tid == 0) {
+    int64_t s = 0;
+    for (int w = 0; w < a.nw; ++w) s += s_red[w];
+    s_base = (int64_t)g * a.capG + s;
+  }
+
+  // ---- per-row selection
+  const int64_t first = tau * a.W;
+  int len = (int)((a.T - first) < a.W ? (a.T - first) : a.W);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(wbase + (size_t)warp * WARP_BYTES);
+  uint32_t* ck = hist + NB0;
+  int32_t* ci = reinterpret_cast<int32_t*>(ck + CAND_CAP);
+  for (int i = warp; i < len; i += a.nw) select_row(a, g, first + i, hist, ck, ci, tile_bits);
+  __syncthreads();
+
+  // ---- union list: ranks from a prefix sum of word popcounts
+  if (warp == 0) {
+    uint32_t carry = 0;
+    for (int base = 0; base < a.nwords; base += 32) {
+      const int w = base + lane;
+      const uint32_t c = w < a.nwords ? __popc(tile_bits[w]) : 0u;
+      uint32_t incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (w < a.nwords) wprefix[w] = carry + incl - c;
+      carry += __shfl_sync(FULL, incl, 31);
+    }
+    if (lane == 0) wprefix[a.nwords] = carry;
+  }
+  __syncthreads();
+  const int64_t U = wprefix[a.nwords];
+  const int64_t base = s_base;
+  const int64_t cap = cap_of_tile(a, tau);
+  const int64_t lt = (int64_t)g * a.lay_ntiles + (tau - a.lay_tau0);
+  if (U > cap || base + U > a.ucap) {
+    if (tid == 0) {
+      report(a.status, SGQA_ERR_CAPACITY, (int)tau);
+      a.uoff[lt] = base;
+      a.ulen[lt] = 0;
+    }
+    return;
+  }
+  for (int w = tid; w < a.nwords; w += nthr) {
+    uint32_t bits = tile_bits[w];
+    uint32_t r = wprefix[w];
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      a.ublk[base + r++] = w * 32 + b;
+      bits &= bits - 1;
+    }
+  }
+
+  // ---- member masks
+  const int64_t mask_words = (int64_t)a.nw * WARP_BYTES / 8;  // lo/hi pairs that fit
+  const bool in_smem = U <= mask_words;
+  uint32_t* mlo = reinterpret_cast<uint32_t*>(wbase);
+  uint32_t* mhi = mlo + (in_smem ? U : 0);
+  if (in_smem) {
+    for (int64_t s = tid; s < 2 * U; s += nthr) mlo[s] = 0;
+  } else {
+    for (int64_t s = tid; s < U; s += nthr) a.umask[base + s] = 0;
+  }
+  __syncthreads();
+  for (int i = warp; i < len; i += a.nw) {
+    const int64_t t = first + i;
+    int64_t nh = (a.off + t) / a.B;
+    if (nh > a.nblk) nh = a.nblk;
+    const int64_t need = nh < a.Ks ? nh : a.Ks;
+    const int32_t* lst = a.sel + ((int64_t)g * a.nq + (t - a.q_begin)) * a.Ks;
+    for (int64_t x = lane; x < need; x += 32) {
+      const int32_t j = lst[x];
+      const int w = j >> 5;
+      const int64_t slot = wprefix[w] + __popc(tile_bits[w] & ((1u << (j & 31)) - 1u));
+      if (in_smem) {
+        atomicOr(i < 32 ? &mlo[slot] : &mhi[slot], 1u << (i & 31));
+      } else {
+        atomicOr(reinterpret_cast<unsigned long long*>(&a.umask[base + slot]),
+                 1ull << i);
+      }
+    }
+  }
+  __syncthreads();
+  if (in_smem)
+    for (int64_t s = tid; s < U; s += nthr)
+      a.umask[base + s] = (static_cast<uint64_t>(mhi[s]) << 32) | mlo[s];
+  if (tid == 0) {
+    a.uoff[lt] = base;
+    a.ulen[lt] = (int32_t)U;
+  }
+}
+
+}  // namespace
+
+size_t topk_union_ws_bytes(const Dims& dm, int64_t nq) {
+  return (size_t)dm.Hkv * nq * (dm.Ks > 0 ? dm.Ks : 1) * sizeof(int32_t);
+}
+
+// Queries [q_begin, q_end) of the call; slot layout over tiles
+// [lay_tau0, lay_tau0 + lay_ntiles) with capG slots per group.
+int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begin, int64_t q_end,
+                             int32_t* sel, int64_t* union_off, int32_t* union_len,
+                             int32_t* union_blk, uint64_t* union_mask, int64_t union_cap,
+                             int64_t lay_tau0, int64_t lay_ntiles, int64_t capG,
+                             int32_t* status, cudaStream_t st) {
+  if (q_end <= q_begin) return SGQA_OK;
+  TUArgs a;
+  a.scores = scores;
+  a.nq = q_end - q_begin;
+  a.q_begin = q_begin;
+  a.q_end = q_end;
+  a.T = dm.T;
+  a.off = dm.off;
+  a.nblk = dm.nblk;
+  a.B = dm.B;
+  a.Ks = dm.Ks;
+  a.W = dm.W;
+  a.sel = sel;
+  a.uoff = union_off;
+  a.ulen = union_len;
+  a.ublk = union_blk;
+  a.umask = union_mask;
+  a.ucap = union_cap;
+  a.lay_tau0 = lay_tau0;
+  a.lay_ntiles = lay_ntiles;
+  a.capG = capG;
+  a.tau_begin = q_begin / dm.W;
+  a.nwords = (int)((dm.nblk + 31) / 32);
+  a.status = status;
+  const int64_t tau_end = (q_end + dm.W - 1) / dm.W;
+  const size_t fixed = (size_t)(((a.nwords + 3) & ~3) + ((a.nwords + 1 + 3) & ~3)) * 4;
+  const size_t budget = 200 * 1024;
+  if (fixed + WARP_BYTES > budget) return SGQA_ERR_UNSUPPORTED;
+  int nw = (int)((budget - fixed) / WARP_BYTES);
+  if (nw > 16) nw = 16;
+  if (nw > dm.W) nw = dm.W < 1 ? 1 : dm.W;
+  if (nw < 1) nw = 1;
+  a.nw = nw;
+  const size_t smem = fixed + (size_t)nw * WARP_BYTES;
+  if (cudaFuncSetAttribute(k_topk_union, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return SGQA_ERR_CUDA;
+  dim3 grid((unsigned)(tau_end - a.tau_begin), (unsigned)dm.Hkv);
+  log_begin(SGQA_K_TOPK_UNION, st);
+  k_topk_union<<<grid, nw * 32, smem, st>>>(a);
+  log_end(st);
+  return cudaGetLastError() == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA;
+}
+
+int launch_topk_union(const Dims& dm, const float* scores, int64_t q_begin, int64_t q_end,
+                      int32_t* sel, int64_t* union_off, int32_t* union_len, int32_t* union_blk,
+                      uint64_t* union_mask, int64_t union_cap, int32_t* status, cudaStream_t st) {
+  return launch_topk_union_layout(dm, scores, q_begin, q_end, sel, union_off, union_len,
+                                  union_blk, union_mask, union_cap, 0, dm.ntiles, group_cap(dm),
+                                  status, st);
+}
+
+}  // namespace sgqa

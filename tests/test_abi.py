@@ -1,0 +1,116 @@
+"""Host-only checks of the C ABI: the library loads without a GPU, exports
+every entry point include/sgqa.h declares, and rejects bad arguments on the
+host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from block_sparse_long_sgqa_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def s():
+    from block_sparse_long_sgqa_gb300 import sgqa
+
+    return sgqa
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "sgqa.h")).read()
+    return sorted(set(re.findall(r"SGQA_API\s+[\w\s\*]+?\b(sgqa_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(s):
+    decl = declared_symbols()
+    assert len(decl) >= 11
+    for name in decl:
+        assert hasattr(s._lib, name), name
+    assert set(decl) == set(s.EXPORTED)
+
+
+def test_version_and_strings(s):
+    assert s.version() == 100
+    assert s.status_string(0) == "ok"
+    for c in range(1, 9):
+        assert s.status_string(c) not in ("ok", "unknown status")
+    assert s.status_string(99) == "unknown status"
+
+
+def p_small(s, **kw):
+    base = dict(seq_q=300, seq_kv=300, q_offset=0, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                block_size=8, topk_tokens=64, tile_q=64)
+    base.update(kw)
+    return s.params(**base)
+
+
+def test_workspace_and_capacity(s):
+    p = p_small(s)
+    for w in (s.WS_INDEX_SCORES, s.WS_TOPK_UNION, s.WS_PREFILL):
+        assert s.workspace_bytes(p, w) > 0
+    assert s.workspace_bytes(p, 99) == 0
+    assert s.workspace_bytes(p_small(s, seq_q=0), s.WS_PREFILL) == 0
+    # capacity: sum over groups and tiles of min(|tile| * k/B, nh(last query))
+    T, W, B, Ks, Hkv = 300, 64, 8, 8, 2
+    exp = 0
+    for tau in range((T + W - 1) // W):
+        n = min(W, T - tau * W)
+        exp += min(n * Ks, (tau * W + n - 1) // B)
+    assert s.union_capacity(p) == exp * Hkv
+    assert s.union_capacity(p_small(s, n_q_heads=7)) == -1
+
+
+def test_capacity_bounds_oracle_union(s):
+    """The oracle's union of a random selection never exceeds the capacity."""
+    import numpy as np
+
+    wl = synth.WORKLOADS["gqa_32k"].replace(seq_q=200, seq_kv=200, n_q_heads=8, n_kv_heads=2,
+                                            topk_tokens=32, tile_q=16)
+    inp = synth.make_inputs(wl)
+    Q, K, V = (synth.widen(inp[x]) for x in "QKV")
+    rows = np.arange(wl.seq_q)
+    S = oracle.scores(oracle.index_query(Q, 2, rows), oracle.merge_f64(K, 8), 8, 0, rows)
+    sel = oracle.select(S, 8, 0, rows, 4)
+    uoff, ublk, _ = oracle.union(sel, 16, wl.n_blocks)
+    assert len(ublk) <= s.union_capacity(s.params_for(wl))
+
+
+def _call_prefill(s, p, Q=0x1000, K=0x1000, V=0x1000, O=0x1000, lse=0x1000, Kbar=0x1000,
+                  ws=0x1000, ws_bytes=1 << 40, pt=None, kvalid=0):
+    vp = ctypes.c_void_p
+    return s._lib.sgqa_prefill(ctypes.byref(p), vp(Q), vp(K), vp(V), vp(pt) if pt else None,
+                               vp(Kbar), kvalid, vp(O), vp(lse), vp(ws), ws_bytes, None, None)
+
+
+def test_host_validation_codes(s):
+    assert _call_prefill(s, p_small(s, seq_q=0)) == s.ERR_INVALID_ARG
+    assert _call_prefill(s, p_small(s, seq_kv=100)) == s.ERR_INVALID_ARG       # Tkv < off + T
+    assert _call_prefill(s, p_small(s, n_q_heads=7)) == s.ERR_INVALID_ARG
+    assert _call_prefill(s, p_small(s, topk_tokens=60)) == s.ERR_INVALID_ARG    # not a multiple of B
+    assert _call_prefill(s, p_small(s, head_dim=96)) == s.ERR_UNSUPPORTED
+    assert _call_prefill(s, p_small(s, block_size=3, topk_tokens=63)) == s.ERR_UNSUPPORTED
+    assert _call_prefill(s, p_small(s, tile_q=65)) == s.ERR_UNSUPPORTED
+    assert _call_prefill(s, p_small(s, page_size=12, seq_kv=300)) == s.ERR_UNSUPPORTED
+    assert _call_prefill(s, p_small(s), Q=0) == s.ERR_INVALID_ARG               # null pointer
+    assert _call_prefill(s, p_small(s), K=0x1008) == s.ERR_ALIGNMENT
+    assert _call_prefill(s, p_small(s), ws_bytes=16) == s.ERR_WORKSPACE
+    assert _call_prefill(s, p_small(s), kvalid=10**6) == s.ERR_INVALID_ARG
+    # paged layout needs a page table, and a page table needs a paged layout
+    assert _call_prefill(s, p_small(s, page_size=64, seq_kv=320)) == s.ERR_INVALID_ARG
+    assert _call_prefill(s, p_small(s), pt=0x2000) == s.ERR_INVALID_ARG
+
+
+def test_topk_union_range_validation(s):
+    p = p_small(s)
+    vp = ctypes.c_void_p
+    f = s._lib.sgqa_topk_union
+    args = lambda qb, qe, cap: (ctypes.byref(p), vp(0x1000), qb, qe, None, vp(0x1000), vp(0x1000),
+                                vp(0x1000), vp(0x1000), cap, vp(0x1000), 1 << 40, None, None)
+    assert f(*args(10, 64, 1 << 30)) == s.ERR_INVALID_ARG      # q_begin not tile aligned
+    assert f(*args(0, 70, 1 << 30)) == s.ERR_INVALID_ARG       # q_end not tile aligned nor T
+    assert f(*args(0, 301, 1 << 30)) == s.ERR_INVALID_ARG
+    assert f(*args(0, 64, 1)) == s.ERR_WORKSPACE               # union capacity too small

@@ -1,0 +1,157 @@
+"""GPU parity of the fused prefill (sgqa_prefill) against the CPU oracle.
+
+End to end, the GPU's selection may legitimately differ from the fp64 oracle
+at near-ties (rule R2), which changes the attention output of those rows; so
+R3 is applied to the (row, head) pairs whose fp64 selection has a clear
+margin, and R2 is checked on the standalone selection path that the fused
+call is built from.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_long_sgqa_gb300 import synth
+from helpers import clear_margin, dev_inputs, lse_tol_for, r2_check, r3_check, sample_rows, widened
+from test_parity_steps import SMALL, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def s():
+    from block_sparse_long_sgqa_gb300 import sgqa
+
+    return sgqa
+
+
+def run_prefill(s, p, d, kbar=None, kvalid=0):
+    O, lse = s.alloc_outputs(p)
+    Kbar = s.kbar_empty(p) if kbar is None else kbar
+    ws = s.alloc_workspace(p, s.WS_PREFILL)
+    st = s.new_status()
+    s.sgqa_prefill(p, d["Q"], d["K"], d["V"], Kbar, O, lse, ws, page_table=d["page_table"],
+                   kbar_valid_blocks=kvalid, status=st)
+    code, det = s.read_status(st)
+    assert code == 0, (s.status_string(code), det)
+    return O, lse, Kbar
+
+
+def gpu_selection(s, p, d, Kbar, q_begin, q_end):
+    """Standalone GPU path: index scores -> top-k (same kernels as the fused call)."""
+    wl_T = q_end - q_begin
+    nblk = p.seq_kv // p.block_size
+    ws = s.alloc_workspace(p, s.WS_INDEX_SCORES)
+    scores = torch.empty(p.n_kv_heads, wl_T, nblk, device="cuda")
+    s.sgqa_index_scores(p, d["Q"], Kbar, q_begin, q_end, scores, ws)
+    sel = torch.empty(p.n_kv_heads, wl_T, p.topk_tokens // p.block_size, dtype=torch.int32,
+                      device="cuda")
+    uo, ul, ub, um = s.alloc_union(p)
+    st = s.new_status()
+    s.sgqa_topk_union(p, scores, q_begin, q_end, sel, uo, ul, ub, um, status=st)
+    assert s.read_status(st)[0] == 0
+    return sel.cpu().numpy()
+
+
+def check_end_to_end(s, wl, inp, O, lse, rows, Kbar, d):
+    Q, K, V = widened(inp)
+    S, sel_rows, O64, lse64 = oracle.prefill_rows(Q, K, V, wl.q_offset, wl.block_size, wl.k_blocks,
+                                                  rows)
+    clear = clear_margin(S, wl, rows)                       # [Hkv][nrows]
+    G = wl.n_q_heads // wl.n_kv_heads
+    mask = np.repeat(clear.T, G, axis=1)                    # [nrows][H]
+    Og = O.float().cpu().numpy()[rows]
+    lg = lse.cpu().numpy()[:, rows]
+    stats = r3_check(Og, lg, O64, lse64, mask, lse_tol=lse_tol_for(wl, inp, rows))
+    # R2 on the standalone selection of the same rows (contiguous query range)
+    q0, q1 = int(rows.min()) // wl.tile_q * wl.tile_q, wl.seq_q
+    q0 = min(q0, q1)
+    sel = gpu_selection(s, s.params_for(wl), d, Kbar, q0, q1)
+    r2_check(sel[:, rows - q0], S, wl, rows)
+    return stats, float(mask.mean())
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_prefill_end_to_end(s, name):
+    wl, inp = SMALL[name], inputs(name)
+    p = s.params_for(wl)
+    d = dev_inputs(inp)
+    O, lse, Kbar = run_prefill(s, p, d)
+    rows = np.arange(wl.seq_q, dtype=np.int32)
+    _, frac = check_end_to_end(s, wl, inp, O, lse, rows, Kbar, d)
+    assert frac > 0.9
+
+
+def test_prefill_mode_full(s):
+    wl, inp = SMALL["b8"], inputs("b8")
+    p = s.params_for(wl, union_mode=1)
+    d = dev_inputs(inp)
+    O, lse, _ = run_prefill(s, p, d)
+    Q, K, V = widened(inp)
+    rows = np.arange(wl.seq_q, dtype=np.int32)
+    S = oracle.scores(oracle.index_query(Q, wl.n_kv_heads, rows), oracle.merge_f64(K, 8), 8,
+                      wl.q_offset, rows)
+    sel = oracle.select(S, 8, wl.q_offset, rows, wl.k_blocks)
+    O64, lse64 = oracle.sparse_attn(Q, K, V, wl.q_offset, 8, sel, mode=1, W=wl.tile_q)
+    # a near-tie anywhere in a tile can change that tile's union: compare tiles whose
+    # rows all have a clear margin
+    clear = clear_margin(S, wl, rows)
+    tiles_ok = np.array([clear[:, i // wl.tile_q * wl.tile_q:(i // wl.tile_q + 1) * wl.tile_q].all()
+                         for i in rows])
+    G = wl.n_q_heads // wl.n_kv_heads
+    mask = np.repeat(tiles_ok[:, None], wl.n_q_heads, axis=1)
+    r3_check(O.float().cpu().numpy(), lse.cpu().numpy(), O64, lse64, mask)
+
+
+def test_paged_equals_contiguous_bitexact(s):
+    wl = SMALL["paged"]
+    inp = inputs("paged")
+    p = s.params_for(wl)
+    O1, l1, _ = run_prefill(s, p, dev_inputs(inp))
+    wl2 = wl.replace(page_size=0)
+    p2 = s.params_for(wl2)
+    inp2 = dict(inp, workload=wl2)
+    O2, l2, _ = run_prefill(s, p2, dev_inputs(inp2))
+    assert torch.equal(O1, O2) and torch.equal(l1, l2)
+
+
+def test_chunked_prefill_bitexact(s):
+    """Two calls (first half, then second half reusing the block-key cache)
+    equal one call, bit for bit."""
+    wl = SMALL["b8"]
+    inp = inputs("b8")
+    d = dev_inputs(inp)
+    p = s.params_for(wl)
+    O, lse, Kbar_full = run_prefill(s, p, d)
+    half = (wl.seq_q // 2) // wl.tile_q * wl.tile_q
+    # call 1: queries [0, half) with the KV prefix up to their last position
+    wl1 = wl.replace(seq_q=half, seq_kv=wl.q_offset + half)
+    p1 = s.params_for(wl1)
+    d1 = dict(d, Q=d["Q"][:half].contiguous(), K=d["K"][:wl1.seq_kv].contiguous(),
+              V=d["V"][:wl1.seq_kv].contiguous())
+    O1, l1, Kb1 = run_prefill(s, p1, d1)
+    # call 2: the rest, with the cached block keys of call 1
+    wl2 = wl.replace(seq_q=wl.seq_q - half, q_offset=wl.q_offset + half)
+    p2 = s.params_for(wl2)
+    Kbar = s.kbar_empty(p2)
+    Kbar[:, :Kb1.shape[1]] = Kb1
+    d2 = dict(d, Q=d["Q"][half:].contiguous())
+    O2, l2, Kb2 = run_prefill(s, p2, d2, kbar=Kbar, kvalid=Kb1.shape[1])
+    assert torch.equal(Kb2, Kbar_full)
+    assert torch.equal(torch.cat([O1, O2]), O)
+    assert torch.equal(torch.cat([l1, l2], dim=1), lse)
+
+
+@pytest.mark.parametrize("name", ["gqa_32k"])
+def test_prefill_full_size_sampled(s, name):
+    """The 32K workload at full size, in the launch configuration the benchmark
+    times; sampled rows against the oracle."""
+    wl = synth.WORKLOADS[name]
+    inp = synth.make_inputs(wl)
+    p = s.params_for(wl)
+    d = dev_inputs(inp)
+    O, lse, Kbar = run_prefill(s, p, d)
+    rows = sample_rows(wl.seq_q, wl.tile_q, 48, seed=1)
+    rows = rows[rows >= wl.seq_q - 4096]  # one contiguous range for the standalone selection
+    _, frac = check_end_to_end(s, wl, inp, O, lse, rows, Kbar, d)
+    assert frac > 0.8
