@@ -30,7 +30,8 @@ UNION_MASKED, UNION_FULL = 0, 1
 WS_INDEX_SCORES, WS_TOPK_UNION, WS_SPARSE_ATTN, WS_PREFILL = 1, 2, 3, 4
 
 EXPORTED = ("sgqa_workspace_bytes", "sgqa_union_capacity", "sgqa_block_merge", "sgqa_index_scores",
-            "sgqa_topk_union", "sgqa_sparse_attn_fwd", "sgqa_prefill", "sgqa_prefill_plan",
+            "sgqa_topk_union", "sgqa_topk_union_noalloc", "sgqa_sparse_attn_fwd", "sgqa_prefill",
+            "sgqa_prefill_plan",
             "sgqa_set_launch_log", "sgqa_reset_status", "sgqa_read_status", "sgqa_status_string",
             "sgqa_version")
 K_MERGE, K_SPLIT, K_INDEX_QUERY, K_INDEX_SCORES, K_TOPK_UNION, K_ATTN, K_STAGE = 1, 2, 3, 4, 5, 6, 7
@@ -68,6 +69,7 @@ _lib.sgqa_union_capacity.restype = _i64
 _lib.sgqa_block_merge.argtypes = [_P, _vp, _vp, _i32, _i32, _vp, _vp, _vp]
 _lib.sgqa_index_scores.argtypes = [_P, _vp, _vp, _i32, _i32, _vp, _vp, _sz, _vp, _vp]
 _lib.sgqa_topk_union.argtypes = [_P, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _sz, _vp, _vp]
+_lib.sgqa_topk_union_noalloc.argtypes = [_P, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp]
 _lib.sgqa_sparse_attn_fwd.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                       _vp, _vp]
 _lib.sgqa_prefill.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp, _vp]
@@ -78,7 +80,8 @@ _lib.sgqa_read_status.argtypes = [_vp, ctypes.POINTER(_i32), _vp]
 _lib.sgqa_status_string.argtypes = [ctypes.c_int]
 _lib.sgqa_status_string.restype = ctypes.c_char_p
 _lib.sgqa_version.restype = ctypes.c_int
-for _f in ("sgqa_block_merge", "sgqa_index_scores", "sgqa_topk_union", "sgqa_sparse_attn_fwd",
+for _f in ("sgqa_block_merge", "sgqa_index_scores", "sgqa_topk_union", "sgqa_topk_union_noalloc",
+           "sgqa_sparse_attn_fwd",
            "sgqa_prefill", "sgqa_prefill_plan", "sgqa_set_launch_log", "sgqa_reset_status",
            "sgqa_read_status"):
     getattr(_lib, _f).restype = ctypes.c_int
@@ -167,6 +170,15 @@ def sgqa_topk_union(p, scores, q_begin, q_end, topk_idx, union_off, union_len, u
                                 union_blk.numel(), _ptr(ws),
                                 0 if ws is None else ws.numel() * ws.element_size(), _ptr(status),
                                 _stream(stream)), "sgqa_topk_union")
+
+
+def sgqa_topk_union_noalloc(p, scores, q_begin, q_end, union_off, union_len, union_blk,
+                            union_mask, status=None, stream=None):
+    """Top-k + union with the library's fixed scratch array (no workspace)."""
+    _check(_lib.sgqa_topk_union_noalloc(ctypes.byref(p), _ptr(scores), q_begin, q_end,
+                                        _ptr(union_off), _ptr(union_len), _ptr(union_blk),
+                                        _ptr(union_mask), union_blk.numel(), _ptr(status),
+                                        _stream(stream)), "sgqa_topk_union_noalloc")
 
 
 def sgqa_sparse_attn_fwd(p, Q, K, V, union_off, union_len, union_blk, union_mask, O, lse,

@@ -184,6 +184,27 @@ SGQA_API int sgqa_sparse_attn_fwd(const sgqa_params* p, const void* Q, const voi
                                   float* lse, void* ws, size_t ws_bytes, int32_t* status,
                                   sgqa_stream_t stream);
 
+/* Top-k and tile union without a workspace, for callers that cannot
+ * allocate device memory (code running inside another framework's memory
+ * pool, serving loops whose device memory is carved once up front, runtimes
+ * with a fixed memory plan).  The pages have no counterpart: this is an
+ * interface variant of sgqa_topk_union, with the same inputs, outputs and
+ * results, whose per-query selection lists live in a library-owned static
+ * device array of 2^21 int32 entries (8 MiB, held by every GPU that loads the
+ * library until exit).  topk_idx is not produced.
+ *   - Rejects n_kv_heads * (q_end - q_begin) * (k / B) > 2^21 with
+ *     SGQA_ERR_WORKSPACE (call it on smaller query ranges).
+ *   - Allocates nothing.  The first call on a device looks up the array's
+ *     device address (cudaGetSymbolAddress) with that device current; make
+ *     that first call before any stream capture.
+ *   - All calls share the one array, so calls whose kernels overlap on the GPU
+ *     (different streams, or different host threads) race; serialise them.
+ *     Nothing in the array needs to start at zero. */
+SGQA_API int sgqa_topk_union_noalloc(const sgqa_params* p, const float* scores, int32_t q_begin,
+                                     int32_t q_end, int64_t* union_off, int32_t* union_len,
+                                     int32_t* union_blk, uint64_t* union_mask, int64_t union_cap,
+                                     int32_t* status, sgqa_stream_t stream);
+
 /* Steps 1-6 fused into one enqueue: merge -> index scores -> top-k -> union ->
  * attention, chunked over queries so that intermediates stay within the
  * workspace.  Kbar is a caller-owned block-key cache [Hkv][nblk] fp32: blocks
