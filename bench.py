@@ -52,6 +52,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--seq", type=int, default=None,
+                    help="shrink the workload to this many queries (profiling small cases)")
     return ap.parse_args(argv)
 
 
@@ -314,6 +316,8 @@ def main(argv=None):
     from block_sparse_long_sgqa_gb300 import synth
 
     wl = synth.WORKLOADS[args.workload]
+    if args.seq:
+        wl = wl.replace(seq_q=args.seq, seq_kv=wl.q_offset + args.seq)
     if args.impl == "reference":
         line = run_reference(args, wl, rank)
         if line is not None:
