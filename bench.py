@@ -136,7 +136,7 @@ class ClockSampler:
                  "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(1.0)  # let nvidia-smi attach before the timed region starts
         return self
 
     def __exit__(self, *exc):

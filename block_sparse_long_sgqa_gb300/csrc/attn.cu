@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(224, 1) k_sparse_attn(AttnArgs a) {
         if (last) break;
       }
       umma_commit(mma_done);
-      mbar_wait_drain(mma_done, 0);
+      mbar_wait_drain(mma_done, 0, a.status, 299);
     }
   } else {
     // =============================================================== softmax

@@ -102,12 +102,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
-// Same, without an abort flag: used for the final drain of in-flight copies.
-__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+// Same, without an abort flag: used for the final drain of in-flight copies
+// and MMAs.  A drain that gives up is reported too (detail = where).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
+                                                int32_t* status = nullptr, int where = 0) {
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 63 && globaltimer() - t0 > kWaitLimitNs) return false;
+    if ((i & 63) == 63 && globaltimer() - t0 > kWaitLimitNs) {
+      report(status, SGQA_ERR_TIMEOUT, where);
+      return false;
+    }
   }
 }
 

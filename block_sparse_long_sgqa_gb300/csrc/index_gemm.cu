@@ -112,9 +112,9 @@ __global__ void __launch_bounds__(192, 1)
         ++issued[s];
       }
       if (ab.set()) {  // let every copy this CTA started land before it exits
-        mbar_wait_drain(a_full, 0);
+        mbar_wait_drain(a_full, 0, status, 198);
         for (int s = 0; s < 2; ++s)
-          if (issued[s] > 0) mbar_wait_drain(&b_full[s], (issued[s] - 1) & 1);
+          if (issued[s] > 0) mbar_wait_drain(&b_full[s], (issued[s] - 1) & 1, status, 197);
       }
     }
   } else if (warp == 1) {
@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       umma_commit(mma_done);
-      mbar_wait_drain(mma_done, 0);
+      mbar_wait_drain(mma_done, 0, status, 199);
     }
   } else {
     // --------------------------------------------------------------- epilogue

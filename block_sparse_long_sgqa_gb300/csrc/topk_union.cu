@@ -24,10 +24,13 @@
 namespace sgqa {
 namespace {
 
-constexpr int NB0 = 2048;        // bins of the level-0 and level-1 histograms (11 bits)
-constexpr int CAND_CAP = 1024;   // bucket members kept in shared memory per warp
-constexpr int WARP_BYTES = NB0 * 4 + CAND_CAP * 8;
+constexpr int NB0 = 2048;        // bins of the level-0 histogram (top 11 key bits)
+constexpr int NBR = 512;         // bins of the refinement histograms (9 bits)
+constexpr int WARP_BYTES = NB0 * 4;  // per-warp scratch: level-0 histogram, then
+                                     // bucket candidates + a refinement histogram
+constexpr int CAND_CAP = (WARP_BYTES - NBR * 4) / 8;  // 768 (key, index) pairs
 constexpr unsigned FULL = 0xffffffffu;
+constexpr int BATCH = 8;         // 32-element groups loaded before use
 
 struct TUArgs {
   const float* scores;  // [Hkv][nq][nblk], rows q_begin .. q_end-1 of the call
@@ -109,65 +112,81 @@ __device__ __forceinline__ void zero_hist(uint32_t* hist, int nbins) {
 }
 
 // Histogram of (key >> shift) & (nbins-1) over row keys whose key >> pshift == pval
-// (no filter when pshift == 32).
+// (no filter when pshift == 32).  Loads 8 float4 per lane before using them.
 __device__ void hist_row(const float* __restrict__ row, int64_t nh, bool vec, uint32_t* hist,
                          int shift, int nbins, int pshift, uint32_t pval) {
   const int lane = lane_id();
   const uint32_t bm = nbins - 1;
+  auto add = [&](float v) {
+    const uint32_t key = order_key(v);
+    if (pshift == 32 || (key >> pshift) == pval) atomicAdd(&hist[(key >> shift) & bm], 1u);
+  };
+  int64_t done = 0;
   if (vec) {
     const float4* r4 = reinterpret_cast<const float4*>(row);
     const int64_t n4 = nh / 4;
     int64_t x = lane;
-    for (; x + 7 * 32 < n4; x += 8 * 32) {  // 8 loads in flight per lane
+    for (; x + 7 * 32 < n4; x += 8 * 32) {
       float4 v[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) v[u] = __ldg(r4 + x + u * 32);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t key = order_key(e[k]);
-          if (pshift == 32 || (key >> pshift) == pval) atomicAdd(&hist[(key >> shift) & bm], 1u);
-        }
+        add(v[u].x);
+        add(v[u].y);
+        add(v[u].z);
+        add(v[u].w);
       }
     }
     for (; x < n4; x += 32) {
       const float4 v = __ldg(r4 + x);
-      const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t key = order_key(e[k]);
-        if (pshift == 32 || (key >> pshift) == pval) atomicAdd(&hist[(key >> shift) & bm], 1u);
-      }
+      add(v.x);
+      add(v.y);
+      add(v.z);
+      add(v.w);
     }
-    for (int64_t j = n4 * 4 + lane; j < nh; j += 32) {
-      const uint32_t key = order_key(__ldg(row + j));
-      if (pshift == 32 || (key >> pshift) == pval) atomicAdd(&hist[(key >> shift) & bm], 1u);
-    }
-  } else {
-    for (int64_t j = lane; j < nh; j += 32) {
-      const uint32_t key = order_key(__ldg(row + j));
-      if (pshift == 32 || (key >> pshift) == pval) atomicAdd(&hist[(key >> shift) & bm], 1u);
-    }
+    done = n4 * 4;
   }
+  for (int64_t j = done + lane; j < nh; j += 32) add(__ldg(row + j));
   __syncwarp();
 }
 
-__device__ void hist_cand(const uint32_t* ck, int n, uint32_t* hist, int shift, int nbins,
+__device__ void hist_cand(const uint2* cand, int n, uint32_t* hist, int shift, int nbins,
                           int pshift, uint32_t pval) {
   const uint32_t bm = nbins - 1;
   for (int i = lane_id(); i < n; i += 32) {
-    const uint32_t key = ck[i];
+    const uint32_t key = cand[i].x;
     if ((key >> pshift) == pval) atomicAdd(&hist[(key >> shift) & bm], 1u);
   }
   __syncwarp();
 }
 
+// Visit row elements j = 0 .. nh-1 in ascending order, 32 at a time (lane l
+// gets j = base + l), with BATCH groups of loads in flight.  f(j, valid, key)
+// is called by all lanes for every group.
+template <typename F>
+__device__ __forceinline__ void ordered_pass(const float* __restrict__ row, int64_t nh, F f) {
+  const int lane = lane_id();
+  for (int64_t base = 0; base < nh; base += 32 * BATCH) {
+    uint32_t keys[BATCH];
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int64_t j = base + u * 32 + lane;
+      keys[u] = j < nh ? order_key(__ldg(row + j)) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int64_t j0 = base + u * 32;
+      if (j0 >= nh) break;  // warp-uniform
+      f(j0, j0 + lane < nh, keys[u]);
+    }
+  }
+}
+
 // Select row t of group g, write its ascending list and OR it into the tile
-// bitmask.  Returns nothing; all lanes participate.
-__device__ void select_row(const TUArgs& a, int g, int64_t t, uint32_t* hist, uint32_t* ck,
-                           int32_t* ci, uint32_t* tile_bits) {
+// bitmask.  All lanes participate.
+__device__ void select_row(const TUArgs& a, int g, int64_t t, uint32_t* warp_smem,
+                           uint32_t* tile_bits) {
   const int lane = lane_id();
   const int64_t tl = t - a.q_begin;
   int64_t nh = (a.off + t) / a.B;
@@ -181,10 +200,13 @@ __device__ void select_row(const TUArgs& a, int g, int64_t t, uint32_t* hist, ui
     return;
   }
 
-  bool take_all = (int64_t)need == nh;
+  // The selection is: every key above the threshold prefix Tp (compared on
+  // key >> shift), plus the first `rem` keys equal to it in block order.
+  const bool take_all = (int64_t)need == nh;
   uint32_t Tp = 0, rem = need;
   int shift = 0;
   if (!take_all) {
+    uint32_t* hist = warp_smem;
     uint32_t b, above, cnt;
     zero_hist(hist, NB0);
     hist_row(row, nh, vec, hist, 21, NB0, 32, 0);
@@ -193,67 +215,75 @@ __device__ void select_row(const TUArgs& a, int g, int64_t t, uint32_t* hist, ui
     Tp = b;
     shift = 21;
     if (cnt != rem) {
+      // refine the remaining 21 bits in levels of 9, 9 and 3 bits
+      uint2* cand = reinterpret_cast<uint2*>(warp_smem);          // reuses the histogram
+      uint32_t* rh = warp_smem + CAND_CAP * 2;                     // refinement histogram
       const bool use_cand = cnt <= (uint32_t)CAND_CAP;
       int n = 0;
-      if (use_cand) {  // compact the bucket's members, in block order
-        for (int64_t base = 0; base < nh; base += 32) {
-          const int64_t j = base + lane;
-          const uint32_t key = j < nh ? order_key(__ldg(row + j)) : 0u;
-          const bool in = j < nh && (key >> 21) == b;
+      __syncwarp();
+      if (use_cand) {  // compact the bucket's members (order does not matter here)
+        ordered_pass(row, nh, [&](int64_t j0, bool valid, uint32_t key) {
+          const bool in = valid && (key >> 21) == b;
           const uint32_t m = __ballot_sync(FULL, in);
-          if (in) {
-            const int p = n + __popc(m & lanemask_lt());
-            ck[p] = key;
-            ci[p] = (int32_t)j;
-          }
+          if (in) cand[n + __popc(m & lanemask_lt())] = make_uint2(key, (uint32_t)(j0 + lane));
           n += __popc(m);
-        }
+        });
         __syncwarp();
       }
-      // level 1: bits 20..10
-      zero_hist(hist, NB0);
-      if (use_cand) hist_cand(ck, n, hist, 10, NB0, 21, Tp);
-      else hist_row(row, nh, vec, hist, 10, NB0, 21, Tp);
-      find_bin(hist, NB0, rem, b, above, cnt);
-      rem -= above;
-      Tp = (Tp << 11) | b;
-      shift = 10;
-      if (cnt != rem) {
-        // level 2: bits 9..0
-        zero_hist(hist, 1024);
-        if (use_cand) hist_cand(ck, n, hist, 0, 1024, 10, Tp);
-        else hist_row(row, nh, vec, hist, 0, 1024, 10, Tp);
-        find_bin(hist, 1024, rem, b, above, cnt);
+      const int widths[3] = {9, 9, 3};
+      for (int lv = 0; lv < 3 && cnt != rem; ++lv) {
+        const int w = widths[lv];
+        const int nb = 1 << w;
+        const int nshift = shift - w;
+        zero_hist(rh, nb < 128 ? 128 : nb);
+        if (use_cand) hist_cand(cand, n, rh, nshift, nb, shift, Tp);
+        else hist_row(row, nh, vec, rh, nshift, nb, shift, Tp);
+        if (nb >= 32) {
+          find_bin(rh, nb, rem, b, above, cnt);
+        } else {  // tiny last level: scan serially on every lane
+          uint32_t acc = 0;
+          b = 0;
+          above = 0;
+          cnt = 0;
+          for (int i = nb - 1; i >= 0; --i) {
+            const uint32_t h = rh[i];
+            if (acc + h >= rem) {
+              b = i;
+              above = acc;
+              cnt = h;
+              break;
+            }
+            acc += h;
+          }
+        }
         rem -= above;
-        Tp = (Tp << 10) | b;
-        shift = 0;
+        Tp = (Tp << w) | b;
+        shift = nshift;
+        __syncwarp();
       }
     }
   }
 
   // emission in ascending block order
   uint32_t eq_seen = 0, n_out = 0;
-  for (int64_t base = 0; base < nh; base += 32) {
-    const int64_t j = base + lane;
-    const bool valid = j < nh;
+  ordered_pass(row, nh, [&](int64_t j0, bool valid, uint32_t key) {
     bool take;
     uint32_t meq = 0;
     if (take_all) {
       take = valid;
     } else {
-      const uint32_t kp = valid ? (order_key(__ldg(row + j)) >> shift) : 0u;
-      const bool above = valid && kp > Tp;
+      const uint32_t kp = key >> shift;
       const bool eq = valid && kp == Tp;
       meq = __ballot_sync(FULL, eq);
       const uint32_t rank = eq_seen + __popc(meq & lanemask_lt());
-      take = above || (eq && rank < rem);
+      take = (valid && kp > Tp) || (eq && rank < rem);
     }
     const uint32_t mt = __ballot_sync(FULL, take);
-    if (take) out[n_out + __popc(mt & lanemask_lt())] = (int32_t)j;
-    if (lane == 0 && mt) atomicOr(&tile_bits[base >> 5], mt);
+    if (take) out[n_out + __popc(mt & lanemask_lt())] = (int32_t)(j0 + lane);
+    if (lane == 0 && mt) atomicOr(&tile_bits[j0 >> 5], mt);
     n_out += __popc(mt);
     eq_seen += __popc(meq);
-  }
+  });
   for (int64_t x = n_out + lane; x < a.Ks; x += 32) out[x] = -1;
   if (lane == 0 && n_out != need) report(a.status, SGQA_ERR_BOUNDS, (int)t);
 }
@@ -287,10 +317,8 @@ __global__ void k_topk_union(TUArgs a) {
   // ---- per-row selection
   const int64_t first = tau * a.W;
   int len = (int)((a.T - first) < a.W ? (a.T - first) : a.W);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(wbase + (size_t)warp * WARP_BYTES);
-  uint32_t* ck = hist + NB0;
-  int32_t* ci = reinterpret_cast<int32_t*>(ck + CAND_CAP);
-  for (int i = warp; i < len; i += a.nw) select_row(a, g, first + i, hist, ck, ci, tile_bits);
+  uint32_t* wsm = reinterpret_cast<uint32_t*>(wbase + (size_t)warp * WARP_BYTES);
+  for (int i = warp; i < len; i += a.nw) select_row(a, g, first + i, wsm, tile_bits);
   __syncthreads();
 
   // ---- union list: ranks from a prefix sum of word popcounts
@@ -414,7 +442,7 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
   const size_t budget = 200 * 1024;
   if (fixed + WARP_BYTES > budget) return SGQA_ERR_UNSUPPORTED;
   int nw = (int)((budget - fixed) / WARP_BYTES);
-  if (nw > 16) nw = 16;
+  if (nw > 8) nw = 8;  // 8 warps and ~70 KB: three CTAs share an SM
   if (nw > dm.W) nw = dm.W < 1 ? 1 : dm.W;
   if (nw < 1) nw = 1;
   a.nw = nw;
