@@ -98,7 +98,7 @@ static int64_t caps_between(const Dims& dm, int64_t tau0, int64_t tau1) {
 int64_t group_cap(const Dims& dm) { return caps_between(dm, 0, dm.ntiles); }
 
 // ------------------------------------------------------------------ TMA encode
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -114,7 +114,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
-  auto fn = encode_fn();
+  auto fn = tmap_encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_bytes};

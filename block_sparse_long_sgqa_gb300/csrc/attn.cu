@@ -15,14 +15,20 @@
 // sub-tile's first current block, followed by the sub-tile's current blocks.
 // Keys are gathered 128 per stage.
 //
-// Warps 0-1 build each stage's block list and gather K/V rows into 128-byte
-// swizzled shared tiles with cp.async; warp 2 issues S = Q K^T into a
-// double-buffered TMEM tile and O += P V into a TMEM accumulator; warps 3-6
-// hold one row each: they read S from TMEM, apply the per-query block mask
-// and the causal cut of the current block, run the fp32 online softmax
-// (rescaling O in TMEM only when the running maximum grows by more than 2^8),
-// write P (bf16) to shared memory for the PV product, and finally normalise
-// O and write O and the log-sum-exp.
+// Roles (7 warps):
+//  warp 0   builds each stage's block list from the union entries (a 4-deep
+//           ring) and issues the K loads: one TMA box per (block, 64-wide
+//           head-dim half) for B >= 8, a cp.async row gather for B < 8;
+//  warp 1   issues the V loads;
+//  warp 2   one thread issues S = Q K^T into a double-buffered TMEM tile
+//           (K slots are released as soon as their QK product is done) and
+//           O += P V into the TMEM accumulator (V as an MN-major operand);
+//  warps 3-6 one query-head row per thread: read S from TMEM, apply the
+//           per-query block masks (the causal cut only on current blocks), run
+//           the fp32 online softmax in base 2 (O is rescaled in TMEM only when
+//           the running maximum grows by more than 2^8), write P (bf16) to
+//           shared memory, and finally normalise O and write O and the
+//           log-sum-exp.
 #include "common.cuh"
 #include "internal.h"
 
@@ -31,32 +37,39 @@ namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
 
-template <int D>
+template <int NBPS>
+struct MetaT {         // one stage's block list
+  int32_t nb;          // blocks in the stage
+  int32_t last;        // last stage of the work item
+  int32_t blk[NBPS];
+  uint64_t mask[NBPS]; // bit qi: query qi of the sub-tile may attend the block
+};
+
+template <int D, int B>
 struct AttnCfg {
   static constexpr int BM = 128;  // rows per MMA
   static constexpr int KB = 128;  // keys per stage
-  static constexpr int S = 2;     // K/V stages
+  static constexpr int NBPS = KB / B;
+  static constexpr bool TMA = B >= 8;  // blocks are whole 8-row swizzle atoms
+  static constexpr int SK = TMA ? 3 : 2;  // K slots
+  static constexpr int SV = 2;            // V slots
+  static constexpr int NM = 4;            // stage block-list slots
+  static constexpr int KC = D / 64;
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_TILE = KB * D * 2;
   static constexpr int P_BYTES = BM * KB * 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + S * KV_TILE;
-  static constexpr int OFF_P = OFF_V + S * KV_TILE;
+  static constexpr int OFF_V = OFF_K + SK * KV_TILE;
+  static constexpr int OFF_P = OFF_V + SV * KV_TILE;
   static constexpr int OFF_META = OFF_P + P_BYTES;
-  static constexpr int OFF_BAR = OFF_META + S * 1552;  // sizeof(Meta) rounded
+  static constexpr int META_BYTES = (int)((sizeof(MetaT<NBPS>) + 15) / 16 * 16);
+  static constexpr int OFF_BAR = OFF_META + NM * META_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;  // S[2] at 0 / 128, O at 256
   static constexpr int NTHREADS = 224;
+  static_assert(SMEM <= 232448, "shared memory plan");
 };
-
-struct Meta {          // one stage's block list
-  int32_t nb;          // blocks in the stage
-  int32_t last;        // last stage of the work item
-  int32_t blk[128];
-  uint64_t mask[128];  // bit qi: query qi of the sub-tile may attend the block
-};
-static_assert(sizeof(Meta) <= 1552, "meta size");
 
 struct AttnArgs {
   const __nv_bfloat16* Q;
@@ -70,7 +83,7 @@ struct AttnArgs {
   void* O;
   float* lse;
   int64_t T, Tkv, off, nblk, lay_tau0, lay_ntiles, tau_begin, tau_end;
-  int H, Hkv, G, B, W, ps, QS, nsub, mode, out_f32;
+  int H, Hkv, G, B, W, ps, QS, nsub, mode, out_f32, npages;
   float scale_log2;
   int32_t* status;
 };
@@ -111,6 +124,7 @@ struct Gen {
 };
 
 // Fill `m` with up to nbps blocks.  Warp-cooperative (warp 0).
+template <typename Meta>
 __device__ void gen_stage(const AttnArgs& a, Gen& gs, Meta& m, int nbps, int sh, uint64_t qmask) {
   const int lane = lane_id();
   int n = 0;
@@ -163,12 +177,10 @@ __device__ void gen_stage(const AttnArgs& a, Gen& gs, Meta& m, int nbps, int sh,
     if (lane == 0) {
       while (n < nbps && nd <= gs.c_last) {
         while (cur < gs.end && a.ublk[cur] < nd) ++cur;
-        const uint64_t um = (cur < gs.end && a.ublk[cur] == nd) ? a.umask[cur] : 0ull;
-        uint64_t sub;
-        if (a.mode == SGQA_UNION_MASKED)
-          sub = (um >> sh) & qmask;
-        else
-          sub = (cur < gs.end && a.ublk[cur] == nd) ? ~0ull : 0ull;
+        const bool in_u = cur < gs.end && a.ublk[cur] == nd;
+        const uint64_t um = in_u ? a.umask[cur] : 0ull;
+        const uint64_t sub =
+            a.mode == SGQA_UNION_MASKED ? ((um >> sh) & qmask) : (in_u ? ~0ull : 0ull);
         m.blk[n] = (int32_t)nd;
         m.mask[n] = sub;
         ++n;
@@ -197,26 +209,54 @@ __device__ __forceinline__ const __nv_bfloat16* kv_row(const AttnArgs& a, const 
   return base + (p * a.Hkv + g) * (int64_t)D;
 }
 
+// TMA load of block b (B rows, one 64-wide head-dim half c) of KV head g into
+// dst.  b < 0 selects an out-of-range box: the copy writes zeros.
+template <int B>
+__device__ __forceinline__ void tma_block(const AttnArgs& a, const CUtensorMap* map, void* dst,
+                                          uint64_t* bar, int c, int g, int64_t b) {
+  if (a.ps > 0) {
+    int32_t page = a.npages, inpage = 0;  // page index npages: out of range
+    if (b >= 0) {
+      const int64_t p = b * B;
+      page = a.page_table[p / a.ps];
+      inpage = (int32_t)(p % a.ps);
+    }
+    tma_load_4d(dst, map, bar, c * 64, inpage, g, page);
+  } else {
+    const int32_t row = b >= 0 ? (int32_t)(b * B) : (int32_t)((a.Tkv + B - 1) / B * B + B);
+    tma_load_3d(dst, map, bar, c * 64, g, row);
+  }
+}
+
 template <int D, int B>
-__global__ void __launch_bounds__(224, 1) k_sparse_attn(AttnArgs a) {
-  using C = AttnCfg<D>;
-  constexpr int NBPS = C::KB / B;  // blocks per stage
+__global__ void __launch_bounds__(224, 1)
+    k_sparse_attn(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                  const __grid_constant__ CUtensorMap mv, AttnArgs a) {
+  using C = AttnCfg<D, B>;
+  using Meta = MetaT<C::NBPS>;
+  constexpr int NBPS = C::NBPS;  // blocks per stage
+  constexpr bool kTma = C::TMA;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Meta* meta = reinterpret_cast<Meta*>(smem + C::OFF_META);
+  auto meta_at = [&](int i) -> Meta& {
+    return *reinterpret_cast<Meta*>(smem + C::OFF_META + i * C::META_BYTES);
+  };
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;    // [S]
-  uint64_t* kv_empty = bars + 3;   // [S]
-  uint64_t* meta_rdy = bars + 5;   // [S]
-  uint64_t* s_full = bars + 7;     // [2]
-  uint64_t* s_empty = bars + 9;    // [2]
-  uint64_t* p_full = bars + 11;
-  uint64_t* p_empty = bars + 12;
-  uint64_t* mma_done = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
-  int* abort_flag = reinterpret_cast<int*>(bars + 15);
+  uint64_t* k_full = bars + 1;     // [SK]
+  uint64_t* k_empty = bars + 4;    // [SK]
+  uint64_t* v_full = bars + 7;     // [SV]
+  uint64_t* v_empty = bars + 9;    // [SV]
+  uint64_t* m_full = bars + 11;    // [NM]
+  uint64_t* m_empty = bars + 15;   // [NM]
+  uint64_t* s_full = bars + 19;    // [2]
+  uint64_t* s_empty = bars + 21;   // [2]
+  uint64_t* p_full = bars + 23;
+  uint64_t* p_empty = bars + 24;
+  uint64_t* mma_done = bars + 25;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 26);
+  int* abort_flag = reinterpret_cast<int*>(bars + 27);
 
   // ---- work item
   const int64_t item = blockIdx.x;
@@ -228,16 +268,24 @@ __global__ void __launch_bounds__(224, 1) k_sparse_attn(AttnArgs a) {
   const int64_t tile_len = (a.T - tile_first) < a.W ? (a.T - tile_first) : a.W;
   if ((int64_t)s * a.QS >= tile_len) return;  // uniform exit: empty sub-tile
   const int64_t tq0 = tile_first + (int64_t)s * a.QS;
-  const int nq_sub = (int)((tile_len - (int64_t)s * a.QS) < a.QS ? (tile_len - (int64_t)s * a.QS) : a.QS);
+  const int nq_sub =
+      (int)((tile_len - (int64_t)s * a.QS) < a.QS ? (tile_len - (int64_t)s * a.QS) : a.QS);
   const int rows = nq_sub * a.G;
   const int warp = warp_id(), lane = lane_id();
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 128);
-    for (int i = 0; i < C::S; ++i) {
-      mbar_init(&kv_full[i], 128);
-      mbar_init(&kv_empty[i], 1);
-      mbar_init(&meta_rdy[i], 1);
+    mbar_init(q_full, 1);
+    for (int i = 0; i < C::SK; ++i) {
+      mbar_init(&k_full[i], kTma ? 1 : 64);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < C::SV; ++i) {
+      mbar_init(&v_full[i], kTma ? 1 : 64);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < C::NM; ++i) {
+      mbar_init(&m_full[i], 1);
+      mbar_init(&m_empty[i], 5);  // 4 softmax warps + the V producer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -256,23 +304,17 @@ __global__ void __launch_bounds__(224, 1) k_sparse_attn(AttnArgs a) {
   const uint32_t tmem = *tmem_slot;
   const Abort ab{abort_flag};
 
-  if (warp < 2) {
-    // ============================================================== producer
-    const int pt = threadIdx.x;  // 0..63
-    uint8_t* sQ = smem + C::OFF_Q;
-    for (int idx = pt; idx < C::BM * (D / 8); idx += 64) {
-      const int r = idx / (D / 8), c = idx % (D / 8);
-      uint8_t* dst = sQ + (c >> 3) * (C::BM * 128) + sw128(r, c & 7);
-      if (r < rows) {
-        const int qi = r / a.G, h = r % a.G;
-        cp_async16(dst, a.Q + ((tq0 + qi) * a.H + (int64_t)g * a.G + h) * D + c * 8);
-      } else {
-        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-      }
+  if (warp == 0) {
+    // ================================================ block lists + K loads
+    if (lane == 0) {
+      tma_prefetch_desc(&mq);
+      tma_prefetch_desc(&mk);
+      // the Q box is G x QS rows (fewer than 128 when a sub-tile cannot fill M)
+      mbar_expect_tx(q_full, (uint32_t)(C::KC * 128 * a.G * a.QS));
+      for (int c = 0; c < C::KC; ++c)  // box (64, G, QS) lands as rows qi * G + h
+        tma_load_3d(smem + C::OFF_Q + c * (C::BM * 128), &mq, q_full, c * 64, g * a.G,
+                    (int32_t)tq0);
     }
-    mbar_arrive(q_full);
-    cp_async_arrive(q_full);
-
     Gen gs;
     const int64_t lt = (int64_t)g * a.lay_ntiles + (tau - a.lay_tau0);
     gs.cur = a.uoff[lt];
@@ -283,39 +325,98 @@ __global__ void __launch_bounds__(224, 1) k_sparse_attn(AttnArgs a) {
     gs.phase = 0;
     const int sh = s * a.QS;
     const uint64_t qmask = nq_sub >= 64 ? ~0ull : ((1ull << nq_sub) - 1ull);
-
+    int issued_k[C::SK] = {};
     for (int i = 0;; ++i) {
-      const int st = i % C::S;
-      const uint32_t ph = (uint32_t)((i / C::S) & 1);
-      if (!mbar_wait(&kv_empty[st], ph ^ 1u, ab, a.status, 201)) break;
-      Meta& m = meta[st];
-      if (warp == 0) {
-        gen_stage(a, gs, m, NBPS, sh, qmask);
-        if (lane == 0) mbar_arrive(&meta_rdy[st]);
-      } else {
-        if (!mbar_wait(&meta_rdy[st], ph, ab, a.status, 202)) break;
-      }
-      const int nkeys = m.nb * B;
-      const int last = m.last;
-      uint8_t* sK = smem + C::OFF_K + st * C::KV_TILE;
-      uint8_t* sV = smem + C::OFF_V + st * C::KV_TILE;
-      for (int idx = pt; idx < C::KB * (D / 8); idx += 64) {
-        const int k = idx / (D / 8), c = idx % (D / 8);
-        const uint32_t o = (c >> 3) * (C::KB * 128) + sw128(k, c & 7);
-        const int64_t p = k < nkeys ? (int64_t)m.blk[k / B] * B + (k % B) : a.Tkv;
-        if (p < a.Tkv) {  // a partial current block ends at the last key
-          cp_async16(sK + o, kv_row<D>(a, a.K, g, p) + c * 8);
-          cp_async16(sV + o, kv_row<D>(a, a.V, g, p) + c * 8);
-        } else {
-          *reinterpret_cast<uint4*>(sK + o) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(sV + o) = make_uint4(0, 0, 0, 0);
+      const int ms = i % C::NM, ks = i % C::SK;
+      bool w = mbar_wait(&m_empty[ms], (uint32_t)(((i / C::NM) & 1) ^ 1), ab, a.status, 201);
+      if (!__all_sync(FULL, w)) break;
+      Meta& m = meta_at(ms);
+      gen_stage(a, gs, m, NBPS, sh, qmask);
+      if (lane == 0) mbar_arrive(&m_full[ms]);
+      w = mbar_wait(&k_empty[ks], (uint32_t)(((i / C::SK) & 1) ^ 1), ab, a.status, 202);
+      if (!__all_sync(FULL, w)) break;
+      uint8_t* sK = smem + C::OFF_K + ks * C::KV_TILE;
+      if constexpr (kTma) {
+        if (lane == 0) {
+          mbar_expect_tx(&k_full[ks], C::KV_TILE);
+          for (int bs = 0; bs < NBPS; ++bs) {
+            const int64_t b = bs < m.nb ? (int64_t)m.blk[bs] : -1;
+            for (int c = 0; c < C::KC; ++c)
+              tma_block<B>(a, &mk, sK + c * (C::KB * 128) + bs * (B * 128), &k_full[ks], c, g, b);
+          }
+          ++issued_k[ks];
         }
+      } else {
+        const int nkeys = m.nb * B;
+        for (int idx = lane; idx < C::KB * (D / 8); idx += 32) {
+          const int k = idx / (D / 8), c = idx % (D / 8);
+          const uint32_t o = (c >> 3) * (C::KB * 128) + sw128(k, c & 7);
+          const int64_t p = k < nkeys ? (int64_t)m.blk[k / B] * B + (k % B) : a.Tkv;
+          if (p < a.Tkv)
+            cp_async16(sK + o, kv_row<D>(a, a.K, g, p) + c * 8);
+          else
+            *reinterpret_cast<uint4*>(sK + o) = make_uint4(0, 0, 0, 0);
+        }
+        mbar_arrive(&k_full[ks]);
+        cp_async_arrive(&k_full[ks]);
       }
-      mbar_arrive(&kv_full[st]);
-      cp_async_arrive(&kv_full[st]);
+      if (m.last) break;
+    }
+    if constexpr (kTma) {
+      if (lane == 0 && ab.set()) {  // let in-flight copies land before the CTA exits
+        mbar_wait_drain(q_full, 0, a.status, 291);
+        for (int k = 0; k < C::SK; ++k)
+          if (issued_k[k] > 0) mbar_wait_drain(&k_full[k], (issued_k[k] - 1) & 1, a.status, 292);
+      }
+    } else {
+      cp_async_wait_all();
+    }
+  } else if (warp == 1) {
+    // ============================================================= V loads
+    int issued_v[C::SV] = {};
+    for (int i = 0;; ++i) {
+      const int ms = i % C::NM, vs = i % C::SV;
+      bool w = mbar_wait(&m_full[ms], (uint32_t)((i / C::NM) & 1), ab, a.status, 203) &&
+               mbar_wait(&v_empty[vs], (uint32_t)(((i / C::SV) & 1) ^ 1), ab, a.status, 204);
+      if (!__all_sync(FULL, w)) break;
+      const Meta& m = meta_at(ms);
+      const bool last = m.last != 0;
+      uint8_t* sV = smem + C::OFF_V + vs * C::KV_TILE;
+      if constexpr (kTma) {
+        if (lane == 0) {
+          mbar_expect_tx(&v_full[vs], C::KV_TILE);
+          for (int bs = 0; bs < NBPS; ++bs) {
+            const int64_t b = bs < m.nb ? (int64_t)m.blk[bs] : -1;
+            for (int c = 0; c < C::KC; ++c)
+              tma_block<B>(a, &mv, sV + c * (C::KB * 128) + bs * (B * 128), &v_full[vs], c, g, b);
+          }
+          ++issued_v[vs];
+        }
+      } else {
+        const int nkeys = m.nb * B;
+        for (int idx = lane; idx < C::KB * (D / 8); idx += 32) {
+          const int k = idx / (D / 8), c = idx % (D / 8);
+          const uint32_t o = (c >> 3) * (C::KB * 128) + sw128(k, c & 7);
+          const int64_t p = k < nkeys ? (int64_t)m.blk[k / B] * B + (k % B) : a.Tkv;
+          if (p < a.Tkv)
+            cp_async16(sV + o, kv_row<D>(a, a.V, g, p) + c * 8);
+          else
+            *reinterpret_cast<uint4*>(sV + o) = make_uint4(0, 0, 0, 0);
+        }
+        mbar_arrive(&v_full[vs]);
+        cp_async_arrive(&v_full[vs]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m_empty[ms]);
       if (last) break;
     }
-    cp_async_wait_all();
+    if constexpr (kTma) {
+      if (lane == 0 && ab.set())
+        for (int k = 0; k < C::SV; ++k)
+          if (issued_v[k] > 0) mbar_wait_drain(&v_full[k], (issued_v[k] - 1) & 1, a.status, 293);
+    } else {
+      cp_async_wait_all();
+    }
   } else if (warp == 2) {
     // ============================================================ MMA issuer
     if (lane == 0) {
@@ -324,17 +425,18 @@ __global__ void __launch_bounds__(224, 1) k_sparse_attn(AttnArgs a) {
       const uint32_t sQ = smem_u32(smem + C::OFF_Q);
       const uint32_t sP = smem_u32(smem + C::OFF_P);
       const uint32_t tO = tmem + 256;
-      bool ok = mbar_wait(q_full, 0, ab, a.status, 203);
-      fence_proxy_async_smem();
-      // S_j = Q K_j^T into TMEM buffer j % 2
-      auto issue_qk = [&](int j) -> bool {
-        const int st = j % C::S;
-        if (!mbar_wait(&kv_full[st], (uint32_t)((j / C::S) & 1), ab, a.status, 204)) return false;
-        fence_proxy_async_smem();
-        if (!mbar_wait(&s_empty[j & 1], (uint32_t)(((j >> 1) & 1) ^ 1), ab, a.status, 205))
+      bool ok = mbar_wait(q_full, 0, ab, a.status, 205);
+      // S_j = Q K_j^T into TMEM buffer j % 2; returns the stage's `last` flag
+      auto issue_qk = [&](int j, bool& last) -> bool {
+        const int ks = j % C::SK;
+        if (!mbar_wait(&m_full[j % C::NM], (uint32_t)((j / C::NM) & 1), ab, a.status, 206) ||
+            !mbar_wait(&k_full[ks], (uint32_t)((j / C::SK) & 1), ab, a.status, 207) ||
+            !mbar_wait(&s_empty[j & 1], (uint32_t)(((j >> 1) & 1) ^ 1), ab, a.status, 208))
           return false;
+        last = meta_at(j % C::NM).last != 0;
+        if (!kTma) fence_proxy_async_smem();  // cp.async writes -> tensor-core reads
         tc_fence_after();
-        const uint32_t sK = smem_u32(smem + C::OFF_K + st * C::KV_TILE);
+        const uint32_t sK = smem_u32(smem + C::OFF_K + ks * C::KV_TILE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
@@ -343,16 +445,21 @@ __global__ void __launch_bounds__(224, 1) k_sparse_attn(AttnArgs a) {
                    sdesc_sw128(sK + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[j & 1]);
+        umma_commit(&k_empty[ks]);  // the K slot is free once this product is done
         return true;
       };
-      if (ok) ok = issue_qk(0);
+      bool last_i = false;
+      if (ok) ok = issue_qk(0, last_i);
       for (int i = 0; ok; ++i) {
-        const int st = i % C::S;
-        const bool last = meta[st].last != 0;
-        if (!last && !issue_qk(i + 1)) break;
-        if (!mbar_wait(p_full, (uint32_t)(i & 1), ab, a.status, 206)) break;
+        bool last_next = false;
+        if (!last_i && !issue_qk(i + 1, last_next)) break;
+        const int vs = i % C::SV;
+        if (!mbar_wait(p_full, (uint32_t)(i & 1), ab, a.status, 209) ||
+            !mbar_wait(&v_full[vs], (uint32_t)((i / C::SV) & 1), ab, a.status, 210))
+          break;
+        if (!kTma) fence_proxy_async_smem();
         tc_fence_after();
-        const uint32_t sV = smem_u32(smem + C::OFF_V + st * C::KV_TILE);
+        const uint32_t sV = smem_u32(smem + C::OFF_V + vs * C::KV_TILE);
 #pragma unroll
         for (int kk = 0; kk < C::KB / 16; ++kk) {
           const uint32_t poff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
@@ -361,8 +468,9 @@ __global__ void __launch_bounds__(224, 1) k_sparse_attn(AttnArgs a) {
                    (i > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(p_empty);
-        umma_commit(&kv_empty[st]);
-        if (last) break;
+        umma_commit(&v_empty[vs]);
+        if (last_i) break;
+        last_i = last_next;
       }
       umma_commit(mma_done);
       mbar_wait_drain(mma_done, 0, a.status, 299);
@@ -376,18 +484,20 @@ __global__ void __launch_bounds__(224, 1) k_sparse_attn(AttnArgs a) {
     const int64_t t = tq0 + qi;
     const int64_t pos = a.off + t;
     const int64_t cur = pos / B;
+    const int64_t c0 = (a.off + tq0) / B;  // first current block of the sub-tile
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const float ninf = -__int_as_float(0x7f800000);
+    const float sl2 = a.scale_log2;
     uint8_t* sP = smem + C::OFF_P;
     float m_used = ninf, l = 0.0f;
     int i = 0;
     bool ok = true;
     for (;; ++i) {
-      const int st = i % C::S;
+      const int ms = i % C::NM;
       // waits are polled per thread but their outcome is made warp-uniform:
       // the tcgen05.ld/st below are warp-collective
-      bool w = mbar_wait(&s_full[i & 1], (uint32_t)((i >> 1) & 1), ab, a.status, 207) &&
-               mbar_wait(&kv_full[st], (uint32_t)((i / C::S) & 1), ab, a.status, 208);
+      bool w = mbar_wait(&s_full[i & 1], (uint32_t)((i >> 1) & 1), ab, a.status, 211) &&
+               mbar_wait(&m_full[ms], (uint32_t)((i / C::NM) & 1), ab, a.status, 212);
       if (!__all_sync(FULL, w)) {
         ok = false;
         break;
@@ -400,27 +510,33 @@ __global__ void __launch_bounds__(224, 1) k_sparse_attn(AttnArgs a) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[i & 1]);
-      const Meta& m = meta[st];
+      const Meta& m = meta_at(ms);
       const int nb = m.nb;
       const bool last = m.last != 0;
-      // mask and running maximum (log2 units)
+      // per-block masks: a historical block is attended iff the query's bit is
+      // set; a current block (>= c0) also needs the causal cut inside it
       float smax = ninf;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int bs = 0; bs < NBPS; ++bs) {
+        const int64_t b = bs < nb ? (int64_t)m.blk[bs] : -1;
+        const bool sel = b >= 0 && row_ok && ((m.mask[bs] >> qi) & 1ull) && b < cur;
+        if (b < c0) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int k = cc * 32 + e;
-          const int bs = k / B;
-          bool allowed = false;
-          if (row_ok && bs < nb) {
-            const int64_t b = m.blk[bs];
-            const bool hist_ok = ((m.mask[bs] >> qi) & 1ull) && b < cur;
-            const bool cur_ok = b == cur && (b * B + (k % B)) <= pos;
-            allowed = hist_ok || cur_ok;
+          for (int e = 0; e < B; ++e) {
+            const int k = bs * B + e;
+            const float x = sel ? __uint_as_float(sv[k >> 5][k & 31]) * sl2 : ninf;
+            sv[k >> 5][k & 31] = __float_as_uint(x);
+            smax = fmaxf(smax, x);
           }
-          const float x = allowed ? __uint_as_float(sv[cc][e]) * a.scale_log2 : ninf;
-          sv[cc][e] = __float_as_uint(x);
-          smax = fmaxf(smax, x);
+        } else {
+#pragma unroll
+          for (int e = 0; e < B; ++e) {
+            const int k = bs * B + e;
+            const bool ok2 = sel || (row_ok && b == cur && b * B + e <= pos);
+            const float x = ok2 ? __uint_as_float(sv[k >> 5][k & 31]) * sl2 : ninf;
+            sv[k >> 5][k & 31] = __float_as_uint(x);
+            smax = fmaxf(smax, x);
+          }
         }
       }
       // Raise the reference maximum when this stage exceeds it by more than 2^8.
@@ -430,7 +546,7 @@ __global__ void __launch_bounds__(224, 1) k_sparse_attn(AttnArgs a) {
       const bool raise = smax > m_used + 8.0f;
       const bool rescale = raise && m_used != ninf;
       if (__any_sync(FULL, rescale)) {
-        bool w2 = mbar_wait(p_empty, (uint32_t)((i - 1) & 1), ab, a.status, 209);
+        bool w2 = mbar_wait(p_empty, (uint32_t)((i - 1) & 1), ab, a.status, 213);
         if (!__all_sync(FULL, w2)) {
           ok = false;
           break;
@@ -450,7 +566,9 @@ __global__ void __launch_bounds__(224, 1) k_sparse_attn(AttnArgs a) {
         l *= f;
       }
       if (raise) m_used = smax;
-      // probabilities -> bf16 pairs
+      // probabilities -> bf16 pairs.  Masked keys hold -inf and give 0; a row
+      // with nothing allowed so far has m_used = -inf and subtracts 0 instead.
+      const float msub = m_used == ninf ? 0.0f : m_used;
       uint32_t pk[64];
       float rs = 0.0f;
 #pragma unroll
@@ -458,15 +576,17 @@ __global__ void __launch_bounds__(224, 1) k_sparse_attn(AttnArgs a) {
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const float x0 = __uint_as_float(sv[cc][e]), x1 = __uint_as_float(sv[cc][e + 1]);
-          const float p0 = x0 == ninf ? 0.0f : ex2(x0 - m_used);
-          const float p1 = x1 == ninf ? 0.0f : ex2(x1 - m_used);
+          const float p0 = ex2(x0 - msub);
+          const float p1 = ex2(x1 - msub);
           rs += p0 + p1;
           pk[(cc * 32 + e) / 2] = pack_bf16x2(p0, p1);
         }
       }
       l += rs;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m_empty[ms]);  // done with this stage's block list
       if (i > 0) {
-        bool w3 = mbar_wait(p_empty, (uint32_t)((i - 1) & 1), ab, a.status, 210);
+        bool w3 = mbar_wait(p_empty, (uint32_t)((i - 1) & 1), ab, a.status, 214);
         if (!__all_sync(FULL, w3)) {
           ok = false;
           break;
@@ -486,7 +606,7 @@ __global__ void __launch_bounds__(224, 1) k_sparse_attn(AttnArgs a) {
       if (last) break;
     }
     // ---- epilogue: O / l and the log-sum-exp
-    bool fin = ok && mbar_wait(p_empty, (uint32_t)(i & 1), ab, a.status, 211);
+    bool fin = ok && mbar_wait(p_empty, (uint32_t)(i & 1), ab, a.status, 215);
     if (__all_sync(FULL, fin)) {
       tc_fence_after();
       const float inv = row_ok && l > 0.0f ? 1.0f / l : 0.0f;
@@ -530,26 +650,74 @@ __global__ void __launch_bounds__(224, 1) k_sparse_attn(AttnArgs a) {
   }
 }
 
+// Tensor maps for Q [T][H][d] (box 64 x G x QS) and K/V: contiguous
+// [Tkv][Hkv][d] (box 64 x 1 x B) or paged [pages][Hkv][ps][d] (box 64 x B x 1 x 1).
+bool make_maps(const Dims& dm, int QS, const void* Q, const void* K, const void* V,
+               CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv) {
+  auto fn = tmap_encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t e = 2;
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)dm.d, (cuuint64_t)dm.H, (cuuint64_t)dm.T};
+    cuuint64_t str[2] = {dm.d * e, (cuuint64_t)dm.H * dm.d * e};
+    cuuint32_t box[3] = {64, (cuuint32_t)dm.G, (cuuint32_t)QS};
+    if (fn(mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(Q), dims, str, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  const int Bb = dm.B >= 8 ? dm.B : 8;  // unused for B < 8 (cp.async gather)
+  for (int w = 0; w < 2; ++w) {
+    CUtensorMap* m = w == 0 ? mk : mv;
+    void* base = const_cast<void*>(w == 0 ? K : V);
+    CUresult r;
+    if (dm.ps > 0) {
+      const cuuint64_t npages = dm.Tkv / dm.ps;
+      cuuint64_t dims[4] = {(cuuint64_t)dm.d, (cuuint64_t)dm.ps, (cuuint64_t)dm.Hkv, npages};
+      cuuint64_t str[3] = {dm.d * e, (cuuint64_t)dm.ps * dm.d * e,
+                           (cuuint64_t)dm.Hkv * dm.ps * dm.d * e};
+      cuuint32_t box[4] = {64, (cuuint32_t)Bb, 1, 1};
+      r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, str, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+      cuuint64_t dims[3] = {(cuuint64_t)dm.d, (cuuint64_t)dm.Hkv, (cuuint64_t)dm.Tkv};
+      cuuint64_t str[2] = {dm.d * e, (cuuint64_t)dm.Hkv * dm.d * e};
+      cuuint32_t box[3] = {64, 1, (cuuint32_t)Bb};
+      r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, str, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) return false;
+  }
+  return true;
+}
+
 template <int D, int B>
-int launch_db(const AttnArgs& a, int64_t items, cudaStream_t st) {
-  using C = AttnCfg<D>;
+int launch_db(const Dims& dm, const AttnArgs& a, const void* Q, const void* K, const void* V,
+              int64_t items, cudaStream_t st) {
+  using C = AttnCfg<D, B>;
+  CUtensorMap mq, mk, mv;
+  if (!make_maps(dm, a.QS, Q, K, V, &mq, &mk, &mv)) return SGQA_ERR_CUDA;
   if (cudaFuncSetAttribute(k_sparse_attn<D, B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM) != cudaSuccess)
     return SGQA_ERR_CUDA;
   log_begin(SGQA_K_ATTN, st);
-  k_sparse_attn<D, B><<<(unsigned)items, C::NTHREADS, C::SMEM, st>>>(a);
+  k_sparse_attn<D, B><<<(unsigned)items, C::NTHREADS, C::SMEM, st>>>(mq, mk, mv, a);
   log_end(st);
   return cudaGetLastError() == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA;
 }
 
 template <int D>
-int launch_d(const AttnArgs& a, int B, int64_t items, cudaStream_t st) {
-  switch (B) {
-    case 1: return launch_db<D, 1>(a, items, st);
-    case 2: return launch_db<D, 2>(a, items, st);
-    case 4: return launch_db<D, 4>(a, items, st);
-    case 8: return launch_db<D, 8>(a, items, st);
-    case 16: return launch_db<D, 16>(a, items, st);
+int launch_d(const Dims& dm, const AttnArgs& a, const void* Q, const void* K, const void* V,
+             int64_t items, cudaStream_t st) {
+  switch (dm.B) {
+    case 1: return launch_db<D, 1>(dm, a, Q, K, V, items, st);
+    case 2: return launch_db<D, 2>(dm, a, Q, K, V, items, st);
+    case 4: return launch_db<D, 4>(dm, a, Q, K, V, items, st);
+    case 8: return launch_db<D, 8>(dm, a, Q, K, V, items, st);
+    case 16: return launch_db<D, 16>(dm, a, Q, K, V, items, st);
     default: return SGQA_ERR_UNSUPPORTED;
   }
 }
@@ -589,6 +757,7 @@ int launch_sparse_attn_layout(const Dims& dm, const __nv_bfloat16* Q, const __nv
   a.B = dm.B;
   a.W = dm.W;
   a.ps = dm.ps;
+  a.npages = dm.ps > 0 ? (int)(dm.Tkv / dm.ps) : 0;
   a.QS = 128 / dm.G < dm.W ? 128 / dm.G : dm.W;
   a.nsub = (dm.W + a.QS - 1) / a.QS;
   a.mode = dm.mode;
@@ -596,8 +765,8 @@ int launch_sparse_attn_layout(const Dims& dm, const __nv_bfloat16* Q, const __nv
   a.scale_log2 = dm.scale * 1.4426950408889634f;
   a.status = status;
   const int64_t items = (tau_end - tau_begin) * dm.Hkv * a.nsub;
-  if (dm.d == 128) return launch_d<128>(a, dm.B, items, st);
-  if (dm.d == 64) return launch_d<64>(a, dm.B, items, st);
+  if (dm.d == 128) return launch_d<128>(dm, a, Q, K, V, items, st);
+  if (dm.d == 64) return launch_d<64>(dm, a, Q, K, V, items, st);
   return SGQA_ERR_UNSUPPORTED;
 }
 

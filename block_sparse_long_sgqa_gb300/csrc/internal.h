@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include "sgqa.h"
@@ -34,6 +35,10 @@ inline int64_t nh_of(const Dims& dm, int64_t t) {
 // Union slot capacity of tile tau of one group, and of one whole group.
 int64_t tile_cap(const Dims& dm, int64_t tau);
 int64_t group_cap(const Dims& dm);
+
+// cuTensorMapEncodeTiled, fetched once through the runtime's driver entry
+// point (so the library does not link the driver); nullptr if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn();
 
 // Encode a tiled TMA descriptor (2-D, 128-byte swizzle, bf16) through the
 // driver entry point; returns false on failure.
