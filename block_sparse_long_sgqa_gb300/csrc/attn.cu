@@ -121,7 +121,18 @@ struct Gen {
   int64_t cur, end;  // cursor into the tile's union entries
   int64_t c0, c_last, nd;
   int phase;         // 0: historical union entries, 1: current blocks, 2: done
+  int64_t pf_at;     // chunk start of the prefetched entries (-1: none)
+  int32_t pf_b;      // this lane's prefetched entry pf_at + lane
+  uint64_t pf_m;
 };
+
+// Load entry `idx` of the union list (lane-strided chunk), or a sentinel.
+__device__ __forceinline__ void union_entry(const AttnArgs& a, int64_t idx, int64_t end,
+                                            int32_t& b, uint64_t& m) {
+  const bool valid = idx < end;
+  b = valid ? a.ublk[idx] : 0x7fffffff;
+  m = valid ? a.umask[idx] : 0ull;
+}
 
 // Fill `m` with up to nbps blocks.  Warp-cooperative (warp 0).
 template <typename Meta>
@@ -135,8 +146,14 @@ __device__ void gen_stage(const AttnArgs& a, Gen& gs, Meta& m, int nbps, int sh,
     }
     const int64_t idx = gs.cur + lane;
     const bool valid = idx < gs.end;
-    const int32_t b = valid ? a.ublk[idx] : 0x7fffffff;
-    const uint64_t um = valid ? a.umask[idx] : 0ull;
+    int32_t b;
+    uint64_t um;
+    if (gs.pf_at == gs.cur) {  // the chunk was prefetched by the previous step
+      b = gs.pf_b;
+      um = gs.pf_m;
+    } else {
+      union_entry(a, idx, gs.end, b, um);
+    }
     const bool hist = valid && b < gs.c0;
     const uint64_t sub = a.mode == SGQA_UNION_MASKED ? ((um >> sh) & qmask) : ~0ull;
     const uint32_t nonhist = __ballot_sync(FULL, !hist);
@@ -170,6 +187,9 @@ __device__ void gen_stage(const AttnArgs& a, Gen& gs, Meta& m, int nbps, int sh,
       n += room;
       gs.cur += last_lane + 1;
     }
+    // start loading the chunk the next step will read
+    gs.pf_at = gs.cur;
+    union_entry(a, gs.cur + lane, gs.end, gs.pf_b, gs.pf_m);
   }
   __syncwarp();
   if (gs.phase == 1 && n < nbps) {
@@ -323,6 +343,7 @@ __global__ void __launch_bounds__(224, 1)
     gs.c_last = (a.off + tq0 + nq_sub - 1) / B;
     gs.nd = gs.c0;
     gs.phase = 0;
+    gs.pf_at = -1;
     const int sh = s * a.QS;
     const uint64_t qmask = nq_sub >= 64 ? ~0ull : ((1ull << nq_sub) - 1ull);
     int issued_k[C::SK] = {};
@@ -503,42 +524,53 @@ __global__ void __launch_bounds__(224, 1)
         break;
       }
       tc_fence_after();
-      uint32_t sv[4][32];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tl + (i & 1) * 128 + cc * 32, sv[cc]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[i & 1]);
       const Meta& m = meta_at(ms);
       const int nb = m.nb;
       const bool last = m.last != 0;
-      // per-block masks: a historical block is attended iff the query's bit is
-      // set; a current block (>= c0) also needs the causal cut inside it
-      float smax = ninf;
-#pragma unroll
-      for (int bs = 0; bs < NBPS; ++bs) {
-        const int64_t b = bs < nb ? (int64_t)m.blk[bs] : -1;
-        const bool sel = b >= 0 && row_ok && ((m.mask[bs] >> qi) & 1ull) && b < cur;
-        if (b < c0) {
-#pragma unroll
-          for (int e = 0; e < B; ++e) {
-            const int k = bs * B + e;
-            const float x = sel ? __uint_as_float(sv[k >> 5][k & 31]) * sl2 : ninf;
-            sv[k >> 5][k & 31] = __float_as_uint(x);
-            smax = fmaxf(smax, x);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < B; ++e) {
-            const int k = bs * B + e;
-            const bool ok2 = sel || (row_ok && b == cur && b * B + e <= pos);
-            const float x = ok2 ? __uint_as_float(sv[k >> 5][k & 31]) * sl2 : ninf;
-            sv[k >> 5][k & 31] = __float_as_uint(x);
-            smax = fmaxf(smax, x);
+      // Allowed keys of this row in this stage as a 128-bit mask: a whole block
+      // when the query selected it (bit qi of the block's mask) and it is
+      // historical, the causal prefix of the query's own block, nothing else.
+      uint32_t allow[4] = {0u, 0u, 0u, 0u};
+      if (row_ok) {
+#pragma unroll 4
+        for (int bs = 0; bs < nb; ++bs) {
+          const int64_t b = m.blk[bs];
+          int lim = 0;
+          if (((m.mask[bs] >> qi) & 1ull) && b < cur)
+            lim = B;
+          else if (b == cur)
+            lim = (int)(pos - b * B + 1);
+          if (lim > 0) {
+            const int k0 = bs * B;
+            const uint32_t bits = lim >= 32 ? 0xffffffffu : ((1u << lim) - 1u);
+            const uint32_t sh2 = (uint32_t)(k0 & 31);
+            const uint32_t wv = bits << sh2;
+            const int wi = k0 >> 5;
+            allow[0] |= wi == 0 ? wv : 0u;
+            allow[1] |= wi == 1 ? wv : 0u;
+            allow[2] |= wi == 2 ? wv : 0u;
+            allow[3] |= wi == 3 ? wv : 0u;
           }
         }
       }
+      const uint32_t sbase = tl + (i & 1) * 128;
+      // pass 1: masked, scaled maximum over the stage (32 keys per TMEM load)
+      float mx0 = ninf, mx1 = ninf, mx2 = ninf, mx3 = ninf;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(sbase + cc * 32, v);
+        tmem_wait_ld();
+        const uint32_t am = cc == 0 ? allow[0] : cc == 1 ? allow[1] : cc == 2 ? allow[2] : allow[3];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          mx0 = fmaxf(mx0, ((am >> e) & 1u) ? __uint_as_float(v[e]) : ninf);
+          mx1 = fmaxf(mx1, ((am >> (e + 1)) & 1u) ? __uint_as_float(v[e + 1]) : ninf);
+          mx2 = fmaxf(mx2, ((am >> (e + 2)) & 1u) ? __uint_as_float(v[e + 2]) : ninf);
+          mx3 = fmaxf(mx3, ((am >> (e + 3)) & 1u) ? __uint_as_float(v[e + 3]) : ninf);
+        }
+      }
+      const float smax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
       // Raise the reference maximum when this stage exceeds it by more than 2^8.
       // O holds contributions under the old maximum, so it is rescaled once
       // PV_{i-1} is done; the whole warp takes that path together (rows that do
@@ -553,7 +585,7 @@ __global__ void __launch_bounds__(224, 1)
         }
         tc_fence_after();
         const float f = rescale ? ex2(m_used - smax) : 1.0f;
-#pragma unroll
+#pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t ov[32];
           tmem_ld32(tl + 256 + cc * 32, ov);
@@ -566,25 +598,7 @@ __global__ void __launch_bounds__(224, 1)
         l *= f;
       }
       if (raise) m_used = smax;
-      // probabilities -> bf16 pairs.  Masked keys hold -inf and give 0; a row
-      // with nothing allowed so far has m_used = -inf and subtracts 0 instead.
-      const float msub = m_used == ninf ? 0.0f : m_used;
-      uint32_t pk[64];
-      float rs = 0.0f;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float x0 = __uint_as_float(sv[cc][e]), x1 = __uint_as_float(sv[cc][e + 1]);
-          const float p0 = ex2(x0 - msub);
-          const float p1 = ex2(x1 - msub);
-          rs += p0 + p1;
-          pk[(cc * 32 + e) / 2] = pack_bf16x2(p0, p1);
-        }
-      }
-      l += rs;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&m_empty[ms]);  // done with this stage's block list
+      // P buffer is free once PV_{i-1} is done
       if (i > 0) {
         bool w3 = mbar_wait(p_empty, (uint32_t)((i - 1) & 1), ab, a.status, 214);
         if (!__all_sync(FULL, w3)) {
@@ -592,13 +606,40 @@ __global__ void __launch_bounds__(224, 1)
           break;
         }
       }
-      // P row r: keys 8u..8u+7 of chunk c at unit u (swizzled)
+      // pass 2: probabilities p = 2^(s * scale * log2(e) - m), bf16, into P.
+      // A row with nothing allowed so far has m_used = -inf and writes zeros.
+      const float msub = m_used == ninf ? 0.0f : m_used;
+      float rs0 = 0.0f, rs1 = 0.0f;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(sbase + cc * 32, v);
+        tmem_wait_ld();
+        const uint32_t am = cc == 0 ? allow[0] : cc == 1 ? allow[1] : cc == 2 ? allow[2] : allow[3];
+        uint32_t pk[16];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int c = u >> 3;
-        uint4 v = make_uint4(pk[u * 4 + 0], pk[u * 4 + 1], pk[u * 4 + 2], pk[u * 4 + 3]);
-        *reinterpret_cast<uint4*>(sP + c * (C::BM * 128) + sw128(r, u & 7)) = v;
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = ((am >> e) & 1u) ? ex2(fmaf(__uint_as_float(v[e]), sl2, -msub)) : 0.0f;
+          const float p1 =
+              ((am >> (e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -msub)) : 0.0f;
+          rs0 += p0;
+          rs1 += p1;
+          pk[e >> 1] = pack_bf16x2(p0, p1);
+        }
+        // keys cc*32 .. cc*32+31 are 16-byte units 4*(cc&1) .. +3 of chunk cc>>1
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 vv = make_uint4(pk[u * 4 + 0], pk[u * 4 + 1], pk[u * 4 + 2], pk[u * 4 + 3]);
+          *reinterpret_cast<uint4*>(sP + (cc >> 1) * (C::BM * 128) +
+                                    sw128(r, (cc & 1) * 4 + u)) = vv;
+        }
       }
+      l += rs0 + rs1;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[i & 1]);  // S buffer read twice, now free
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m_empty[ms]);  // done with this stage's block list
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
