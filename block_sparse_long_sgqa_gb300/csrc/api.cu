@@ -17,7 +17,8 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
                              int64_t lay_tau0, int64_t lay_ntiles, int64_t capG,
                              int32_t* status, cudaStream_t st);
 int launch_sparse_attn_layout(const Dims& dm, const __nv_bfloat16* Q, const __nv_bfloat16* K,
-                              const __nv_bfloat16* V, const int32_t* page_table,
+                              const __nv_bfloat16* V, const __nv_bfloat16* Kp,
+                              const __nv_bfloat16* Vp, const int32_t* page_table,
                               const int64_t* union_off, const int32_t* union_len,
                               const int32_t* union_blk, const uint64_t* union_mask, void* O,
                               float* lse, int64_t tau_begin, int64_t tau_end, int64_t lay_tau0,
@@ -176,12 +177,16 @@ IndexWs carve_index(Carve& c, const Dims& dm, int64_t nq) {
 }
 
 struct AttnWs {
-  __nv_bfloat16 *Q, *K, *V;  // bf16 copies of fp32 inputs (null for bf16 inputs)
+  __nv_bfloat16 *Q, *K, *V;  // bf16 copies of fp32 inputs (null when not needed)
+  __nv_bfloat16 *Kp, *Vp;    // block-packed K/V for B >= 8 (k_kv_pack)
 };
 AttnWs carve_attn(Carve& c, const Dims& dm) {
-  AttnWs w{nullptr, nullptr, nullptr};
-  if (dm.dtype == SGQA_FP32) {
-    w.Q = c.take<__nv_bfloat16>((size_t)dm.T * dm.H * dm.d);
+  AttnWs w{nullptr, nullptr, nullptr, nullptr, nullptr};
+  if (dm.dtype == SGQA_FP32) w.Q = c.take<__nv_bfloat16>((size_t)dm.T * dm.H * dm.d);
+  if (dm.B >= 8) {  // packed copies (converted to bf16 on the way)
+    w.Kp = c.take<__nv_bfloat16>((size_t)kv_pack_elems(dm));
+    w.Vp = c.take<__nv_bfloat16>((size_t)kv_pack_elems(dm));
+  } else if (dm.dtype == SGQA_FP32) {
     w.K = c.take<__nv_bfloat16>((size_t)dm.Tkv * dm.Hkv * dm.d);
     w.V = c.take<__nv_bfloat16>((size_t)dm.Tkv * dm.Hkv * dm.d);
   }
@@ -222,13 +227,31 @@ PrefillWs carve_prefill(Carve& c, const Dims& dm) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA; }
 
-cudaError_t stage_bf16(const Dims& dm, const void* Q, const void* K, const void* V,
-                       const AttnWs& w, cudaStream_t st) {
-  cudaError_t e = launch_to_bf16(static_cast<const float*>(Q), w.Q, dm.T * dm.H * dm.d, st);
-  if (e == cudaSuccess)
-    e = launch_to_bf16(static_cast<const float*>(K), w.K, dm.Tkv * dm.Hkv * dm.d, st);
-  if (e == cudaSuccess)
-    e = launch_to_bf16(static_cast<const float*>(V), w.V, dm.Tkv * dm.Hkv * dm.d, st);
+// Attention operands: fp32 inputs rounded to bf16, and for B >= 8 the
+// block-packed K/V.  Sets q/k/v to the buffers the attention kernel reads.
+cudaError_t stage_attn(const Dims& dm, const void* Q, const void* K, const void* V,
+                       const int32_t* page_table, const AttnWs& w, const __nv_bfloat16** q,
+                       const __nv_bfloat16** k, const __nv_bfloat16** v, cudaStream_t st) {
+  *q = static_cast<const __nv_bfloat16*>(Q);
+  *k = static_cast<const __nv_bfloat16*>(K);
+  *v = static_cast<const __nv_bfloat16*>(V);
+  cudaError_t e = cudaSuccess;
+  if (dm.dtype == SGQA_FP32) {
+    e = launch_to_bf16(static_cast<const float*>(Q), w.Q, dm.T * dm.H * dm.d, st);
+    *q = w.Q;
+    if (dm.B < 8) {
+      if (e == cudaSuccess)
+        e = launch_to_bf16(static_cast<const float*>(K), w.K, dm.Tkv * dm.Hkv * dm.d, st);
+      if (e == cudaSuccess)
+        e = launch_to_bf16(static_cast<const float*>(V), w.V, dm.Tkv * dm.Hkv * dm.d, st);
+      *k = w.K;
+      *v = w.V;
+    }
+  }
+  if (dm.B >= 8) {
+    if (e == cudaSuccess) e = launch_kv_pack(dm, K, page_table, w.Kp, st);
+    if (e == cudaSuccess) e = launch_kv_pack(dm, V, page_table, w.Vp, st);
+  }
   return e;
 }
 
@@ -360,21 +383,15 @@ SGQA_API int sgqa_sparse_attn_fwd(const sgqa_params* p, const void* Q, const voi
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
     return SGQA_ERR_ALIGNMENT;
   const size_t need = sgqa_workspace_bytes(p, SGQA_WS_SPARSE_ATTN);
-  if (dm.dtype == SGQA_FP32 && (ws == nullptr || ws_bytes < need)) return SGQA_ERR_WORKSPACE;
+  if ((dm.dtype == SGQA_FP32 || dm.B >= 8) && (ws == nullptr || ws_bytes < need))
+    return SGQA_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const __nv_bfloat16 *q = static_cast<const __nv_bfloat16*>(Q),
-                      *k = static_cast<const __nv_bfloat16*>(K),
-                      *v = static_cast<const __nv_bfloat16*>(V);
-  if (dm.dtype == SGQA_FP32) {
-    Carve c(align_ws(ws));
-    AttnWs w = carve_attn(c, dm);
-    if (stage_bf16(dm, Q, K, V, w, st) != cudaSuccess) return SGQA_ERR_CUDA;
-    q = w.Q;
-    k = w.K;
-    v = w.V;
-  }
-  return launch_sparse_attn(dm, q, k, v, page_table, union_off, union_len, union_blk, union_mask,
-                            O, lse, 0, dm.ntiles, status, st);
+  Carve c(align_ws(ws));
+  AttnWs w = carve_attn(c, dm);
+  const __nv_bfloat16 *q, *k, *v;
+  if (stage_attn(dm, Q, K, V, page_table, w, &q, &k, &v, st) != cudaSuccess) return SGQA_ERR_CUDA;
+  return launch_sparse_attn(dm, q, k, v, w.Kp, w.Vp, page_table, union_off, union_len, union_blk,
+                            union_mask, O, lse, 0, dm.ntiles, status, st);
 }
 
 SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, const void* V,
@@ -408,15 +425,8 @@ SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, co
       e = launch_split_kbar(part, Kbar + o, w.ix.khi + o, w.ix.klo + o, st);
     }
   }
-  const __nv_bfloat16 *q = static_cast<const __nv_bfloat16*>(Q),
-                      *k = static_cast<const __nv_bfloat16*>(K),
-                      *v = static_cast<const __nv_bfloat16*>(V);
-  if (e == cudaSuccess && dm.dtype == SGQA_FP32) {
-    e = stage_bf16(dm, Q, K, V, w.at, st);
-    q = w.at.Q;
-    k = w.at.K;
-    v = w.at.V;
-  }
+  const __nv_bfloat16 *q, *k, *v;
+  if (e == cudaSuccess) e = stage_attn(dm, Q, K, V, page_table, w.at, &q, &k, &v, st);
   if (e != cudaSuccess) return SGQA_ERR_CUDA;
 
   for (int64_t q0 = 0; q0 < dm.T; q0 += w.chunk) {
@@ -432,8 +442,9 @@ SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, co
     rc = launch_topk_union_layout(dm, w.scores, q0, q1, w.sel, w.uoff, w.ulen, w.ublk, w.umask,
                                   w.ucap, tau0, w.chunk_tiles, w.capG, status, st);
     if (rc != SGQA_OK) return rc;
-    rc = launch_sparse_attn_layout(dm, q, k, v, page_table, w.uoff, w.ulen, w.ublk, w.umask, O,
-                                   lse, tau0, tau1, tau0, w.chunk_tiles, status, st);
+    rc = launch_sparse_attn_layout(dm, q, k, v, w.at.Kp, w.at.Vp, page_table, w.uoff, w.ulen,
+                                   w.ublk, w.umask, O, lse, tau0, tau1, tau0, w.chunk_tiles,
+                                   status, st);
     if (rc != SGQA_OK) return rc;
   }
   return SGQA_OK;
@@ -446,10 +457,12 @@ SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int
   const int64_t chunk = prefill_chunk(dm);
   if (chunk_queries) *chunk_queries = chunk;
   if (launches) {
-    // with an empty block-key cache: merge, fp32 staging, then per chunk the
-    // index query and indexer GEMM (when there are blocks), top-k/union, attention
+    // with an empty block-key cache: merge, operand staging (fp32 rounding,
+    // K/V block packing), then per chunk the index query and indexer GEMM
+    // (when there are blocks), top-k/union and attention
     const int64_t nchunks = (dm.T + chunk - 1) / chunk;
-    int64_t n = (dm.nblk > 0 ? 1 : 0) + (dm.dtype == SGQA_FP32 ? 3 : 0);
+    int64_t n = (dm.nblk > 0 ? 1 : 0) + (dm.dtype == SGQA_FP32 ? (dm.B >= 8 ? 1 : 3) : 0) +
+                (dm.B >= 8 ? 2 : 0);
     n += nchunks * ((dm.nblk > 0 ? 2 : 0) + 2);
     *launches = (int32_t)n;
   }

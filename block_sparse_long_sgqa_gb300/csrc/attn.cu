@@ -17,18 +17,21 @@
 //
 // Roles (7 warps):
 //  warp 0   builds each stage's block list from the union entries (a 4-deep
-//           ring) and issues the K loads: one TMA box per (block, 64-wide
-//           head-dim half) for B >= 8, a cp.async row gather for B < 8;
+//           ring), with each query's selected blocks as a bitmask, and issues
+//           the K loads: for B >= 8 one contiguous bulk copy per block from the
+//           block-packed, pre-swizzled K (see k_kv_pack), for B < 8 a cp.async
+//           row gather from the original layout;
 //  warp 1   issues the V loads;
 //  warp 2   one thread issues S = Q K^T into a double-buffered TMEM tile
 //           (K slots are released as soon as their QK product is done) and
 //           O += P V into the TMEM accumulator (V as an MN-major operand);
-//  warps 3-6 one query-head row per thread: read S from TMEM, apply the
-//           per-query block masks (the causal cut only on current blocks), run
-//           the fp32 online softmax in base 2 (O is rescaled in TMEM only when
-//           the running maximum grows by more than 2^8), write P (bf16) to
-//           shared memory, and finally normalise O and write O and the
-//           log-sum-exp.
+//  warps 3-10 two threads per query-head row, each owning 64 of the stage's
+//           128 keys (and 64 of O's columns): read S from TMEM, apply the
+//           per-query block masks (the causal cut only on current blocks),
+//           exchange partial maxima through shared memory, run the fp32 online
+//           softmax in base 2 (O is rescaled in TMEM only when the running
+//           maximum grows by more than 2^8), write P (bf16) to shared memory,
+//           and finally normalise O and write O and the log-sum-exp.
 #include "common.cuh"
 #include "internal.h"
 
@@ -41,8 +44,11 @@ template <int NBPS>
 struct MetaT {         // one stage's block list
   int32_t nb;          // blocks in the stage
   int32_t last;        // last stage of the work item
+  int32_t diag;        // first slot holding a current block of the sub-tile (or nb)
+  int32_t pad;
   int32_t blk[NBPS];
   uint64_t mask[NBPS]; // bit qi: query qi of the sub-tile may attend the block
+  uint32_t qbits[64];  // bit bs: query qi selected the (historical) block in slot bs
 };
 
 template <int D, int B>
@@ -51,7 +57,7 @@ struct AttnCfg {
   static constexpr int KB = 128;  // keys per stage
   static constexpr int NBPS = KB / B;
   static constexpr bool TMA = B >= 8;  // blocks are whole 8-row swizzle atoms
-  static constexpr int SK = TMA ? 3 : 2;  // K slots
+  static constexpr int SK = 2;            // K slots
   static constexpr int SV = 2;            // V slots
   static constexpr int NM = 4;            // stage block-list slots
   static constexpr int KC = D / 64;
@@ -64,10 +70,11 @@ struct AttnCfg {
   static constexpr int OFF_P = OFF_V + SV * KV_TILE;
   static constexpr int OFF_META = OFF_P + P_BYTES;
   static constexpr int META_BYTES = (int)((sizeof(MetaT<NBPS>) + 15) / 16 * 16);
-  static constexpr int OFF_BAR = OFF_META + NM * META_BYTES;
+  static constexpr int OFF_X = OFF_META + NM * META_BYTES;  // softmax half-row exchange
+  static constexpr int OFF_BAR = OFF_X + (2 * 2 + 2) * BM * 4;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;  // S[2] at 0 / 128, O at 256
-  static constexpr int NTHREADS = 224;
+  static constexpr int NTHREADS = 352;        // 3 pipeline warps + 8 softmax warps
   static_assert(SMEM <= 232448, "shared memory plan");
 };
 
@@ -75,6 +82,9 @@ struct AttnArgs {
   const __nv_bfloat16* Q;
   const __nv_bfloat16* K;
   const __nv_bfloat16* V;
+  const __nv_bfloat16* Kp;  // block-packed K and V (B >= 8)
+  const __nv_bfloat16* Vp;
+  int64_t nblkp;            // packed blocks per head, excluding the zero block
   const int32_t* page_table;
   const int64_t* uoff;
   const int32_t* ulen;
@@ -136,7 +146,8 @@ __device__ __forceinline__ void union_entry(const AttnArgs& a, int64_t idx, int6
 
 // Fill `m` with up to nbps blocks.  Warp-cooperative (warp 0).
 template <typename Meta>
-__device__ void gen_stage(const AttnArgs& a, Gen& gs, Meta& m, int nbps, int sh, uint64_t qmask) {
+__device__ void gen_stage(const AttnArgs& a, Gen& gs, Meta& m, int nbps, int sh, uint64_t qmask,
+                          int nq) {
   const int lane = lane_id();
   int n = 0;
   while (gs.phase == 0 && n < nbps) {
@@ -217,6 +228,22 @@ __device__ void gen_stage(const AttnArgs& a, Gen& gs, Meta& m, int nbps, int sh,
     m.last = gs.phase == 2 ? 1 : 0;
   }
   __syncwarp();
+  if (nbps <= 32) {
+    // per query of the sub-tile: the historical blocks of this stage it
+    // selected (lane = block slot; one ballot per query)
+    const bool inb = lane < n;
+    const int32_t blk = inb ? m.blk[lane] : 0;
+    const uint64_t msk = inb ? m.mask[lane] : 0ull;
+    const uint32_t cur_m = __ballot_sync(FULL, inb && blk >= gs.c0);
+    const int diag = cur_m ? __ffs(cur_m) - 1 : n;
+    const uint32_t hist_m = diag >= 32 ? FULL : ((1u << diag) - 1u);
+    for (int qi = 0; qi < nq; ++qi) {
+      const uint32_t bits = __ballot_sync(FULL, (msk >> qi) & 1ull) & hist_m;
+      if (lane == 0) m.qbits[qi] = bits;
+    }
+    if (lane == 0) m.diag = diag;
+    __syncwarp();
+  }
 }
 
 template <int D>
@@ -229,29 +256,9 @@ __device__ __forceinline__ const __nv_bfloat16* kv_row(const AttnArgs& a, const 
   return base + (p * a.Hkv + g) * (int64_t)D;
 }
 
-// TMA load of block b (B rows, one 64-wide head-dim half c) of KV head g into
-// dst.  b < 0 selects an out-of-range box: the copy writes zeros.
-template <int B>
-__device__ __forceinline__ void tma_block(const AttnArgs& a, const CUtensorMap* map, void* dst,
-                                          uint64_t* bar, int c, int g, int64_t b) {
-  if (a.ps > 0) {
-    int32_t page = a.npages, inpage = 0;  // page index npages: out of range
-    if (b >= 0) {
-      const int64_t p = b * B;
-      page = a.page_table[p / a.ps];
-      inpage = (int32_t)(p % a.ps);
-    }
-    tma_load_4d(dst, map, bar, c * 64, inpage, g, page);
-  } else {
-    const int32_t row = b >= 0 ? (int32_t)(b * B) : (int32_t)((a.Tkv + B - 1) / B * B + B);
-    tma_load_3d(dst, map, bar, c * 64, g, row);
-  }
-}
-
 template <int D, int B>
-__global__ void __launch_bounds__(224, 1)
-    k_sparse_attn(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                  const __grid_constant__ CUtensorMap mv, AttnArgs a) {
+__global__ void __launch_bounds__(352, 1)
+    k_sparse_attn(const __grid_constant__ CUtensorMap mq, AttnArgs a) {
   using C = AttnCfg<D, B>;
   using Meta = MetaT<C::NBPS>;
   constexpr int NBPS = C::NBPS;  // blocks per stage
@@ -275,8 +282,12 @@ __global__ void __launch_bounds__(224, 1)
   uint64_t* p_full = bars + 23;
   uint64_t* p_empty = bars + 24;
   uint64_t* mma_done = bars + 25;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 26);
-  int* abort_flag = reinterpret_cast<int*>(bars + 27);
+  uint64_t* x_bar = bars + 26;     // [2] half-row maxima exchanged
+  uint64_t* l_bar = bars + 28;     // half-row sums exchanged (epilogue)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 29);
+  int* abort_flag = reinterpret_cast<int*>(bars + 30);
+  float* xmax = reinterpret_cast<float*>(smem + C::OFF_X);          // [2 parity][2 half][BM]
+  float* xsum = xmax + 2 * 2 * C::BM;                                 // [2 half][BM]
 
   // ---- work item
   const int64_t item = blockIdx.x;
@@ -305,13 +316,15 @@ __global__ void __launch_bounds__(224, 1)
     }
     for (int i = 0; i < C::NM; ++i) {
       mbar_init(&m_full[i], 1);
-      mbar_init(&m_empty[i], 5);  // 4 softmax warps + the V producer
+      mbar_init(&m_empty[i], 9);  // 8 softmax warps + the V producer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);
+      mbar_init(&s_empty[i], 8);
+      mbar_init(&x_bar[i], 8);
     }
-    mbar_init(p_full, 4);
+    mbar_init(l_bar, 8);
+    mbar_init(p_full, 8);
     mbar_init(p_empty, 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -328,7 +341,6 @@ __global__ void __launch_bounds__(224, 1)
     // ================================================ block lists + K loads
     if (lane == 0) {
       tma_prefetch_desc(&mq);
-      tma_prefetch_desc(&mk);
       // the Q box is G x QS rows (fewer than 128 when a sub-tile cannot fill M)
       mbar_expect_tx(q_full, (uint32_t)(C::KC * 128 * a.G * a.QS));
       for (int c = 0; c < C::KC; ++c)  // box (64, G, QS) lands as rows qi * G + h
@@ -352,21 +364,22 @@ __global__ void __launch_bounds__(224, 1)
       bool w = mbar_wait(&m_empty[ms], (uint32_t)(((i / C::NM) & 1) ^ 1), ab, a.status, 201);
       if (!__all_sync(FULL, w)) break;
       Meta& m = meta_at(ms);
-      gen_stage(a, gs, m, NBPS, sh, qmask);
+      gen_stage(a, gs, m, NBPS, sh, qmask, nq_sub);
       if (lane == 0) mbar_arrive(&m_full[ms]);
       w = mbar_wait(&k_empty[ks], (uint32_t)(((i / C::SK) & 1) ^ 1), ab, a.status, 202);
       if (!__all_sync(FULL, w)) break;
       uint8_t* sK = smem + C::OFF_K + ks * C::KV_TILE;
       if constexpr (kTma) {
-        if (lane == 0) {
-          mbar_expect_tx(&k_full[ks], C::KV_TILE);
-          for (int bs = 0; bs < NBPS; ++bs) {
-            const int64_t b = bs < m.nb ? (int64_t)m.blk[bs] : -1;
-            for (int c = 0; c < C::KC; ++c)
-              tma_block<B>(a, &mk, sK + c * (C::KB * 128) + bs * (B * 128), &k_full[ks], c, g, b);
-          }
-          ++issued_k[ks];
+        // lane bs copies block slot bs (one contiguous packed block each)
+        constexpr uint32_t BLK = B * D * 2;
+        if (lane == 0) mbar_expect_tx(&k_full[ks], C::KV_TILE);
+        __syncwarp();
+        if (lane < NBPS) {
+          const __nv_bfloat16* kg = a.Kp + (int64_t)g * (a.nblkp + 1) * (B * D);
+          const int64_t b = lane < m.nb ? (int64_t)m.blk[lane] : a.nblkp;  // zero block
+          bulk_load(sK + lane * BLK, kg + b * (B * D), BLK, &k_full[ks]);
         }
+        ++issued_k[ks];
       } else {
         const int nkeys = m.nb * B;
         for (int idx = lane; idx < C::KB * (D / 8); idx += 32) {
@@ -404,15 +417,15 @@ __global__ void __launch_bounds__(224, 1)
       const bool last = m.last != 0;
       uint8_t* sV = smem + C::OFF_V + vs * C::KV_TILE;
       if constexpr (kTma) {
-        if (lane == 0) {
-          mbar_expect_tx(&v_full[vs], C::KV_TILE);
-          for (int bs = 0; bs < NBPS; ++bs) {
-            const int64_t b = bs < m.nb ? (int64_t)m.blk[bs] : -1;
-            for (int c = 0; c < C::KC; ++c)
-              tma_block<B>(a, &mv, sV + c * (C::KB * 128) + bs * (B * 128), &v_full[vs], c, g, b);
-          }
-          ++issued_v[vs];
+        constexpr uint32_t BLK = B * D * 2;
+        if (lane == 0) mbar_expect_tx(&v_full[vs], C::KV_TILE);
+        __syncwarp();
+        if (lane < NBPS) {
+          const __nv_bfloat16* vg = a.Vp + (int64_t)g * (a.nblkp + 1) * (B * D);
+          const int64_t b = lane < m.nb ? (int64_t)m.blk[lane] : a.nblkp;
+          bulk_load(sV + lane * BLK, vg + b * (B * D), BLK, &v_full[vs]);
         }
+        ++issued_v[vs];
       } else {
         const int nkeys = m.nb * B;
         for (int idx = lane; idx < C::KB * (D / 8); idx += 32) {
@@ -461,9 +474,13 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
-          const uint32_t koff = (kk >> 2) * (C::KB * 128) + (kk & 3) * 32;
+          // packed stage: 8-key groups every KC KB, head-dim halves 1 KB apart;
+          // gathered stage: halves KB*128 apart, groups every 1 KB
+          const uint32_t koff = kTma ? (kk >> 2) * 1024 + (kk & 3) * 32
+                                     : (kk >> 2) * (C::KB * 128) + (kk & 3) * 32;
+          const uint32_t ksbo = kTma ? C::KC * 1024 : 1024;
           umma_f16(tmem + (j & 1) * 128, sdesc_sw128(sQ + off, 16, 1024),
-                   sdesc_sw128(sK + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                   sdesc_sw128(sK + koff, 16, ksbo), idesc_qk, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[j & 1]);
         umma_commit(&k_empty[ks]);  // the K slot is free once this product is done
@@ -484,8 +501,12 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
         for (int kk = 0; kk < C::KB / 16; ++kk) {
           const uint32_t poff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
-          umma_f16(tO, sdesc_sw128(sP + poff, 16, 1024),
-                   sdesc_sw128(sV + kk * 16 * 128, C::KB * 128, 1024), idesc_pv,
+          // V as an MN-major operand: LBO = stride between head-dim halves,
+          // SBO = stride between 8-key groups
+          const uint64_t vdesc =
+              kTma ? sdesc_sw128(sV + kk * 2 * (C::KC * 1024), 1024, C::KC * 1024)
+                   : sdesc_sw128(sV + kk * 16 * 128, C::KB * 128, 1024);
+          umma_f16(tO, sdesc_sw128(sP + poff, 16, 1024), vdesc, idesc_pv,
                    (i > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(p_empty);
@@ -498,21 +519,22 @@ __global__ void __launch_bounds__(224, 1)
     }
   } else {
     // =============================================================== softmax
-    const int q = warp & 3;
+    const int q = warp & 3;          // TMEM lane quadrant of this warp
+    const int half = (warp - 3) >> 2;  // keys [64 * half, 64 * half + 64) of each stage
     const int r = q * 32 + lane;
     const bool row_ok = r < rows;
     const int qi = r / a.G, h = r % a.G;
     const int64_t t = tq0 + qi;
     const int64_t pos = a.off + t;
     const int64_t cur = pos / B;
-    const int64_t c0 = (a.off + tq0) / B;  // first current block of the sub-tile
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const float ninf = -__int_as_float(0x7f800000);
     const float sl2 = a.scale_log2;
     uint8_t* sP = smem + C::OFF_P;
-    float m_used = ninf, l = 0.0f;
+    float m_used = ninf, l = 0.0f;  // l: this half-row's share of the denominator
     int i = 0;
     bool ok = true;
+    constexpr int BPH = 64 / B < 1 ? 1 : 64 / B;  // blocks per half stage
     for (;; ++i) {
       const int ms = i % C::NM;
       // waits are polled per thread but their outcome is made warp-uniform:
@@ -527,13 +549,29 @@ __global__ void __launch_bounds__(224, 1)
       const Meta& m = meta_at(ms);
       const int nb = m.nb;
       const bool last = m.last != 0;
-      // Allowed keys of this row in this stage as a 128-bit mask: a whole block
-      // when the query selected it (bit qi of the block's mask) and it is
-      // historical, the causal prefix of the query's own block, nothing else.
-      uint32_t allow[4] = {0u, 0u, 0u, 0u};
+      // Allowed keys of this row among this half's 64 keys, as a 64-bit mask:
+      // a whole block when the query selected it (bit qi of the block's mask)
+      // and it is historical, the causal prefix of the query's own block.
+      uint32_t allow0 = 0u, allow1 = 0u;
       if (row_ok) {
-#pragma unroll 4
-        for (int bs = 0; bs < nb; ++bs) {
+        const int bs0 = half * BPH;
+        const int bs1 = min(nb, bs0 + BPH);
+        int bsd = bs0;  // first slot handled block by block
+        if constexpr (kTma) {
+          // historical blocks: the query's bitmask, one bit per block -> B keys
+          const uint32_t hb = (m.qbits[qi] >> bs0) & ((1u << BPH) - 1u);
+          if constexpr (B == 8) {
+            allow0 = ((((hb & 0xFu) * 0x00204081u) & 0x01010101u) * 0xFFu);
+            allow1 = (((((hb >> 4) & 0xFu) * 0x00204081u) & 0x01010101u) * 0xFFu);
+          } else {  // B == 16: four blocks of 16 keys
+            allow0 = ((hb & 1u) ? 0x0000FFFFu : 0u) | ((hb & 2u) ? 0xFFFF0000u : 0u);
+            allow1 = ((hb & 4u) ? 0x0000FFFFu : 0u) | ((hb & 8u) ? 0xFFFF0000u : 0u);
+          }
+          bsd = max(bs0, (int)m.diag);
+        }
+        // current blocks of the sub-tile (and, without the bitmask, every block)
+#pragma unroll 1
+        for (int bs = bsd; bs < bs1; ++bs) {
           const int64_t b = m.blk[bs];
           int lim = 0;
           if (((m.mask[bs] >> qi) & 1ull) && b < cur)
@@ -541,27 +579,23 @@ __global__ void __launch_bounds__(224, 1)
           else if (b == cur)
             lim = (int)(pos - b * B + 1);
           if (lim > 0) {
-            const int k0 = bs * B;
+            const int k0 = bs * B - half * 64;  // key offset within this half
             const uint32_t bits = lim >= 32 ? 0xffffffffu : ((1u << lim) - 1u);
-            const uint32_t sh2 = (uint32_t)(k0 & 31);
-            const uint32_t wv = bits << sh2;
-            const int wi = k0 >> 5;
-            allow[0] |= wi == 0 ? wv : 0u;
-            allow[1] |= wi == 1 ? wv : 0u;
-            allow[2] |= wi == 2 ? wv : 0u;
-            allow[3] |= wi == 3 ? wv : 0u;
+            const uint32_t wv = bits << (uint32_t)(k0 & 31);
+            allow0 |= (k0 >> 5) == 0 ? wv : 0u;
+            allow1 |= (k0 >> 5) == 1 ? wv : 0u;
           }
         }
       }
-      const uint32_t sbase = tl + (i & 1) * 128;
-      // pass 1: masked, scaled maximum over the stage (32 keys per TMEM load)
+      const uint32_t sbase = tl + (i & 1) * 128 + half * 64;
+      // pass 1: masked maximum over this half (32 keys per TMEM load)
       float mx0 = ninf, mx1 = ninf, mx2 = ninf, mx3 = ninf;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t v[32];
         tmem_ld32(sbase + cc * 32, v);
         tmem_wait_ld();
-        const uint32_t am = cc == 0 ? allow[0] : cc == 1 ? allow[1] : cc == 2 ? allow[2] : allow[3];
+        const uint32_t am = cc == 0 ? allow0 : allow1;
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           mx0 = fmaxf(mx0, ((am >> e) & 1u) ? __uint_as_float(v[e]) : ninf);
@@ -570,11 +604,23 @@ __global__ void __launch_bounds__(224, 1)
           mx3 = fmaxf(mx3, ((am >> (e + 3)) & 1u) ? __uint_as_float(v[e + 3]) : ninf);
         }
       }
-      const float smax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      // combine with the other half of the row
+      const float pmx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      float* xm = xmax + (i & 1) * 2 * C::BM;
+      xm[half * C::BM + r] = pmx;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&x_bar[i & 1]);
+      bool wx = mbar_wait(&x_bar[i & 1], (uint32_t)((i >> 1) & 1), ab, a.status, 216);
+      if (!__all_sync(FULL, wx)) {
+        ok = false;
+        break;
+      }
+      const float smax = fmaxf(pmx, xm[(1 - half) * C::BM + r]) * sl2;
       // Raise the reference maximum when this stage exceeds it by more than 2^8.
       // O holds contributions under the old maximum, so it is rescaled once
-      // PV_{i-1} is done; the whole warp takes that path together (rows that do
-      // not need it scale by 1).
+      // PV_{i-1} is done; both threads of a row decide alike, each warp takes
+      // that path together (rows that do not need it scale by 1), and each half
+      // rescales its own 64 columns of O.
       const bool raise = smax > m_used + 8.0f;
       const bool rescale = raise && m_used != ninf;
       if (__any_sync(FULL, rescale)) {
@@ -586,13 +632,14 @@ __global__ void __launch_bounds__(224, 1)
         tc_fence_after();
         const float f = rescale ? ex2(m_used - smax) : 1.0f;
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < D / 64; ++cc) {
           uint32_t ov[32];
-          tmem_ld32(tl + 256 + cc * 32, ov);
+          const uint32_t oc = tl + 256 + half * (D / 2) + cc * 32;
+          tmem_ld32(oc, ov);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
-          tmem_st32(tl + 256 + cc * 32, ov);
+          tmem_st32(oc, ov);
         }
         tmem_wait_st();
         l *= f;
@@ -611,11 +658,11 @@ __global__ void __launch_bounds__(224, 1)
       const float msub = m_used == ninf ? 0.0f : m_used;
       float rs0 = 0.0f, rs1 = 0.0f;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t v[32];
         tmem_ld32(sbase + cc * 32, v);
         tmem_wait_ld();
-        const uint32_t am = cc == 0 ? allow[0] : cc == 1 ? allow[1] : cc == 2 ? allow[2] : allow[3];
+        const uint32_t am = cc == 0 ? allow0 : allow1;
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -626,47 +673,53 @@ __global__ void __launch_bounds__(224, 1)
           rs1 += p1;
           pk[e >> 1] = pack_bf16x2(p0, p1);
         }
-        // keys cc*32 .. cc*32+31 are 16-byte units 4*(cc&1) .. +3 of chunk cc>>1
+        // keys 64*half + 32*cc .. +31 are 16-byte units 4*cc .. 4*cc+3 of chunk `half`
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const uint4 vv = make_uint4(pk[u * 4 + 0], pk[u * 4 + 1], pk[u * 4 + 2], pk[u * 4 + 3]);
-          *reinterpret_cast<uint4*>(sP + (cc >> 1) * (C::BM * 128) +
-                                    sw128(r, (cc & 1) * 4 + u)) = vv;
+          *reinterpret_cast<uint4*>(sP + half * (C::BM * 128) + sw128(r, cc * 4 + u)) = vv;
         }
       }
       l += rs0 + rs1;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[i & 1]);  // S buffer read twice, now free
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&m_empty[ms]);  // done with this stage's block list
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) {
+        mbar_arrive(&s_empty[i & 1]);  // S buffer read twice, now free
+        mbar_arrive(&m_empty[ms]);     // done with this stage's block list
+        mbar_arrive(p_full);
+      }
       if (last) break;
     }
     // ---- epilogue: O / l and the log-sum-exp
     bool fin = ok && mbar_wait(p_empty, (uint32_t)(i & 1), ab, a.status, 215);
     if (__all_sync(FULL, fin)) {
+      xsum[half * C::BM + r] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(l_bar);
+      fin = mbar_wait(l_bar, 0, ab, a.status, 217);
+    }
+    if (__all_sync(FULL, fin)) {
+      const float lt = xsum[r] + xsum[C::BM + r];
       tc_fence_after();
-      const float inv = row_ok && l > 0.0f ? 1.0f / l : 0.0f;
+      const float inv = row_ok && lt > 0.0f ? 1.0f / lt : 0.0f;
       const int64_t hq = (int64_t)g * a.G + h;
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+#pragma unroll 1
+      for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t ov[32];
-        tmem_ld32(tl + 256 + cc * 32, ov);
+        const int col = half * (D / 2) + cc * 32;
+        tmem_ld32(tl + 256 + col, ov);
         tmem_wait_ld();
         if (row_ok) {
           if (a.out_f32) {
-            float* dst = static_cast<float*>(a.O) + (t * a.H + hq) * D + cc * 32;
+            float* dst = static_cast<float*>(a.O) + (t * a.H + hq) * D + col;
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
               *reinterpret_cast<float4*>(dst + e) =
                   make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
                               __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
           } else {
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.O) + (t * a.H + hq) * D + cc * 32;
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.O) + (t * a.H + hq) * D + col;
 #pragma unroll
             for (int e = 0; e < 32; e += 8) {
               uint4 v;
@@ -679,7 +732,7 @@ __global__ void __launch_bounds__(224, 1)
           }
         }
       }
-      if (row_ok) a.lse[hq * a.T + t] = (m_used + __log2f(l)) * 0.69314718055994531f;
+      if (row_ok && half == 0) a.lse[hq * a.T + t] = (m_used + __log2f(lt)) * 0.69314718055994531f;
     }
     tc_fence_before();
   }
@@ -691,74 +744,42 @@ __global__ void __launch_bounds__(224, 1)
   }
 }
 
-// Tensor maps for Q [T][H][d] (box 64 x G x QS) and K/V: contiguous
-// [Tkv][Hkv][d] (box 64 x 1 x B) or paged [pages][Hkv][ps][d] (box 64 x B x 1 x 1).
-bool make_maps(const Dims& dm, int QS, const void* Q, const void* K, const void* V,
-               CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv) {
+// Tensor map for Q [T][H][d] with box 64 x G x QS: one sub-tile's query heads.
+bool make_qmap(const Dims& dm, int QS, const void* Q, CUtensorMap* mq) {
   auto fn = tmap_encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t e = 2;
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  {
-    cuuint64_t dims[3] = {(cuuint64_t)dm.d, (cuuint64_t)dm.H, (cuuint64_t)dm.T};
-    cuuint64_t str[2] = {dm.d * e, (cuuint64_t)dm.H * dm.d * e};
-    cuuint32_t box[3] = {64, (cuuint32_t)dm.G, (cuuint32_t)QS};
-    if (fn(mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(Q), dims, str, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return false;
-  }
-  const int Bb = dm.B >= 8 ? dm.B : 8;  // unused for B < 8 (cp.async gather)
-  for (int w = 0; w < 2; ++w) {
-    CUtensorMap* m = w == 0 ? mk : mv;
-    void* base = const_cast<void*>(w == 0 ? K : V);
-    CUresult r;
-    if (dm.ps > 0) {
-      const cuuint64_t npages = dm.Tkv / dm.ps;
-      cuuint64_t dims[4] = {(cuuint64_t)dm.d, (cuuint64_t)dm.ps, (cuuint64_t)dm.Hkv, npages};
-      cuuint64_t str[3] = {dm.d * e, (cuuint64_t)dm.ps * dm.d * e,
-                           (cuuint64_t)dm.Hkv * dm.ps * dm.d * e};
-      cuuint32_t box[4] = {64, (cuuint32_t)Bb, 1, 1};
-      r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, str, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {
-      cuuint64_t dims[3] = {(cuuint64_t)dm.d, (cuuint64_t)dm.Hkv, (cuuint64_t)dm.Tkv};
-      cuuint64_t str[2] = {dm.d * e, (cuuint64_t)dm.Hkv * dm.d * e};
-      cuuint32_t box[3] = {64, 1, (cuuint32_t)Bb};
-      r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, str, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    }
-    if (r != CUDA_SUCCESS) return false;
-  }
-  return true;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  cuuint64_t dims[3] = {(cuuint64_t)dm.d, (cuuint64_t)dm.H, (cuuint64_t)dm.T};
+  cuuint64_t str[2] = {dm.d * e, (cuuint64_t)dm.H * dm.d * e};
+  cuuint32_t box[3] = {64, (cuuint32_t)dm.G, (cuuint32_t)QS};
+  return fn(mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(Q), dims, str, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int D, int B>
-int launch_db(const Dims& dm, const AttnArgs& a, const void* Q, const void* K, const void* V,
-              int64_t items, cudaStream_t st) {
+int launch_db(const Dims& dm, const AttnArgs& a, const void* Q, int64_t items, cudaStream_t st) {
   using C = AttnCfg<D, B>;
-  CUtensorMap mq, mk, mv;
-  if (!make_maps(dm, a.QS, Q, K, V, &mq, &mk, &mv)) return SGQA_ERR_CUDA;
+  CUtensorMap mq;
+  if (!make_qmap(dm, a.QS, Q, &mq)) return SGQA_ERR_CUDA;
   if (cudaFuncSetAttribute(k_sparse_attn<D, B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM) != cudaSuccess)
     return SGQA_ERR_CUDA;
   log_begin(SGQA_K_ATTN, st);
-  k_sparse_attn<D, B><<<(unsigned)items, C::NTHREADS, C::SMEM, st>>>(mq, mk, mv, a);
+  k_sparse_attn<D, B><<<(unsigned)items, C::NTHREADS, C::SMEM, st>>>(mq, a);
   log_end(st);
   return cudaGetLastError() == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA;
 }
 
 template <int D>
-int launch_d(const Dims& dm, const AttnArgs& a, const void* Q, const void* K, const void* V,
-             int64_t items, cudaStream_t st) {
+int launch_d(const Dims& dm, const AttnArgs& a, const void* Q, int64_t items, cudaStream_t st) {
   switch (dm.B) {
-    case 1: return launch_db<D, 1>(dm, a, Q, K, V, items, st);
-    case 2: return launch_db<D, 2>(dm, a, Q, K, V, items, st);
-    case 4: return launch_db<D, 4>(dm, a, Q, K, V, items, st);
-    case 8: return launch_db<D, 8>(dm, a, Q, K, V, items, st);
-    case 16: return launch_db<D, 16>(dm, a, Q, K, V, items, st);
+    case 1: return launch_db<D, 1>(dm, a, Q, items, st);
+    case 2: return launch_db<D, 2>(dm, a, Q, items, st);
+    case 4: return launch_db<D, 4>(dm, a, Q, items, st);
+    case 8: return launch_db<D, 8>(dm, a, Q, items, st);
+    case 16: return launch_db<D, 16>(dm, a, Q, items, st);
     default: return SGQA_ERR_UNSUPPORTED;
   }
 }
@@ -766,7 +787,8 @@ int launch_d(const Dims& dm, const AttnArgs& a, const void* Q, const void* K, co
 }  // namespace
 
 int launch_sparse_attn_layout(const Dims& dm, const __nv_bfloat16* Q, const __nv_bfloat16* K,
-                              const __nv_bfloat16* V, const int32_t* page_table,
+                              const __nv_bfloat16* V, const __nv_bfloat16* Kp,
+                              const __nv_bfloat16* Vp, const int32_t* page_table,
                               const int64_t* union_off, const int32_t* union_len,
                               const int32_t* union_blk, const uint64_t* union_mask, void* O,
                               float* lse, int64_t tau_begin, int64_t tau_end, int64_t lay_tau0,
@@ -777,6 +799,9 @@ int launch_sparse_attn_layout(const Dims& dm, const __nv_bfloat16* Q, const __nv
   a.Q = Q;
   a.K = K;
   a.V = V;
+  a.Kp = Kp;
+  a.Vp = Vp;
+  a.nblkp = (dm.Tkv + dm.B - 1) / dm.B;
   a.page_table = page_table;
   a.uoff = union_off;
   a.ulen = union_len;
@@ -806,17 +831,19 @@ int launch_sparse_attn_layout(const Dims& dm, const __nv_bfloat16* Q, const __nv
   a.scale_log2 = dm.scale * 1.4426950408889634f;
   a.status = status;
   const int64_t items = (tau_end - tau_begin) * dm.Hkv * a.nsub;
-  if (dm.d == 128) return launch_d<128>(dm, a, Q, K, V, items, st);
-  if (dm.d == 64) return launch_d<64>(dm, a, Q, K, V, items, st);
+  if (dm.B >= 8 && (Kp == nullptr || Vp == nullptr)) return SGQA_ERR_INVALID_ARG;
+  if (dm.d == 128) return launch_d<128>(dm, a, Q, items, st);
+  if (dm.d == 64) return launch_d<64>(dm, a, Q, items, st);
   return SGQA_ERR_UNSUPPORTED;
 }
 
 int launch_sparse_attn(const Dims& dm, const __nv_bfloat16* Q, const __nv_bfloat16* K,
-                       const __nv_bfloat16* V, const int32_t* page_table,
-                       const int64_t* union_off, const int32_t* union_len,
-                       const int32_t* union_blk, const uint64_t* union_mask, void* O, float* lse,
-                       int64_t tau_begin, int64_t tau_end, int32_t* status, cudaStream_t st) {
-  return launch_sparse_attn_layout(dm, Q, K, V, page_table, union_off, union_len, union_blk,
+                       const __nv_bfloat16* V, const __nv_bfloat16* Kp, const __nv_bfloat16* Vp,
+                       const int32_t* page_table, const int64_t* union_off,
+                       const int32_t* union_len, const int32_t* union_blk,
+                       const uint64_t* union_mask, void* O, float* lse, int64_t tau_begin,
+                       int64_t tau_end, int32_t* status, cudaStream_t st) {
+  return launch_sparse_attn_layout(dm, Q, K, V, Kp, Vp, page_table, union_off, union_len, union_blk,
                                    union_mask, O, lse, tau_begin, tau_end, 0, dm.ntiles, status,
                                    st);
 }

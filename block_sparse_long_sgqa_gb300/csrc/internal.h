@@ -60,6 +60,14 @@ cudaError_t launch_index_query(const Dims& dm, const void* Q, int64_t q_begin, i
                                __nv_bfloat16* qhi, __nv_bfloat16* qlo, cudaStream_t st);
 cudaError_t launch_to_bf16(const float* in, __nv_bfloat16* out, int64_t n, cudaStream_t st);
 
+// Block-packed, pre-swizzled copy of K or V for the attention gathers (B >= 8):
+// [Hkv][ceil(Tkv/B) + 1][B * d] bf16, the last block of each head all zeros.
+cudaError_t launch_kv_pack(const Dims& dm, const void* X, const int32_t* page_table,
+                           __nv_bfloat16* out, cudaStream_t st);
+inline int64_t kv_pack_elems(const Dims& dm) {
+  return (int64_t)dm.Hkv * ((dm.Tkv + dm.B - 1) / dm.B + 1) * dm.B * dm.d;
+}
+
 // scores [Hkv][q_end-q_begin][nblk]; qhi/qlo are [Hkv][q_end-q_begin][d].
 int launch_index_scores(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* qlo,
                         const __nv_bfloat16* khi, const __nv_bfloat16* klo, int64_t q_begin,
@@ -70,12 +78,13 @@ int launch_topk_union(const Dims& dm, const float* scores, int64_t q_begin, int6
                       int32_t* sel, int64_t* union_off, int32_t* union_len, int32_t* union_blk,
                       uint64_t* union_mask, int64_t union_cap, int32_t* status, cudaStream_t st);
 
-// Attention over the tiles [tau_begin, tau_end) of the call.  Q/K/V are bf16.
+// Attention over the tiles [tau_begin, tau_end) of the call.  Q/K/V are bf16;
+// for B >= 8, Kp/Vp are their block-packed copies (launch_kv_pack).
 int launch_sparse_attn(const Dims& dm, const __nv_bfloat16* Q, const __nv_bfloat16* K,
-                       const __nv_bfloat16* V, const int32_t* page_table,
-                       const int64_t* union_off, const int32_t* union_len,
-                       const int32_t* union_blk, const uint64_t* union_mask, void* O,
-                       float* lse, int64_t tau_begin, int64_t tau_end, int32_t* status,
-                       cudaStream_t st);
+                       const __nv_bfloat16* V, const __nv_bfloat16* Kp, const __nv_bfloat16* Vp,
+                       const int32_t* page_table, const int64_t* union_off,
+                       const int32_t* union_len, const int32_t* union_blk,
+                       const uint64_t* union_mask, void* O, float* lse, int64_t tau_begin,
+                       int64_t tau_end, int32_t* status, cudaStream_t st);
 
 }  // namespace sgqa

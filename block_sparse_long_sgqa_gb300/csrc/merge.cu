@@ -153,6 +153,53 @@ __global__ void __launch_bounds__(256) k_to_bf16(const float* __restrict__ in, i
   }
 }
 
+// Block-packed K/V for the attention gathers: block j of KV head g becomes
+// B/8 groups of 8 positions; each group holds its d/64 head-dim halves as
+// 1 KB atoms of 8 rows x 128 B with the 128-byte swizzle (16-byte unit u of
+// row r stored at unit u ^ r).  One block is then one contiguous copy that
+// lands directly in the layout the tensor cores read.  Positions at or past
+// Tkv (a partial last block) and the extra block at index nblkp are zero.
+// Output [Hkv][nblkp + 1][B * d] bf16, nblkp = ceil(Tkv / B).
+template <typename T>
+__global__ void __launch_bounds__(256) k_kv_pack(const T* __restrict__ X,
+                                                 const int32_t* __restrict__ page_table,
+                                                 int64_t Tkv, int Hkv, int d, int B, int ps,
+                                                 int64_t nblkp, __nv_bfloat16* __restrict__ out) {
+  const int units = d / 8;  // 16-byte units of a row
+  const int KC = d / 64;
+  const int64_t per_g = (nblkp + 1) * B * units;
+  const int64_t total = (int64_t)Hkv * per_g;
+  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
+       x += (int64_t)gridDim.x * blockDim.x) {
+    const int g = (int)(x / per_g);
+    const int64_t rem = x % per_g;
+    const int64_t j = rem / ((int64_t)B * units);
+    const int rr = (int)((rem / units) % B);
+    const int u = (int)(rem % units);
+    const int64_t p = j * B + rr;
+    float v[8];
+    if (j < nblkp && p < Tkv) {
+      const T* row;
+      if (ps > 0) {
+        const int64_t phys = page_table[p / ps];
+        row = X + ((phys * Hkv + g) * ps + (p % ps)) * (int64_t)d;
+      } else {
+        row = X + (p * Hkv + g) * (int64_t)d;
+      }
+      Vec8<T>::load(row + u * 8, v);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = 0.0f;
+    }
+    const int r8 = rr & 7, grp = rr >> 3, c = u >> 3, uu = u & 7;
+    const int64_t o = ((int64_t)g * (nblkp + 1) + j) * B * d +  // element offset of the block
+                      ((int64_t)grp * KC * 1024 + c * 1024 + r8 * 128 + ((uu ^ r8) << 4)) / 2;
+    const uint4 w = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                               pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+    *reinterpret_cast<uint4*>(out + o) = w;
+  }
+}
+
 int grid_for(int64_t work) {
   // enough CTAs to cover every SM several times; grid-stride loops do the rest
   int64_t g = (work + 255) / 256;
@@ -221,6 +268,21 @@ cudaError_t launch_index_query(const Dims& dm, const void* Q, int64_t q_begin, i
   else
     k_index_query<<<grid, 256, 0, st>>>(static_cast<const float*>(Q), q_begin, nq, dm.H, dm.Hkv,
                                         dm.G, dm.d, qhi, qlo);
+  log_end(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_pack(const Dims& dm, const void* X, const int32_t* page_table,
+                           __nv_bfloat16* out, cudaStream_t st) {
+  const int64_t nblkp = (dm.Tkv + dm.B - 1) / dm.B;
+  const int64_t total = (int64_t)dm.Hkv * (nblkp + 1) * dm.B * (dm.d / 8);
+  log_begin(SGQA_K_STAGE, st);
+  if (dm.dtype == SGQA_BF16)
+    k_kv_pack<<<grid_for(total), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(X), page_table,
+                                                 dm.Tkv, dm.Hkv, dm.d, dm.B, dm.ps, nblkp, out);
+  else
+    k_kv_pack<<<grid_for(total), 256, 0, st>>>(static_cast<const float*>(X), page_table, dm.Tkv,
+                                                 dm.Hkv, dm.d, dm.B, dm.ps, nblkp, out);
   log_end(st);
   return cudaGetLastError();
 }

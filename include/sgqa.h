@@ -174,9 +174,12 @@ SGQA_API int sgqa_topk_union(const sgqa_params* p, const float* scores, int32_t 
  * of t's tile that lies before t's own block, plus the same current part).
  * O in the dtype of Q; lse[h][t] = log of the softmax denominator, with the
  * maximum added back.  Runs on tcgen05 tensor cores (bf16 operands, fp32
- * accumulation and fp32 online softmax); fp32 inputs are rounded to bf16 in
- * the workspace first.  Union arrays as written by sgqa_topk_union for all
- * tiles of the call.  Workspace: sgqa_workspace_bytes(p, SGQA_WS_SPARSE_ATTN). */
+ * accumulation and fp32 online softmax).  The workspace receives the staged
+ * operands: fp32 inputs rounded to bf16, and for B >= 8 a block-packed copy
+ * of K and V (each block contiguous, in the tensor cores' shared-memory
+ * layout) that the kernel gathers with one bulk copy per block.  Union arrays
+ * as written by sgqa_topk_union for all tiles of the call.  Workspace:
+ * sgqa_workspace_bytes(p, SGQA_WS_SPARSE_ATTN). */
 SGQA_API int sgqa_sparse_attn_fwd(const sgqa_params* p, const void* Q, const void* K,
                                   const void* V, const int32_t* page_table,
                                   const int64_t* union_off, const int32_t* union_len,
@@ -230,7 +233,7 @@ enum sgqa_kernel_kind {
   SGQA_K_INDEX_SCORES = 4, /* tensor-core indexer GEMM */
   SGQA_K_TOPK_UNION = 5,   /* top-k selection and tile union */
   SGQA_K_ATTN = 6,         /* sparse attention */
-  SGQA_K_STAGE = 7         /* fp32 -> bf16 staging of attention operands */
+  SGQA_K_STAGE = 7         /* attention operand staging: bf16 rounding, K/V block packing */
 };
 
 /* Optional launch log for measurement.  While a log is installed, every
