@@ -183,37 +183,22 @@ __device__ __forceinline__ void ordered_pass(const float* __restrict__ row, int6
   }
 }
 
-// Select row t of group g, write its ascending list and OR it into the tile
-// bitmask.  All lanes participate.
-__device__ void select_row(const TUArgs& a, int g, int64_t t, uint32_t* warp_smem,
-                           uint32_t* tile_bits) {
+// General path of a row's selection (any k/B, any row alignment, any bucket
+// size), given the level-0 histogram result (bucket b0, `above0` keys above
+// it, cnt0 keys in it).  Refines inside the bucket (from shared memory when
+// the bucket fits, else by re-reading the row) and emits the list with a
+// full ascending pass over the row.
+__device__ void select_row_general(const TUArgs& a, const float* __restrict__ row, int64_t nh,
+                                   uint32_t need, int32_t* out, bool vec, uint32_t b0,
+                                   uint32_t above0, uint32_t cnt0, uint32_t* warp_smem,
+                                   uint32_t* tile_bits, int64_t t) {
   const int lane = lane_id();
-  const int64_t tl = t - a.q_begin;
-  int64_t nh = (a.off + t) / a.B;
-  if (nh > a.nblk) nh = a.nblk;
-  const uint32_t need = (uint32_t)(nh < a.Ks ? nh : a.Ks);
-  const float* row = a.scores + ((int64_t)g * a.nq + tl) * a.nblk;
-  int32_t* out = a.sel + ((int64_t)g * a.nq + tl) * a.Ks;
-  const bool vec = (a.nblk & 3) == 0;
-  if (need == 0) {
-    for (int64_t x = lane; x < a.Ks; x += 32) out[x] = -1;
-    return;
-  }
-
   // The selection is: every key above the threshold prefix Tp (compared on
   // key >> shift), plus the first `rem` keys equal to it in block order.
-  const bool take_all = (int64_t)need == nh;
-  uint32_t Tp = 0, rem = need;
-  int shift = 0;
-  if (!take_all) {
-    uint32_t* hist = warp_smem;
-    uint32_t b, above, cnt;
-    zero_hist(hist, NB0);
-    hist_row(row, nh, vec, hist, 21, NB0, 32, 0);
-    find_bin(hist, NB0, rem, b, above, cnt);
-    rem -= above;
-    Tp = b;
-    shift = 21;
+  uint32_t Tp = b0, rem = need - above0;
+  int shift = 21;
+  {
+    uint32_t b = b0, above = above0, cnt = cnt0;
     if (cnt != rem) {
       // refine the remaining 21 bits in levels of 9, 9 and 3 bits
       uint2* cand = reinterpret_cast<uint2*>(warp_smem);          // reuses the histogram
@@ -267,17 +252,11 @@ __device__ void select_row(const TUArgs& a, int g, int64_t t, uint32_t* warp_sme
   // emission in ascending block order
   uint32_t eq_seen = 0, n_out = 0;
   ordered_pass(row, nh, [&](int64_t j0, bool valid, uint32_t key) {
-    bool take;
-    uint32_t meq = 0;
-    if (take_all) {
-      take = valid;
-    } else {
-      const uint32_t kp = key >> shift;
-      const bool eq = valid && kp == Tp;
-      meq = __ballot_sync(FULL, eq);
-      const uint32_t rank = eq_seen + __popc(meq & lanemask_lt());
-      take = (valid && kp > Tp) || (eq && rank < rem);
-    }
+    const uint32_t kp = key >> shift;
+    const bool eq = valid && kp == Tp;
+    const uint32_t meq = __ballot_sync(FULL, eq);
+    const uint32_t rank = eq_seen + __popc(meq & lanemask_lt());
+    const bool take = (valid && kp > Tp) || (eq && rank < rem);
     const uint32_t mt = __ballot_sync(FULL, take);
     if (take) out[n_out + __popc(mt & lanemask_lt())] = (int32_t)(j0 + lane);
     if (lane == 0 && mt) atomicOr(&tile_bits[j0 >> 5], mt);
@@ -286,6 +265,199 @@ __device__ void select_row(const TUArgs& a, int g, int64_t t, uint32_t* warp_sme
   });
   for (int64_t x = n_out + lane; x < a.Ks; x += 32) out[x] = -1;
   if (lane == 0 && n_out != need) report(a.status, SGQA_ERR_BOUNDS, (int)t);
+}
+
+// Fast path of a row's selection: k/B <= 512, 16-byte aligned rows, and a
+// level-0 bucket of at most 512 keys.  One vectorised pass in block order
+// stores the blocks above the bucket (all selected) and the bucket's members
+// in shared memory; the bucket is refined there; and the two ascending lists
+// are merged into the output without another pass over the row.
+constexpr int FAST_MAX = 512;
+static_assert(4 * FAST_MAX * 4 <= WARP_BYTES, "fast-path lists must fit a warp's scratch");
+static_assert(NBR <= FAST_MAX, "refinement histogram must fit its slot");
+
+__device__ __forceinline__ int lower_bound_smem(const int32_t* v, int n, int32_t x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (v[mid] < x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ void select_row_fast(const TUArgs& a, const float* __restrict__ row, int64_t nh,
+                                uint32_t need, int32_t* out, uint32_t b0, uint32_t above0,
+                                uint32_t cnt0, uint32_t* warp_smem, uint32_t* tile_bits,
+                                int64_t t) {
+  const int lane = lane_id();
+  uint2* cand = reinterpret_cast<uint2*>(warp_smem);                  // [512] (key, block)
+  int32_t* defs = reinterpret_cast<int32_t*>(warp_smem + 2 * FAST_MAX);  // [512] above the bucket
+  uint32_t* rh = warp_smem + 3 * FAST_MAX;                             // [512] histogram, then
+  int32_t* csel = reinterpret_cast<int32_t*>(rh);                      // selected bucket members
+  __syncwarp();  // the level-0 histogram in the same space is no longer read
+  const uint32_t lt = lanemask_lt();
+  uint32_t n_def = 0, n_c = 0;
+  // append the flagged elements of this lane's 4 consecutive blocks j0..j0+3, in order
+  auto append = [&](int64_t j0, uint32_t fd, uint32_t fc, const uint32_t (&k)[4]) {
+    const uint32_t nd = __popc(fd), nc = __popc(fc);
+    uint32_t sd = nd, sc = nc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t td = __shfl_up_sync(FULL, sd, o), tc = __shfl_up_sync(FULL, sc, o);
+      if (lane >= o) {
+        sd += td;
+        sc += tc;
+      }
+    }
+    uint32_t pd = n_def + sd - nd, pc = n_c + sc - nc;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if ((fd >> e) & 1u) defs[pd++] = (int32_t)(j0 + e);
+      if ((fc >> e) & 1u) cand[pc++] = make_uint2(k[e], (uint32_t)(j0 + e));
+    }
+    n_def += __shfl_sync(FULL, sd, 31);
+    n_c += __shfl_sync(FULL, sc, 31);
+  };
+  const float4* r4 = reinterpret_cast<const float4*>(row);
+  const int64_t n4 = nh / 4;
+  for (int64_t base = 0; base < n4; base += 32 * BATCH) {
+    float4 v[BATCH];
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int64_t x = base + u * 32 + lane;
+      v[u] = x < n4 ? __ldg(r4 + x) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int64_t g0 = base + u * 32;
+      if (g0 >= n4) break;  // warp-uniform
+      const bool valid = g0 + lane < n4;
+      const uint32_t k[4] = {order_key(v[u].x), order_key(v[u].y), order_key(v[u].z),
+                             order_key(v[u].w)};
+      uint32_t fd = 0, fc = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t bn = k[e] >> 21;
+        fd |= (uint32_t)(valid && bn > b0) << e;
+        fc |= (uint32_t)(valid && bn == b0) << e;
+      }
+      append(4 * (g0 + lane), fd, fc, k);
+    }
+  }
+  {  // the last nh % 4 blocks, one per lane
+    const int64_t j = n4 * 4 + lane;
+    const bool valid = j < nh;
+    const uint32_t key = valid ? order_key(__ldg(row + j)) : 0u;
+    const uint32_t bn = key >> 21;
+    const bool d = valid && bn > b0, c = valid && bn == b0;
+    const uint32_t md = __ballot_sync(FULL, d), mc = __ballot_sync(FULL, c);
+    if (d) defs[n_def + __popc(md & lt)] = (int32_t)j;
+    if (c) cand[n_c + __popc(mc & lt)] = make_uint2(key, (uint32_t)j);
+    n_def += __popc(md);
+    n_c += __popc(mc);
+  }
+  __syncwarp();
+  // refine the threshold inside the bucket: 9, 9 and 3 more key bits
+  uint32_t Tp = b0, rem = need - above0, cnt = cnt0;
+  int shift = 21;
+  const int widths[3] = {9, 9, 3};
+  for (int lv = 0; lv < 3 && cnt != rem; ++lv) {
+    const int w = widths[lv];
+    const int nb = 1 << w;
+    const int nshift = shift - w;
+    zero_hist(rh, nb < 128 ? 128 : nb);
+    hist_cand(cand, (int)n_c, rh, nshift, nb, shift, Tp);
+    uint32_t b, above;
+    if (nb >= 32) {
+      find_bin(rh, nb, rem, b, above, cnt);
+    } else {
+      uint32_t acc = 0;
+      b = 0;
+      above = 0;
+      cnt = 0;
+      for (int i = nb - 1; i >= 0; --i) {
+        const uint32_t h = rh[i];
+        if (acc + h >= rem) {
+          b = i;
+          above = acc;
+          cnt = h;
+          break;
+        }
+        acc += h;
+      }
+    }
+    rem -= above;
+    Tp = (Tp << w) | b;
+    shift = nshift;
+    __syncwarp();
+  }
+  // selected bucket members, in block order: above Tp, or equal and among the first `rem`
+  uint32_t n_sel = 0, eq_seen = 0;
+  for (uint32_t base = 0; base < n_c; base += 32) {
+    const uint32_t i = base + lane;
+    const bool valid = i < n_c;
+    const uint2 cv = valid ? cand[i] : make_uint2(0u, 0u);
+    const uint32_t kp = cv.x >> shift;
+    const bool eq = valid && kp == Tp;
+    const uint32_t meq = __ballot_sync(FULL, eq);
+    const uint32_t rank = eq_seen + __popc(meq & lt);
+    const bool take = (valid && kp > Tp) || (eq && rank < rem);
+    const uint32_t mt = __ballot_sync(FULL, take);
+    if (take) csel[n_sel + __popc(mt & lt)] = (int32_t)cv.y;
+    n_sel += __popc(mt);
+    eq_seen += __popc(meq);
+  }
+  __syncwarp();
+  // merge the two ascending lists (disjoint block sets) into the output
+  for (uint32_t i = lane; i < n_def; i += 32) {
+    const int32_t v = defs[i];
+    out[i + lower_bound_smem(csel, (int)n_sel, v)] = v;
+    atomicOr(&tile_bits[v >> 5], 1u << (v & 31));
+  }
+  for (uint32_t i = lane; i < n_sel; i += 32) {
+    const int32_t v = csel[i];
+    out[i + lower_bound_smem(defs, (int)n_def, v)] = v;
+    atomicOr(&tile_bits[v >> 5], 1u << (v & 31));
+  }
+  for (int x = (int)need + lane; x < a.Ks; x += 32) out[x] = -1;
+  if (lane == 0 && n_def + n_sel != need) report(a.status, SGQA_ERR_BOUNDS, (int)t);
+  __syncwarp();
+}
+
+// Select row t of group g, write its ascending list and OR it into the tile
+// bitmask.  All lanes participate.
+__device__ void select_row(const TUArgs& a, int g, int64_t t, uint32_t* warp_smem,
+                           uint32_t* tile_bits) {
+  const int lane = lane_id();
+  const int64_t tl = t - a.q_begin;
+  int64_t nh = (a.off + t) / a.B;
+  if (nh > a.nblk) nh = a.nblk;
+  const uint32_t need = (uint32_t)(nh < a.Ks ? nh : a.Ks);
+  const float* row = a.scores + ((int64_t)g * a.nq + tl) * a.nblk;
+  int32_t* out = a.sel + ((int64_t)g * a.nq + tl) * a.Ks;
+  const bool vec = (a.nblk & 3) == 0;
+  if (need == 0) {
+    for (int64_t x = lane; x < a.Ks; x += 32) out[x] = -1;
+    return;
+  }
+  if ((int64_t)need == nh) {  // every historical block: no scores to read
+    for (int64_t x = lane; x < nh; x += 32) out[x] = (int32_t)x;
+    for (int64_t w = lane; w < (nh + 31) / 32; w += 32) {
+      const int64_t hi = (w + 1) * 32;
+      atomicOr(&tile_bits[w], hi <= nh ? FULL : ((1u << (nh & 31)) - 1u));
+    }
+    for (int64_t x = nh + lane; x < a.Ks; x += 32) out[x] = -1;
+    return;
+  }
+  // level 0: histogram of the top 11 key bits
+  uint32_t b0, above0, cnt0;
+  zero_hist(warp_smem, NB0);
+  hist_row(row, nh, vec, warp_smem, 21, NB0, 32, 0);
+  find_bin(warp_smem, NB0, need, b0, above0, cnt0);
+  if (vec && need <= (uint32_t)FAST_MAX && cnt0 <= (uint32_t)FAST_MAX)
+    select_row_fast(a, row, nh, need, out, b0, above0, cnt0, warp_smem, tile_bits, t);
+  else
+    select_row_general(a, row, nh, need, out, vec, b0, above0, cnt0, warp_smem, tile_bits, t);
 }
 
 __global__ void k_topk_union(TUArgs a) {
