@@ -338,7 +338,8 @@ SGQA_API int sgqa_index_scores(const sgqa_params* p, const void* Q, const float*
   cudaError_t e = launch_split_kbar(dm, Kbar, w.khi, w.klo, st);
   if (e == cudaSuccess) e = launch_index_query(dm, Q, q_begin, q_end, w.qhi, w.qlo, st);
   if (e != cudaSuccess) return SGQA_ERR_CUDA;
-  return launch_index_scores(dm, w.qhi, w.qlo, w.khi, w.klo, q_begin, q_end, scores, status, st);
+  return launch_index_scores(dm, w.qhi, w.qlo, w.khi, w.klo, q_begin, q_end, scores, true,
+                             status, st);
 }
 
 SGQA_API int sgqa_topk_union(const sgqa_params* p, const float* scores, int32_t q_begin,
@@ -436,7 +437,7 @@ SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, co
       e = launch_index_query(dm, Q, q0, q1, w.ix.qhi, w.ix.qlo, st);
       if (e != cudaSuccess) return SGQA_ERR_CUDA;
       rc = launch_index_scores(dm, w.ix.qhi, w.ix.qlo, w.ix.khi, w.ix.klo, q0, q1, w.scores,
-                               status, st);
+                               false, status, st);
       if (rc != SGQA_OK) return rc;
     }
     rc = launch_topk_union_layout(dm, w.scores, q0, q1, w.sel, w.uoff, w.ulen, w.ublk, w.umask,

@@ -10,11 +10,19 @@
 // three-product scheme of Markidis et al., "NVIDIA Tensor Core
 // Programmability, Performance & Precision", 2018).
 //
-// CTA = 128 queries x all causal blocks of one group, in steps of 128 blocks.
-// Warp 0 issues TMA loads (A once, B double-buffered), warp 1 issues the
-// MMAs into a double-buffered TMEM accumulator (2 x 128 fp32 columns), warps
-// 2-5 drain TMEM (one query row per thread), apply the causal block mask and
-// store the scores.
+// Work item = (128 queries, one group, 128 blocks): one 128x128 output tile.
+// The items of a launch are split into equal contiguous ranges, one per SM
+// (persistent CTAs), so every SM gets the same number of tiles however the
+// causal row lengths vary; consecutive items share the query operand, which
+// is reloaded only when the (row tile, group) pair changes.  Warp 0 issues
+// the TMA loads (B double-buffered), warp 1 the MMAs into a double-buffered
+// TMEM accumulator (2 x 128 fp32 columns), and warps 2-5 drain TMEM (one query
+// row per thread), apply the causal block mask and write the tile.  Stores go
+// through a 128-byte-swizzled shared staging buffer and TMA, so each tile
+// leaves as full 128-byte rows instead of 16-byte pieces of 32 rows.
+#include <algorithm>
+#include <cstring>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -33,18 +41,70 @@ struct IdxCfg {
   static constexpr int OFF_ALO = A_BYTES;
   static constexpr int OFF_B = 2 * A_BYTES;
   static constexpr int STAGE_BYTES = 2 * B_BYTES;  // hi + lo
-  static constexpr int OFF_BAR = OFF_B + STAGES * STAGE_BYTES;
+  static constexpr int STG_BYTES = 32 * 128;       // one 32 x 32 fp32 store box
+  static constexpr int OFF_STG = OFF_B + STAGES * STAGE_BYTES;  // [4 warps][2]
+  static constexpr int OFF_BAR = OFF_STG + 8 * STG_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr int NTHREADS = 192;
+  static_assert(SMEM <= 232448, "shared memory budget");
 };
+
+struct IdxArgs {
+  int64_t nq, q_begin, q_end, q_offset, nblk;
+  int B, Hkv;
+  int64_t total;   // work items of the launch
+  int fill_tail;   // write -inf for the columns past a row tile's last item
+  int tma_store;   // scores rows are 16-byte multiples: store through the tensor map
+  float* scores;
+  int32_t* status;
+};
+
+// Column tiles of row tile rt (at least one, so rows with no complete block
+// still get their -inf row).
+__device__ __forceinline__ int64_t ntiles_of(const IdxArgs& a, int64_t rt) {
+  const int64_t t0 = a.q_begin + rt * 128;
+  const int64_t t_last = (t0 + 128 < a.q_end ? t0 + 128 : a.q_end) - 1;
+  int64_t nh = (a.q_offset + t_last) / a.B;
+  if (nh > a.nblk) nh = a.nblk;
+  const int64_t nt = (nh + 127) / 128;
+  return nt > 0 ? nt : 1;
+}
+
+// Items are ordered by row tile, then group, then column tile.
+struct Item {
+  int64_t rt, n, nt;
+  int g;
+};
+__device__ Item item_at(const IdxArgs& a, int64_t i) {
+  Item w;
+  w.rt = 0;
+  for (;;) {
+    const int64_t nt = ntiles_of(a, w.rt);
+    if (i < nt * a.Hkv) {
+      w.g = (int)(i / nt);
+      w.n = i % nt;
+      w.nt = nt;
+      return w;
+    }
+    i -= nt * a.Hkv;
+    ++w.rt;
+  }
+}
+__device__ __forceinline__ void item_next(const IdxArgs& a, Item& w) {
+  if (++w.n < w.nt) return;
+  w.n = 0;
+  if (++w.g < a.Hkv) return;
+  w.g = 0;
+  ++w.rt;
+  w.nt = ntiles_of(a, w.rt);
+}
 
 template <int D>
 __global__ void __launch_bounds__(192, 1)
     k_index_scores(const __grid_constant__ CUtensorMap mq_hi, const __grid_constant__ CUtensorMap mq_lo,
                    const __grid_constant__ CUtensorMap mk_hi, const __grid_constant__ CUtensorMap mk_lo,
-                   int64_t nq, int64_t q_begin, int64_t q_end, int64_t q_offset, int B, int64_t nblk,
-                   float* __restrict__ scores, int32_t* status) {
+                   const __grid_constant__ CUtensorMap ms, IdxArgs a) {
   using C = IdxCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -56,20 +116,17 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* acc_full = bars + 5;   // [2]
   uint64_t* acc_empty = bars + 7;  // [2]
   uint64_t* mma_done = bars + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
-  int* abort_flag = reinterpret_cast<int*>(bars + 11);
+  uint64_t* a_empty = bars + 10;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  int* abort_flag = reinterpret_cast<int*>(bars + 12);
 
-  const int g = blockIdx.y;
-  const int64_t tl0 = (int64_t)(gridDim.x - 1 - blockIdx.x) * C::BM;  // heavy tiles first
-  const int64_t t0 = q_begin + tl0;
-  const int64_t t_last = (t0 + C::BM < q_end ? t0 + C::BM : q_end) - 1;
-  int64_t nh_max = (q_offset + t_last) / B;
-  if (nh_max > nblk) nh_max = nblk;
-  const int n_tiles = (int)((nh_max + C::BN - 1) / C::BN);
+  const int64_t lo = (int64_t)blockIdx.x * a.total / gridDim.x;
+  const int64_t hi = (int64_t)(blockIdx.x + 1) * a.total / gridDim.x;
   const int warp = warp_id(), lane = lane_id();
 
   if (threadIdx.x == 0) {
     mbar_init(a_full, 1);
+    mbar_init(a_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
@@ -86,67 +143,85 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Abort ab{abort_flag};
+  int32_t* status = a.status;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0 && lo < hi) {
       tma_prefetch_desc(&mq_hi);
       tma_prefetch_desc(&mk_hi);
-      const int32_t arow = (int32_t)(g * nq + tl0);
-      mbar_expect_tx(a_full, 2 * C::A_BYTES);
-      for (int c = 0; c < C::KC; ++c) {
-        tma_load_2d(smem + C::OFF_AHI + c * C::A_TILE, &mq_hi, a_full, c * 64, arow);
-        tma_load_2d(smem + C::OFF_ALO + c * C::A_TILE, &mq_lo, a_full, c * 64, arow);
-      }
+      Item w = item_at(a, lo);
+      int64_t cur_rt = -1;
+      int cur_g = -1, a_loads = 0;
       int issued[2] = {0, 0};
-      for (int n = 0; n < n_tiles; ++n) {
-        const int s = n & 1;
-        if (!mbar_wait(&b_empty[s], ((n >> 1) & 1) ^ 1, ab, status, 101)) break;
+      for (int64_t k = 0; k < hi - lo; ++k, item_next(a, w)) {
+        const int s = (int)(k & 1);
+        if (!mbar_wait(&b_empty[s], (uint32_t)((k >> 1) & 1) ^ 1, ab, status, 101)) break;
         mbar_expect_tx(&b_full[s], C::STAGE_BYTES);
         uint8_t* sb = smem + C::OFF_B + s * C::STAGE_BYTES;
-        const int32_t brow = (int32_t)(g * nblk + (int64_t)n * C::BN);
+        const int32_t brow = (int32_t)(w.g * a.nblk + w.n * C::BN);
         for (int c = 0; c < C::KC; ++c) {
           tma_load_2d(sb + c * C::B_TILE, &mk_hi, &b_full[s], c * 64, brow);
           tma_load_2d(sb + C::B_BYTES + c * C::B_TILE, &mk_lo, &b_full[s], c * 64, brow);
         }
         ++issued[s];
+        if (w.rt != cur_rt || w.g != cur_g) {  // new query operand
+          if (a_loads > 0 && !mbar_wait(a_empty, (a_loads - 1) & 1, ab, status, 100)) break;
+          mbar_expect_tx(a_full, 2 * C::A_BYTES);
+          const int32_t arow = (int32_t)(w.g * a.nq + w.rt * C::BM);
+          for (int c = 0; c < C::KC; ++c) {
+            tma_load_2d(smem + C::OFF_AHI + c * C::A_TILE, &mq_hi, a_full, c * 64, arow);
+            tma_load_2d(smem + C::OFF_ALO + c * C::A_TILE, &mq_lo, a_full, c * 64, arow);
+          }
+          ++a_loads;
+          cur_rt = w.rt;
+          cur_g = w.g;
+        }
       }
       if (ab.set()) {  // let every copy this CTA started land before it exits
-        mbar_wait_drain(a_full, 0, status, 198);
+        if (a_loads > 0) mbar_wait_drain(a_full, (a_loads - 1) & 1, status, 198);
         for (int s = 0; s < 2; ++s)
           if (issued[s] > 0) mbar_wait_drain(&b_full[s], (issued[s] - 1) & 1, status, 197);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0 && lo < hi) {
       constexpr uint32_t idesc = idesc_bf16_f32(C::BM, C::BN, 0, 0);
       const uint32_t a_hi = smem_u32(smem + C::OFF_AHI);
       const uint32_t a_lo = smem_u32(smem + C::OFF_ALO);
-      if (mbar_wait(a_full, 0, ab, status, 102)) {
-        for (int n = 0; n < n_tiles; ++n) {
-          const int s = n & 1, acc = n & 1;
-          if (!mbar_wait(&b_full[s], (n >> 1) & 1, ab, status, 103)) break;
-          if (!mbar_wait(&acc_empty[acc], ((n >> 1) & 1) ^ 1, ab, status, 104)) break;
-          tc_fence_after();
-          const uint32_t b_hi = smem_u32(smem + C::OFF_B + s * C::STAGE_BYTES);
-          const uint32_t b_lo = b_hi + C::B_BYTES;
-          const uint32_t d_t = tmem + acc * C::BN;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::A_TILE + (kk & 3) * 32;
-            const uint32_t boff = (kk >> 2) * C::B_TILE + (kk & 3) * 32;
-            const uint64_t ahi = sdesc_sw128(a_hi + off, 16, 1024);
-            const uint64_t alo = sdesc_sw128(a_lo + off, 16, 1024);
-            const uint64_t bhi = sdesc_sw128(b_hi + boff, 16, 1024);
-            const uint64_t blo = sdesc_sw128(b_lo + boff, 16, 1024);
-            umma_f16(d_t, ahi, bhi, idesc, kk > 0 ? 1u : 0u);
-            umma_f16(d_t, ahi, blo, idesc, 1u);
-            umma_f16(d_t, alo, bhi, idesc, 1u);
-          }
-          umma_commit(&b_empty[s]);
-          umma_commit(&acc_full[acc]);
+      Item w = item_at(a, lo);
+      int64_t cur_rt = -1;
+      int cur_g = -1, a_uses = 0;
+      for (int64_t k = 0; k < hi - lo; ++k, item_next(a, w)) {
+        const int s = (int)(k & 1), acc = (int)(k & 1);
+        if (w.rt != cur_rt || w.g != cur_g) {
+          if (a_uses > 0) umma_commit(a_empty);  // old operand free once its MMAs finish
+          if (!mbar_wait(a_full, a_uses & 1, ab, status, 102)) break;
+          ++a_uses;
+          cur_rt = w.rt;
+          cur_g = w.g;
         }
+        if (!mbar_wait(&b_full[s], (uint32_t)((k >> 1) & 1), ab, status, 103)) break;
+        if (!mbar_wait(&acc_empty[acc], (uint32_t)((k >> 1) & 1) ^ 1, ab, status, 104)) break;
+        tc_fence_after();
+        const uint32_t b_hi = smem_u32(smem + C::OFF_B + s * C::STAGE_BYTES);
+        const uint32_t b_lo = b_hi + C::B_BYTES;
+        const uint32_t d_t = tmem + acc * C::BN;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::A_TILE + (kk & 3) * 32;
+          const uint32_t boff = (kk >> 2) * C::B_TILE + (kk & 3) * 32;
+          const uint64_t ahi = sdesc_sw128(a_hi + off, 16, 1024);
+          const uint64_t alo = sdesc_sw128(a_lo + off, 16, 1024);
+          const uint64_t bhi = sdesc_sw128(b_hi + boff, 16, 1024);
+          const uint64_t blo = sdesc_sw128(b_lo + boff, 16, 1024);
+          umma_f16(d_t, ahi, bhi, idesc, kk > 0 ? 1u : 0u);
+          umma_f16(d_t, ahi, blo, idesc, 1u);
+          umma_f16(d_t, alo, bhi, idesc, 1u);
+        }
+        umma_commit(&b_empty[s]);
+        umma_commit(&acc_full[acc]);
       }
       umma_commit(mma_done);
       mbar_wait_drain(mma_done, 0, status, 199);
@@ -154,56 +229,101 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // --------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quadrant of this warp
-    const int r = q * 32 + lane;
-    const int64_t t = t0 + r;
-    const bool valid = t < q_end;
-    int64_t nh = (q_offset + t) / B;
-    if (nh > nblk) nh = nblk;
-    float* row = scores + ((int64_t)g * nq + (t - q_begin)) * nblk;
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const bool vec = (nblk & 3) == 0;
+    uint8_t* stg = smem + C::OFF_STG + (warp - 2) * 2 * C::STG_BYTES;
     const float ninf = -__int_as_float(0x7f800000);
-    for (int n = 0; n < n_tiles; ++n) {
-      const int acc = n & 1;
-      // outcome made warp-uniform: tcgen05.ld below is warp-collective
-      const bool w = mbar_wait(&acc_full[acc], (n >> 1) & 1, ab, status, 105);
-      if (!__all_sync(0xffffffffu, w)) break;
-      tc_fence_after();
-      uint32_t v[4][32];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tl + acc * C::BN + cc * 32, v[cc]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
-      if (valid) {
-#pragma unroll
+    const bool vec = (a.nblk & 3) == 0;
+    int sc = 0;  // boxes this warp has stored
+    if (lo < hi) {
+      Item w = item_at(a, lo);
+      for (int64_t k = 0; k < hi - lo; ++k, item_next(a, w)) {
+        const int acc = (int)(k & 1);
+        const int64_t tl_row = w.rt * C::BM + q * 32;  // first row of this warp, local
+        const int64_t t = a.q_begin + tl_row + lane;
+        const bool valid = t < a.q_end;
+        int64_t nh = (a.q_offset + t) / a.B;
+        if (nh > a.nblk) nh = a.nblk;
+        float* row = a.scores + ((int64_t)w.g * a.nq + tl_row + lane) * a.nblk;
+        // outcome made warp-uniform: tcgen05.ld below is warp-collective
+        const bool ok = mbar_wait(&acc_full[acc], (uint32_t)((k >> 1) & 1), ab, status, 105);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+#pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(tl + acc * C::BN + cc * 32, v);
+          tmem_wait_ld();
+          if (cc == 3) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          }
+          const int64_t j0 = w.n * C::BN + cc * 32;
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const int64_t j = (int64_t)n * C::BN + cc * 32 + i;
-            float o[4];
+          for (int i = 0; i < 32; ++i)
+            if (j0 + i >= nh) v[i] = __float_as_uint(ninf);
+          if (a.tma_store) {
+            if (j0 >= a.nblk || tl_row >= a.nq) continue;  // box wholly outside (warp-uniform)
+            uint8_t* buf = stg + (sc & 1) * C::STG_BYTES;
+            if (lane == 0) bulk_wait_read<1>();  // the box stored from `buf` two boxes ago
+            __syncwarp();
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[e] = (j + e < nh) ? __uint_as_float(v[cc][i + e]) : ninf;
-            if (vec && j + 3 < nblk) {
-              *reinterpret_cast<float4*>(row + j) = make_float4(o[0], o[1], o[2], o[3]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (j + e < nblk) row[j + e] = o[e];
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                  make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&ms, buf, (int32_t)j0, (int32_t)tl_row, w.g);
+              bulk_commit_group();
             }
+            ++sc;
+          } else if (valid) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const int64_t j = j0 + i;
+              if (vec && j + 3 < a.nblk) {
+                *reinterpret_cast<uint4*>(row + j) = make_uint4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  if (j + e < a.nblk) row[j + e] = __uint_as_float(v[i + e]);
+              }
+            }
+          }
+        }
+        if (a.fill_tail && w.n == w.nt - 1) {
+          // columns past the row tile's last computed tile are never historical
+          const int64_t jt = w.nt * C::BN;
+          if (a.tma_store) {
+            if (jt < a.nblk && tl_row < a.nq) {
+              if (lane == 0) bulk_wait_read<0>();
+              __syncwarp();
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<float4*>(stg + lane * 128 + c * 16) =
+                    make_float4(ninf, ninf, ninf, ninf);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                for (int64_t j = jt; j < a.nblk; j += 32)
+                  tma_store_3d(&ms, stg, (int32_t)j, (int32_t)tl_row, w.g);
+                bulk_commit_group();
+                bulk_wait_read<0>();
+              }
+              __syncwarp();
+            }
+          } else if (valid) {
+            int64_t j = jt;
+            if (vec)
+              for (; j + 3 < a.nblk; j += 4)
+                *reinterpret_cast<float4*>(row + j) = make_float4(ninf, ninf, ninf, ninf);
+            for (; j < a.nblk; ++j) row[j] = ninf;
           }
         }
       }
     }
-    if (valid) {  // blocks past the last computed tile are never historical
-      int64_t j = (int64_t)n_tiles * C::BN;
-      if (vec) {
-        for (; j + 3 < nblk; j += 4)
-          *reinterpret_cast<float4*>(row + j) = make_float4(ninf, ninf, ninf, ninf);
-      }
-      for (; j < nblk; ++j) row[j] = ninf;
-    }
+    if (lane == 0) bulk_wait_all<0>();  // stores complete before the CTA's shared memory goes
+    __syncwarp();
   }
 
   __syncthreads();
@@ -213,27 +333,65 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+bool make_tmap_scores(CUtensorMap* map, float* base, int64_t nblk, int64_t nq, int Hkv) {
+  auto fn = tmap_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)nblk, (cuuint64_t)nq, (cuuint64_t)Hkv};
+  cuuint64_t strides[2] = {(cuuint64_t)nblk * 4, (cuuint64_t)(nblk * nq * 4)};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 int launch_impl(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* qlo,
                 const __nv_bfloat16* khi, const __nv_bfloat16* klo, int64_t q_begin,
-                int64_t q_end, float* scores, int32_t* status, cudaStream_t st) {
+                int64_t q_end, float* scores, bool fill_tail, int32_t* status, cudaStream_t st) {
   using C = IdxCfg<D>;
-  const int64_t nq = q_end - q_begin;
-  CUtensorMap m_qhi, m_qlo, m_khi, m_klo;
+  IdxArgs a;
+  a.nq = q_end - q_begin;
+  a.q_begin = q_begin;
+  a.q_end = q_end;
+  a.q_offset = dm.off;
+  a.nblk = dm.nblk;
+  a.B = dm.B;
+  a.Hkv = dm.Hkv;
+  a.fill_tail = fill_tail ? 1 : 0;
+  a.tma_store = (dm.nblk % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) & 15u) == 0) ? 1 : 0;
+  a.scores = scores;
+  a.status = status;
+  // items: sum over row tiles of Hkv * column tiles (same count as the kernel)
+  int64_t total = 0;
+  for (int64_t t0 = q_begin; t0 < q_end; t0 += C::BM) {
+    const int64_t t_last = std::min(t0 + C::BM, q_end) - 1;
+    const int64_t nh = std::min((dm.off + t_last) / dm.B, dm.nblk);
+    total += dm.Hkv * std::max<int64_t>(1, (nh + C::BN - 1) / C::BN);
+  }
+  a.total = total;
+  CUtensorMap m_qhi, m_qlo, m_khi, m_klo, m_s;
   const uint64_t row_bytes = (uint64_t)D * 2;
-  if (!make_tmap_2d_bf16(&m_qhi, qhi, D, (uint64_t)dm.Hkv * nq, row_bytes, 64, C::BM) ||
-      !make_tmap_2d_bf16(&m_qlo, qlo, D, (uint64_t)dm.Hkv * nq, row_bytes, 64, C::BM) ||
+  if (!make_tmap_2d_bf16(&m_qhi, qhi, D, (uint64_t)dm.Hkv * a.nq, row_bytes, 64, C::BM) ||
+      !make_tmap_2d_bf16(&m_qlo, qlo, D, (uint64_t)dm.Hkv * a.nq, row_bytes, 64, C::BM) ||
       !make_tmap_2d_bf16(&m_khi, khi, D, (uint64_t)dm.Hkv * dm.nblk, row_bytes, 64, C::BN) ||
       !make_tmap_2d_bf16(&m_klo, klo, D, (uint64_t)dm.Hkv * dm.nblk, row_bytes, 64, C::BN))
     return SGQA_ERR_CUDA;
+  if (a.tma_store) {
+    if (!make_tmap_scores(&m_s, scores, dm.nblk, a.nq, dm.Hkv)) return SGQA_ERR_CUDA;
+  } else {
+    std::memset(&m_s, 0, sizeof(m_s));
+  }
   if (cudaFuncSetAttribute(k_index_scores<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM) != cudaSuccess)
     return SGQA_ERR_CUDA;
-  dim3 grid((unsigned)((nq + C::BM - 1) / C::BM), (unsigned)dm.Hkv);
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
+    return SGQA_ERR_CUDA;
+  const unsigned grid = (unsigned)std::min<int64_t>(total, nsm);
   log_begin(SGQA_K_INDEX_SCORES, st);
-  k_index_scores<D><<<grid, C::NTHREADS, C::SMEM, st>>>(m_qhi, m_qlo, m_khi, m_klo, nq, q_begin,
-                                                         q_end, dm.off, dm.B, dm.nblk, scores,
-                                                         status);
+  k_index_scores<D><<<grid, C::NTHREADS, C::SMEM, st>>>(m_qhi, m_qlo, m_khi, m_klo, m_s, a);
   log_end(st);
   return cudaGetLastError() == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA;
 }
@@ -242,10 +400,13 @@ int launch_impl(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* q
 
 int launch_index_scores(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* qlo,
                         const __nv_bfloat16* khi, const __nv_bfloat16* klo, int64_t q_begin,
-                        int64_t q_end, float* scores, int32_t* status, cudaStream_t st) {
+                        int64_t q_end, float* scores, bool fill_tail, int32_t* status,
+                        cudaStream_t st) {
   if (q_end <= q_begin || dm.nblk == 0) return SGQA_OK;  // nothing to score
-  if (dm.d == 128) return launch_impl<128>(dm, qhi, qlo, khi, klo, q_begin, q_end, scores, status, st);
-  if (dm.d == 64) return launch_impl<64>(dm, qhi, qlo, khi, klo, q_begin, q_end, scores, status, st);
+  if (dm.d == 128)
+    return launch_impl<128>(dm, qhi, qlo, khi, klo, q_begin, q_end, scores, fill_tail, status, st);
+  if (dm.d == 64)
+    return launch_impl<64>(dm, qhi, qlo, khi, klo, q_begin, q_end, scores, fill_tail, status, st);
   return SGQA_ERR_UNSUPPORTED;
 }
 

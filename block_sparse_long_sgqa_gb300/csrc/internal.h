@@ -69,9 +69,13 @@ inline int64_t kv_pack_elems(const Dims& dm) {
 }
 
 // scores [Hkv][q_end-q_begin][nblk]; qhi/qlo are [Hkv][q_end-q_begin][d].
+// Every score of a causal block is written, and -inf for the other blocks of
+// each row's last 128-block tile; fill_tail also writes -inf for all blocks
+// past that tile (the public contract), which the fused prefill skips.
 int launch_index_scores(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* qlo,
                         const __nv_bfloat16* khi, const __nv_bfloat16* klo, int64_t q_begin,
-                        int64_t q_end, float* scores, int32_t* status, cudaStream_t st);
+                        int64_t q_end, float* scores, bool fill_tail, int32_t* status,
+                        cudaStream_t st);
 
 size_t topk_union_ws_bytes(const Dims& dm, int64_t nq);
 int launch_topk_union(const Dims& dm, const float* scores, int64_t q_begin, int64_t q_end,
