@@ -460,11 +460,11 @@ SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int
   if (launches) {
     // with an empty block-key cache: merge, operand staging (fp32 rounding,
     // K/V block packing), then per chunk the index query and indexer GEMM
-    // (when there are blocks), top-k/union and attention
+    // (when there are blocks), top-k rows, tile union and attention
     const int64_t nchunks = (dm.T + chunk - 1) / chunk;
     int64_t n = (dm.nblk > 0 ? 1 : 0) + (dm.dtype == SGQA_FP32 ? (dm.B >= 8 ? 1 : 3) : 0) +
                 (dm.B >= 8 ? 2 : 0);
-    n += nchunks * ((dm.nblk > 0 ? 2 : 0) + 2);
+    n += nchunks * ((dm.nblk > 0 ? 2 : 0) + 3);
     *launches = (int32_t)n;
   }
   return SGQA_OK;

@@ -6,18 +6,27 @@
 // block list serves a whole tile (paragraph "Efficient implementation of
 // sparse attention").
 //
-// One CTA per (KV group, tile).  Each warp owns rows (queries) of the tile and
-// runs an exact radix select on the row's fp32 scores, compared through the
-// order-preserving map of their bit patterns: an 11-bit histogram of the top
-// key bits finds the bucket of the k-th largest key, the bucket's members are
-// compacted into shared memory, two more histogram levels (11 + 10 bits) pin
-// the k-th key exactly, and a final pass in ascending block order emits every
-// block above it plus the lowest-indexed blocks equal to it.  Emission uses
-// warp ballots, so each list comes out sorted and each 32-block word of the
-// tile's union bitmask is OR-ed in one shared atomic.  The union is then the
-// set bits of that bitmask (ranks by a prefix sum of word popcounts), and a
-// member mask per union slot is built from the rows' lists with shared (or,
-// for very long unions, global) atomic ORs.
+// Two kernels.  The row kernel runs an exact select per query row (one warp
+// per row, persistent CTAs, rows dealt out in blocks of 8 consecutive
+// queries) on the row's fp32 scores, compared through the order-preserving
+// map of their bit patterns, and writes each list in ascending block order.
+// Rows of 2048 .. 16384 blocks take the candidate path: a float threshold that
+// a little more than k/B of the row's scores clear (predicted from the
+// previous row of the same warp, else from a sample of 8 adjacent blocks in
+// every 64), one pass that compacts the scores above it into shared memory in
+// block order, and a radix select with ties to the lowest index on those
+// candidates, so the row is read once.  Other rows, and rows whose candidates
+// miss the selection or overflow, take the histogram path: an 11-bit
+// histogram of the top key bits finds the bucket of the k-th largest key, the
+// bucket is refined by further levels (in shared memory when it is small),
+// and an ascending pass emits every block above the k-th key plus the
+// lowest-indexed blocks equal to it.  The tile kernel (one CTA per tile and
+// group) ORs the tile's lists into a block bitmask; the union is the set bits
+// (ranks by a prefix sum of word popcounts), and a member mask per union slot
+// is built from the lists with shared (or, for very long unions, global)
+// atomic ORs.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -26,16 +35,15 @@ namespace {
 
 constexpr int NB0 = 2048;        // bins of the level-0 histogram (top 11 key bits)
 constexpr int NBR = 512;         // bins of the refinement histograms (9 bits)
-constexpr int WARP_BYTES = NB0 * 4;  // per-warp scratch: level-0 histogram, then
-                                     // bucket candidates + a refinement histogram
-constexpr int CAND_CAP = (WARP_BYTES - NBR * 4) / 8;  // 768 (key, index) pairs
+constexpr int WARP_BYTES = 12288;  // per-warp scratch: histogram + candidate lists
+constexpr int CAND_CAP = (WARP_BYTES - NBR * 4) / 8;  // 1280 (key, index) pairs
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int BATCH = 8;         // 32-element groups loaded before use
 
 struct TUArgs {
   const float* scores;  // [Hkv][nq][nblk], rows q_begin .. q_end-1 of the call
   int64_t nq, q_begin, q_end, T, off, nblk;
-  int B, Ks, W;
+  int B, Ks, W, Hkv;
   int32_t* sel;         // [Hkv][nq][Ks]
   int64_t* uoff;        // [Hkv][lay_ntiles]
   int32_t* ulen;
@@ -191,7 +199,7 @@ __device__ __forceinline__ void ordered_pass(const float* __restrict__ row, int6
 __device__ void select_row_general(const TUArgs& a, const float* __restrict__ row, int64_t nh,
                                    uint32_t need, int32_t* out, bool vec, uint32_t b0,
                                    uint32_t above0, uint32_t cnt0, uint32_t* warp_smem,
-                                   uint32_t* tile_bits, int64_t t) {
+                                   int64_t t) {
   const int lane = lane_id();
   // The selection is: every key above the threshold prefix Tp (compared on
   // key >> shift), plus the first `rem` keys equal to it in block order.
@@ -259,7 +267,6 @@ __device__ void select_row_general(const TUArgs& a, const float* __restrict__ ro
     const bool take = (valid && kp > Tp) || (eq && rank < rem);
     const uint32_t mt = __ballot_sync(FULL, take);
     if (take) out[n_out + __popc(mt & lanemask_lt())] = (int32_t)(j0 + lane);
-    if (lane == 0 && mt) atomicOr(&tile_bits[j0 >> 5], mt);
     n_out += __popc(mt);
     eq_seen += __popc(meq);
   });
@@ -287,8 +294,7 @@ __device__ __forceinline__ int lower_bound_smem(const int32_t* v, int n, int32_t
 
 __device__ void select_row_fast(const TUArgs& a, const float* __restrict__ row, int64_t nh,
                                 uint32_t need, int32_t* out, uint32_t b0, uint32_t above0,
-                                uint32_t cnt0, uint32_t* warp_smem, uint32_t* tile_bits,
-                                int64_t t) {
+                                uint32_t cnt0, uint32_t* warp_smem, int64_t t) {
   const int lane = lane_id();
   uint2* cand = reinterpret_cast<uint2*>(warp_smem);                  // [512] (key, block)
   int32_t* defs = reinterpret_cast<int32_t*>(warp_smem + 2 * FAST_MAX);  // [512] above the bucket
@@ -412,22 +418,251 @@ __device__ void select_row_fast(const TUArgs& a, const float* __restrict__ row, 
   for (uint32_t i = lane; i < n_def; i += 32) {
     const int32_t v = defs[i];
     out[i + lower_bound_smem(csel, (int)n_sel, v)] = v;
-    atomicOr(&tile_bits[v >> 5], 1u << (v & 31));
   }
   for (uint32_t i = lane; i < n_sel; i += 32) {
     const int32_t v = csel[i];
     out[i + lower_bound_smem(defs, (int)n_def, v)] = v;
-    atomicOr(&tile_bits[v >> 5], 1u << (v & 31));
   }
   for (int x = (int)need + lane; x < a.Ks; x += 32) out[x] = -1;
   if (lane == 0 && n_def + n_sel != need) report(a.status, SGQA_ERR_BOUNDS, (int)t);
   __syncwarp();
 }
 
-// Select row t of group g, write its ascending list and OR it into the tile
-// bitmask.  All lanes participate.
-__device__ void select_row(const TUArgs& a, int g, int64_t t, uint32_t* warp_smem,
-                           uint32_t* tile_bits) {
+// ---------------------------------------------------------------------------
+// Candidate path, for rows of 2048 .. 16384 blocks (16-byte aligned) that
+// select at most CAND_NEED_MAX blocks.  A float threshold tf is chosen so that
+// a little more than k/B of the row's scores clear it; one pass over the row
+// compacts every score >= tf into shared memory in block order, and the exact
+// k-th key and the emission are resolved on those candidates, so the row is
+// read once.  {x >= tf} is an upper set of the key order (the key order only
+// splits -0 below +0), so whenever it holds at least k/B blocks it holds the
+// whole selection, ties included; the pass checks that and that the list did
+// not overflow, and otherwise the row takes the histogram path.  The choice
+// of tf only affects speed:
+//  * predicted: from the previous row of the same warp (consecutive queries of
+//    one group), tf = that row's k-th key minus a margin that a per-warp
+//    controller keeps at about 1.3 k/B candidates;
+//  * sampled: 8 adjacent blocks (one 32-byte sector) of every 64 are read and
+//    a radix select on them picks the key ranked at the expected
+//    count of the selection in the sample plus three standard deviations.
+constexpr int CAND_NEED_MAX = 768;
+constexpr int CAND_MAX = 1024;
+constexpr int CAND_OFF = 1024;      // words: candidates / samples start 4 KB into the scratch
+constexpr int SAMP_MAX = 2048;
+static_assert(CAND_OFF * 4 + CAND_MAX * 8 <= WARP_BYTES, "candidate path scratch");
+static_assert(CAND_OFF * 4 + SAMP_MAX * 4 <= WARP_BYTES, "sample scratch");
+
+struct Pred {         // per-warp threshold predictor
+  float kappa;        // previous row's k-th key (as a float, rounded down)
+  float margin;       // tf = kappa - margin
+  bool valid;
+};
+
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
+
+// Radix select on n keys keys[i * stride] in shared memory (1 <= need <= n),
+// with 8-bit digits from the highest bit at which the keys differ, for at most
+// max_levels digits.  On return the need-th largest key has key >> sh == T;
+// keys with a larger prefix rank above it, and `rem` of the `cnt` keys with
+// prefix T complete the top `need` (cnt == rem once the digits resolve it).
+struct Sel {
+  uint32_t T, rem, cnt, kmin;
+  int sh;
+};
+__device__ Sel warp_radix_select(const uint32_t* keys, int stride, uint32_t n, uint32_t need,
+                                 uint32_t* hist, int max_levels) {
+  const int lane = lane_id();
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  for (uint32_t i = lane; i < n; i += 32) {
+    const uint32_t k = keys[i * stride];
+    kmin = min(kmin, k);
+    kmax = max(kmax, k);
+  }
+  kmin = __reduce_min_sync(FULL, kmin);
+  kmax = __reduce_max_sync(FULL, kmax);
+  Sel s;
+  s.rem = need;
+  s.cnt = n;
+  s.kmin = kmin;
+  if (kmin == kmax) {
+    s.T = kmin;
+    s.sh = 0;
+    return s;
+  }
+  const int hb = 31 - __clz(kmin ^ kmax);  // keys agree above bit hb
+  s.sh = hb + 1;
+  s.T = hb == 31 ? 0u : (kmax >> (hb + 1));
+  for (int lv = 0; lv < max_levels && s.cnt != s.rem && s.sh > 0; ++lv) {
+    const int w = s.sh < 8 ? s.sh : 8;
+    const int nsh = s.sh - w;
+    *reinterpret_cast<uint4*>(hist + lane * 8) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(hist + lane * 8 + 4) = make_uint4(0, 0, 0, 0);
+    __syncwarp();
+    for (uint32_t i = lane; i < n; i += 32) {
+      const uint32_t k = keys[i * stride];
+      if (s.sh >= 32 || (k >> s.sh) == s.T) atomicAdd(&hist[(k >> nsh) & ((1u << w) - 1u)], 1u);
+    }
+    __syncwarp();
+    uint32_t b, above;
+    find_bin(hist, 256, s.rem, b, above, s.cnt);
+    s.rem -= above;
+    s.T = (s.sh >= 32 ? 0u : (s.T << w)) | b;
+    s.sh = nsh;
+    __syncwarp();
+  }
+  return s;
+}
+
+// Sampled threshold (as a key): 8 adjacent blocks of every 64 (two lanes per
+// group), ranked at the expected count of the selection in the sample plus
+// three standard deviations.
+__device__ uint32_t sample_tau(const float* __restrict__ row, int64_t nh, uint32_t need,
+                               uint32_t* hist, uint32_t* samp) {
+  const int lane = lane_id();
+  const float4* r4 = reinterpret_cast<const float4*>(row);
+  const int nsg = (int)(nh / 64);
+  const int ns = nsg * 8;
+  for (int base = 0; base < nsg; base += 64) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = base + u * 16 + (lane >> 1);
+      v[u] = q < nsg ? __ldg(r4 + q * 16 + (lane & 1)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = base + u * 16 + (lane >> 1);
+      if (q < nsg)
+        *reinterpret_cast<uint4*>(samp + q * 8 + (lane & 1) * 4) =
+            make_uint4(order_key(v[u].x), order_key(v[u].y), order_key(v[u].z),
+                       order_key(v[u].w));
+    }
+  }
+  __syncwarp();
+  const float e = (float)need * (float)ns / (float)nh;
+  uint32_t r = (uint32_t)ceilf(e + 3.f * sqrtf(e));
+  if (r > (uint32_t)ns) r = ns;
+  if (r < 1) r = 1;
+  const Sel sl = warp_radix_select(samp, 1, ns, r, hist, 2);
+  return sl.sh >= 32 ? sl.kmin : (sl.T << sl.sh);
+}
+
+// Compact every block with score >= tf into cand (key, block), in block order.
+// Returns the count (stops early once it exceeds CAND_MAX).  A batch gives
+// each lane 32 consecutive blocks (8 float4), so a lane's candidates are
+// contiguous in block order and one warp prefix sum per batch places them;
+// loads run one batch ahead of their use.
+__device__ uint32_t cand_pass(const float* __restrict__ row, int64_t nh, float tf, uint2* cand) {
+  const int lane = lane_id();
+  const uint32_t lt = lanemask_lt();
+  const float4* r4 = reinterpret_cast<const float4*>(row);
+  const int64_t n4 = nh / 4;
+  const int64_t nbat = (n4 + 32 * BATCH - 1) / (32 * BATCH);
+  const float qnan = __int_as_float(0x7fffffff);  // never >= tf
+  uint32_t C = 0;
+  auto load = [&](float4 (&v)[BATCH], int64_t bi) {
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int64_t x = bi * (32 * BATCH) + lane * BATCH + u;
+      v[u] = x < n4 ? __ldg(r4 + x) : make_float4(qnan, qnan, qnan, qnan);
+    }
+  };
+  auto proc = [&](const float4 (&v)[BATCH], int64_t bi) {
+    uint32_t fl = 0;
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      fl |= (uint32_t)(v[u].x >= tf) << (4 * u);
+      fl |= (uint32_t)(v[u].y >= tf) << (4 * u + 1);
+      fl |= (uint32_t)(v[u].z >= tf) << (4 * u + 2);
+      fl |= (uint32_t)(v[u].w >= tf) << (4 * u + 3);
+    }
+    if (__any_sync(FULL, fl != 0u)) {
+      const uint32_t c = __popc(fl);
+      uint32_t incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += y;
+      }
+      uint32_t pos = C + incl - c;
+      const uint32_t j0 = (uint32_t)(4 * (bi * (32 * BATCH) + lane * BATCH));
+      if (fl) {
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+          const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if ((fl >> (4 * u + e)) & 1u) {
+              if (pos < (uint32_t)CAND_MAX)
+                cand[pos] = make_uint2(order_key(x[e]), j0 + 4 * u + e);
+              ++pos;
+            }
+        }
+      }
+      C += __shfl_sync(FULL, incl, 31);
+    }
+  };
+  float4 va[BATCH], vb[BATCH];
+  if (nbat > 0) load(va, 0);
+  for (int64_t bi = 0; bi < nbat && C <= (uint32_t)CAND_MAX; bi += 2) {
+    if (bi + 1 < nbat) load(vb, bi + 1);
+    proc(va, bi);
+    if (bi + 1 < nbat && C <= (uint32_t)CAND_MAX) {
+      if (bi + 2 < nbat) load(va, bi + 2);
+      proc(vb, bi + 1);
+    }
+  }
+  {  // the last nh % 4 blocks
+    const int64_t j = n4 * 4 + lane;
+    const float x = j < nh ? __ldg(row + j) : qnan;
+    const bool f = x >= tf;
+    const uint32_t m = __ballot_sync(FULL, f);
+    const uint32_t pos = C + __popc(m & lt);
+    if (f && pos < (uint32_t)CAND_MAX) cand[pos] = make_uint2(order_key(x), (uint32_t)j);
+    C += __popc(m);
+  }
+  __syncwarp();
+  return C;
+}
+
+// Exact selection among C candidates (need <= C <= CAND_MAX, block order):
+// writes the list and returns the k-th key rounded down to its resolved prefix.
+__device__ uint32_t cand_select(const TUArgs& a, const uint2* cand, uint32_t C, uint32_t need,
+                                int32_t* out, uint32_t* hist, int64_t t) {
+  const int lane = lane_id();
+  const uint32_t lt = lanemask_lt();
+  const Sel sl = warp_radix_select(reinterpret_cast<const uint32_t*>(cand), 2, C, need, hist, 4);
+  // emission in block order: above the k-th key's prefix, or equal to it and
+  // among the first `rem` such (all of them when cnt == rem)
+  uint32_t n_out = 0, eq_seen = 0;
+  const bool ties = sl.cnt != sl.rem;
+  for (uint32_t base = 0; base < C; base += 32) {
+    const uint32_t i = base + lane;
+    const bool valid = i < C;
+    const uint2 c = valid ? cand[i] : make_uint2(0u, 0u);
+    const uint32_t kp = sl.sh >= 32 ? 0u : (c.x >> sl.sh);
+    bool take;
+    if (!ties) {
+      take = valid && kp >= sl.T;
+    } else {
+      const bool eq = valid && kp == sl.T;
+      const uint32_t meq = __ballot_sync(FULL, eq);
+      take = (valid && kp > sl.T) || (eq && eq_seen + __popc(meq & lt) < sl.rem);
+      eq_seen += __popc(meq);
+    }
+    const uint32_t mt = __ballot_sync(FULL, take);
+    if (take) out[n_out + __popc(mt & lt)] = (int32_t)c.y;
+    n_out += __popc(mt);
+  }
+  for (int64_t x = need + lane; x < a.Ks; x += 32) out[x] = -1;
+  if (lane == 0 && n_out != need) report(a.status, SGQA_ERR_BOUNDS, (int)t);
+  return sl.sh >= 32 ? sl.kmin : (sl.T << sl.sh);
+}
+
+// Select row t of group g and write its ascending list.  All lanes participate.
+__device__ void select_row(const TUArgs& a, int g, int64_t t, uint32_t* warp_smem, Pred& pr) {
   const int lane = lane_id();
   const int64_t tl = t - a.q_begin;
   int64_t nh = (a.off + t) / a.B;
@@ -436,68 +671,82 @@ __device__ void select_row(const TUArgs& a, int g, int64_t t, uint32_t* warp_sme
   const float* row = a.scores + ((int64_t)g * a.nq + tl) * a.nblk;
   int32_t* out = a.sel + ((int64_t)g * a.nq + tl) * a.Ks;
   const bool vec = (a.nblk & 3) == 0;
-  if (need == 0) {
-    for (int64_t x = lane; x < a.Ks; x += 32) out[x] = -1;
+  if ((int64_t)need == nh) {  // every historical block (or none): no scores to read
+    for (int64_t x = lane; x < a.Ks; x += 32) out[x] = x < nh ? (int32_t)x : -1;
+    pr.valid = false;
     return;
   }
-  if ((int64_t)need == nh) {  // every historical block: no scores to read
-    for (int64_t x = lane; x < nh; x += 32) out[x] = (int32_t)x;
-    for (int64_t w = lane; w < (nh + 31) / 32; w += 32) {
-      const int64_t hi = (w + 1) * 32;
-      atomicOr(&tile_bits[w], hi <= nh ? FULL : ((1u << (nh & 31)) - 1u));
+  if (vec && nh >= 2048 && nh <= 16384 && need <= (uint32_t)CAND_NEED_MAX) {
+    uint32_t* hist = warp_smem;
+    uint2* cand = reinterpret_cast<uint2*>(warp_smem + CAND_OFF);
+    for (int attempt = 0; attempt < 2; ++attempt) {
+      const bool predicted = attempt == 0 && pr.valid;
+      if (attempt == 0 && !pr.valid) continue;
+      float tf;
+      if (predicted) {
+        tf = pr.kappa - pr.margin;
+      } else {
+        tf = key_to_float(sample_tau(row, nh, need, hist, warp_smem + CAND_OFF));
+      }
+      const uint32_t C = cand_pass(row, nh, tf, cand);
+      if (C >= need && C <= (uint32_t)CAND_MAX) {
+        const float kappa = key_to_float(cand_select(a, cand, C, need, out, hist, t));
+        // keep about 1.3 k/B candidates for the next row
+        float margin = predicted ? pr.margin : kappa - tf;
+        if (!(margin > 0.f)) margin = fabsf(kappa) * 1e-3f + 1e-30f;
+        const float ratio = (float)C / (float)need;
+        if (ratio < 1.1f) margin *= 1.5f;
+        else if (ratio > 1.6f) margin *= 0.7f;
+        pr.kappa = kappa;
+        pr.margin = margin;
+        pr.valid = isfinite(kappa) && isfinite(margin);
+        return;
+      }
+      if (predicted) pr.margin *= (C < need) ? 2.f : 0.5f;
     }
-    for (int64_t x = nh + lane; x < a.Ks; x += 32) out[x] = -1;
-    return;
+    pr.valid = false;
   }
-  // level 0: histogram of the top 11 key bits
+  // histogram path: level 0, the top 11 key bits
   uint32_t b0, above0, cnt0;
   zero_hist(warp_smem, NB0);
   hist_row(row, nh, vec, warp_smem, 21, NB0, 32, 0);
   find_bin(warp_smem, NB0, need, b0, above0, cnt0);
   if (vec && need <= (uint32_t)FAST_MAX && cnt0 <= (uint32_t)FAST_MAX)
-    select_row_fast(a, row, nh, need, out, b0, above0, cnt0, warp_smem, tile_bits, t);
+    select_row_fast(a, row, nh, need, out, b0, above0, cnt0, warp_smem, t);
   else
-    select_row_general(a, row, nh, need, out, vec, b0, above0, cnt0, warp_smem, tile_bits, t);
+    select_row_general(a, row, nh, need, out, vec, b0, above0, cnt0, warp_smem, t);
 }
 
-__global__ void k_topk_union(TUArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int g = blockIdx.y;
-  const int64_t tau = a.tau_begin + blockIdx.x;
+// Slot base of tile tau of group g: g * capG + the caps of the layout's
+// earlier tiles.  Every thread calls it; uses `red` (32 words) and one barrier.
+__device__ int64_t tile_slot_base(const TUArgs& a, int g, int64_t tau, int64_t* red) {
+  const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
   const int nthr = blockDim.x;
-  const int tid = threadIdx.x, warp = warp_id(), lane = lane_id();
-  uint32_t* tile_bits = reinterpret_cast<uint32_t*>(smem);
-  uint32_t* wprefix = tile_bits + ((a.nwords + 3) & ~3);          // nwords + 1 entries
-  uint8_t* wbase = reinterpret_cast<uint8_t*>(wprefix + ((a.nwords + 1 + 3) & ~3));
-  __shared__ int64_t s_red[32];
-  __shared__ int64_t s_base;
-
-  for (int i = tid; i < a.nwords; i += nthr) tile_bits[i] = 0;
-
-  // slot base of this tile: g * capG + sum of the caps of the layout's earlier tiles
   int64_t part = 0;
   for (int64_t x = a.lay_tau0 + tid; x < tau; x += nthr) part += cap_of_tile(a, x);
   for (int o = 16; o > 0; o >>= 1) part += __shfl_down_sync(FULL, part, o);
-  if (lane == 0) s_red[warp] = part;
+  if (lane == 0) red[warp] = part;
   __syncthreads();
-  if (tid == 0) {
-    int64_t s = 0;
-    for (int w = 0; w < a.nw; ++w) s += s_red[w];
-    s_base = (int64_t)g * a.capG + s;
-  }
+  int64_t s = 0;
+  for (int w = 0; w < (nthr >> 5); ++w) s += red[w];
+  return (int64_t)g * a.capG + s;
+}
 
-  // ---- per-row selection
-  const int64_t first = tau * a.W;
-  int len = (int)((a.T - first) < a.W ? (a.T - first) : a.W);
-  uint32_t* wsm = reinterpret_cast<uint32_t*>(wbase + (size_t)warp * WARP_BYTES);
-  for (int i = warp; i < len; i += a.nw) select_row(a, g, first + i, wsm, tile_bits);
+// After every row of the tile has OR-ed its blocks into tile_bits: write the
+// union list (ascending) and, per union slot, the mask of the tile's queries
+// that selected it.  `mspace` (mask_pairs lo/hi word pairs) is shared scratch
+// for the masks; longer unions use global atomics.  Starts with a barrier.
+__device__ void finish_tile(const TUArgs& a, int g, int64_t tau, int64_t base, int len,
+                            uint32_t* tile_bits, uint32_t* wprefix, uint32_t* mspace,
+                            int64_t mask_pairs) {
+  const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
+  const int nthr = blockDim.x, nw = nthr >> 5;
   __syncthreads();
-
-  // ---- union list: ranks from a prefix sum of word popcounts
+  // ranks from a prefix sum of word popcounts
   if (warp == 0) {
     uint32_t carry = 0;
-    for (int base = 0; base < a.nwords; base += 32) {
-      const int w = base + lane;
+    for (int b0 = 0; b0 < a.nwords; b0 += 32) {
+      const int w = b0 + lane;
       const uint32_t c = w < a.nwords ? __popc(tile_bits[w]) : 0u;
       uint32_t incl = c;
 #pragma unroll
@@ -512,7 +761,6 @@ __global__ void k_topk_union(TUArgs a) {
   }
   __syncthreads();
   const int64_t U = wprefix[a.nwords];
-  const int64_t base = s_base;
   const int64_t cap = cap_of_tile(a, tau);
   const int64_t lt = (int64_t)g * a.lay_ntiles + (tau - a.lay_tau0);
   if (U > cap || base + U > a.ucap) {
@@ -532,11 +780,9 @@ __global__ void k_topk_union(TUArgs a) {
       bits &= bits - 1;
     }
   }
-
-  // ---- member masks
-  const int64_t mask_words = (int64_t)a.nw * WARP_BYTES / 8;  // lo/hi pairs that fit
-  const bool in_smem = U <= mask_words;
-  uint32_t* mlo = reinterpret_cast<uint32_t*>(wbase);
+  // member masks
+  const bool in_smem = U <= mask_pairs;
+  uint32_t* mlo = mspace;
   uint32_t* mhi = mlo + (in_smem ? U : 0);
   if (in_smem) {
     for (int64_t s = tid; s < 2 * U; s += nthr) mlo[s] = 0;
@@ -544,7 +790,8 @@ __global__ void k_topk_union(TUArgs a) {
     for (int64_t s = tid; s < U; s += nthr) a.umask[base + s] = 0;
   }
   __syncthreads();
-  for (int i = warp; i < len; i += a.nw) {
+  const int64_t first = tau * a.W;
+  for (int i = warp; i < len; i += nw) {
     const int64_t t = first + i;
     int64_t nh = (a.off + t) / a.B;
     if (nh > a.nblk) nh = a.nblk;
@@ -557,8 +804,7 @@ __global__ void k_topk_union(TUArgs a) {
       if (in_smem) {
         atomicOr(i < 32 ? &mlo[slot] : &mhi[slot], 1u << (i & 31));
       } else {
-        atomicOr(reinterpret_cast<unsigned long long*>(&a.umask[base + slot]),
-                 1ull << i);
+        atomicOr(reinterpret_cast<unsigned long long*>(&a.umask[base + slot]), 1ull << i);
       }
     }
   }
@@ -570,6 +816,72 @@ __global__ void k_topk_union(TUArgs a) {
     a.uoff[lt] = base;
     a.ulen[lt] = (int32_t)U;
   }
+}
+
+// Row kernel: the rows of every group are cut into blocks of 8 consecutive
+// queries; warp w of the grid takes blocks w, w + (warps in the grid), ...
+// (persistent CTAs, so all SMs stay busy however many tiles there are), and
+// carries its threshold predictor from row to row within a block.
+constexpr int ROW_BLOCK = 8;
+constexpr int ROW_WARPS = 4;  // per CTA: 4 x 12 KB of scratch, four CTAs per SM
+
+__global__ void __launch_bounds__(ROW_WARPS * 32, 4) k_topk_rows(TUArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int warp = warp_id();
+  uint32_t* wsm = reinterpret_cast<uint32_t*>(smem + (size_t)warp * WARP_BYTES);
+  const int64_t nwt = (int64_t)gridDim.x * ROW_WARPS;
+  const int64_t bpg = (a.nq + ROW_BLOCK - 1) / ROW_BLOCK;  // row blocks per group
+  for (int64_t b = (int64_t)blockIdx.x * ROW_WARPS + warp; b < bpg * a.Hkv; b += nwt) {
+    const int g = (int)(b / bpg);
+    const int64_t r0 = (b % bpg) * ROW_BLOCK;
+    const int64_t r1 = r0 + ROW_BLOCK < a.nq ? r0 + ROW_BLOCK : a.nq;
+    Pred pr;
+    pr.valid = false;
+    for (int64_t r = r0; r < r1; ++r) select_row(a, g, a.q_begin + r, wsm, pr);
+  }
+}
+
+// Tile kernel: one CTA per (tile, group) ORs the tile's lists into its block
+// bitmask and writes the union and the member masks.
+constexpr int UNION_THREADS = 256;
+
+__global__ void __launch_bounds__(UNION_THREADS) k_tile_union(TUArgs a, int64_t mask_pairs) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int g = blockIdx.y;
+  const int64_t tau = a.tau_begin + blockIdx.x;
+  const int tid = threadIdx.x, warp = warp_id(), lane = lane_id();
+  constexpr int nw = UNION_THREADS / 32;
+  uint32_t* tile_bits = reinterpret_cast<uint32_t*>(smem);
+  uint32_t* wprefix = tile_bits + ((a.nwords + 3) & ~3);          // nwords + 1 entries
+  uint32_t* mspace = wprefix + ((a.nwords + 1 + 3) & ~3);
+  __shared__ int64_t s_red[32];
+
+  for (int i = tid; i < a.nwords; i += UNION_THREADS) tile_bits[i] = 0;
+  const int64_t base = tile_slot_base(a, g, tau, s_red);  // ends with a barrier
+  const int64_t first = tau * a.W;
+  const int len = (int)((a.T - first) < a.W ? (a.T - first) : a.W);
+  for (int i = warp; i < len; i += nw) {
+    const int64_t t = first + i;
+    int64_t nh = (a.off + t) / a.B;
+    if (nh > a.nblk) nh = a.nblk;
+    const int need = (int)(nh < a.Ks ? nh : a.Ks);
+    const int32_t* lst = a.sel + ((int64_t)g * a.nq + (t - a.q_begin)) * a.Ks;
+    // each lane ORs a contiguous piece of the ascending list, one atomic per word run
+    const int per = (need + 31) / 32;
+    const int x1 = min(need, (lane + 1) * per);
+    uint32_t word = 0xffffffffu, bits = 0;
+    for (int x = lane * per; x < x1; ++x) {
+      const int32_t j = lst[x];
+      if ((uint32_t)(j >> 5) != word) {
+        if (bits) atomicOr(&tile_bits[word], bits);
+        word = (uint32_t)(j >> 5);
+        bits = 0;
+      }
+      bits |= 1u << (j & 31);
+    }
+    if (bits) atomicOr(&tile_bits[word], bits);
+  }
+  finish_tile(a, g, tau, base, len, tile_bits, wprefix, mspace, mask_pairs);
 }
 
 }  // namespace
@@ -609,22 +921,37 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
   a.tau_begin = q_begin / dm.W;
   a.nwords = (int)((dm.nblk + 31) / 32);
   a.status = status;
+  a.Hkv = dm.Hkv;
+  a.nw = ROW_WARPS;
+  // rows: persistent CTAs, at most four per SM
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
+    return SGQA_ERR_CUDA;
+  const int64_t row_blocks = (a.nq + ROW_BLOCK - 1) / ROW_BLOCK * dm.Hkv;
+  const int64_t row_ctas =
+      std::min<int64_t>((row_blocks + ROW_WARPS - 1) / ROW_WARPS, (int64_t)nsm * 4);
+  const size_t row_smem = (size_t)ROW_WARPS * WARP_BYTES;
+  // tiles: bitmask + word prefix + member masks (shared while they fit)
   const int64_t tau_end = (q_end + dm.W - 1) / dm.W;
   const size_t fixed = (size_t)(((a.nwords + 3) & ~3) + ((a.nwords + 1 + 3) & ~3)) * 4;
   const size_t budget = 200 * 1024;
-  if (fixed + WARP_BYTES > budget) return SGQA_ERR_UNSUPPORTED;
-  int nw = (int)((budget - fixed) / WARP_BYTES);
-  if (nw > 8) nw = 8;  // 8 warps and ~70 KB: three CTAs share an SM
-  if (nw > dm.W) nw = dm.W < 1 ? 1 : dm.W;
-  if (nw < 1) nw = 1;
-  a.nw = nw;
-  const size_t smem = fixed + (size_t)nw * WARP_BYTES;
-  if (cudaFuncSetAttribute(k_topk_union, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+  if (fixed + 1024 > budget) return SGQA_ERR_UNSUPPORTED;
+  const int64_t u_max = std::min<int64_t>((int64_t)dm.W * dm.Ks, dm.nblk);  // slots of a tile
+  const int64_t mask_pairs = std::min<int64_t>(u_max, (int64_t)((budget - fixed) / 8));
+  const size_t union_smem = fixed + (size_t)mask_pairs * 8;
+  if (cudaFuncSetAttribute(k_topk_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)row_smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k_tile_union, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)union_smem) != cudaSuccess)
     return SGQA_ERR_CUDA;
-  dim3 grid((unsigned)(tau_end - a.tau_begin), (unsigned)dm.Hkv);
   log_begin(SGQA_K_TOPK_UNION, st);
-  k_topk_union<<<grid, nw * 32, smem, st>>>(a);
+  k_topk_rows<<<(unsigned)row_ctas, ROW_WARPS * 32, row_smem, st>>>(a);
+  log_end(st);
+  if (cudaGetLastError() != cudaSuccess) return SGQA_ERR_CUDA;
+  log_begin(SGQA_K_TOPK_UNION, st);
+  k_tile_union<<<dim3((unsigned)(tau_end - a.tau_begin), (unsigned)dm.Hkv), UNION_THREADS,
+                 union_smem, st>>>(a, mask_pairs);
   log_end(st);
   return cudaGetLastError() == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA;
 }

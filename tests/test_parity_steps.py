@@ -177,6 +177,42 @@ def test_topk_union_degenerate_scores(s, case):
     assert _gpu_union_lists(s, p, uo, ul, ub, um) == _oracle_union_lists(*ref_u)
 
 
+@pytest.mark.parametrize("case", ["clustered", "clustered_ties", "iid", "sample_low", "sample_high"])
+@pytest.mark.parametrize("Ks", [512, 37])
+def test_topk_union_long_rows(s, case, Ks):
+    """Rows of 10000+ blocks: the sampled-threshold select (a sample of 8 in
+    every 64 blocks sets a candidate threshold), including samples that are
+    unrepresentative on purpose, so the candidates miss or overflow and the row
+    falls back to the histogram select.  Bit-exact against the oracle."""
+    T, B, off, Hkv, W = 128, 8, 80000, 2, 64
+    wl = synth.Workload("long", T, off + T, off, 8, Hkv, 128, B, Ks * B, W, "bf16", "normal")
+    p = s.params_for(wl)
+    nb = wl.n_blocks
+    rng = np.random.default_rng(11)
+    # scores of clustered blocks: runs of 64 blocks share a level
+    level = np.repeat(rng.normal(0.0, 1.0, (Hkv, 1, nb // 64 + 1)), 64, axis=2)[:, :, :nb]
+    S = level + 0.3 * rng.normal(0.0, 1.0, (Hkv, T, nb))
+    if case == "clustered_ties":
+        S = np.round(S * 8.0) / 8.0
+    elif case == "iid":
+        S = rng.normal(0.0, 1.0, (Hkv, T, nb))
+    elif case in ("sample_low", "sample_high"):
+        sampled = (np.arange(nb) % 64) < 8
+        S = rng.normal(0.0, 1.0, (Hkv, T, nb))
+        S[:, :, sampled] += -6.0 if case == "sample_low" else 6.0
+    S32 = np.ascontiguousarray(S, np.float32)
+    rows = np.arange(T)
+    ref_sel = oracle.select(S32, B, off, rows, Ks)
+    ref_u = oracle.union(ref_sel, W, nb)
+    sel = torch.empty(Hkv, T, Ks, dtype=torch.int32, device="cuda")
+    uo, ul, ub, um = s.alloc_union(p)
+    st = s.new_status()
+    s.sgqa_topk_union(p, torch.from_numpy(S32).cuda(), 0, T, sel, uo, ul, ub, um, status=st)
+    assert s.read_status(st)[0] == 0
+    assert np.array_equal(sel.cpu().numpy(), ref_sel)
+    assert _gpu_union_lists(s, p, uo, ul, ub, um) == _oracle_union_lists(*ref_u)
+
+
 @pytest.mark.parametrize("name", list(SMALL))
 @pytest.mark.parametrize("mode", [0, 1])
 def test_sparse_attn_given_lists(s, name, mode):
