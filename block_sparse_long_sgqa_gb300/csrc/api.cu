@@ -464,7 +464,7 @@ SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int
     const int64_t nchunks = (dm.T + chunk - 1) / chunk;
     int64_t n = (dm.nblk > 0 ? 1 : 0) + (dm.dtype == SGQA_FP32 ? (dm.B >= 8 ? 1 : 3) : 0) +
                 (dm.B >= 8 ? 2 : 0);
-    n += nchunks * ((dm.nblk > 0 ? 2 : 0) + 3);
+    n += nchunks * ((dm.nblk > 0 ? 2 : 0) + topk_union_launches(dm) + 1);
     *launches = (int32_t)n;
   }
   return SGQA_OK;

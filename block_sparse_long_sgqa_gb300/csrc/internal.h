@@ -78,6 +78,8 @@ int launch_index_scores(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfl
                         cudaStream_t st);
 
 size_t topk_union_ws_bytes(const Dims& dm, int64_t nq);
+// Kernel launches of one top-k/union call (aligned score buffers).
+int topk_union_launches(const Dims& dm);
 int launch_topk_union(const Dims& dm, const float* scores, int64_t q_begin, int64_t q_end,
                       int32_t* sel, int64_t* union_off, int32_t* union_len, int32_t* union_blk,
                       uint64_t* union_mask, int64_t union_cap, int32_t* status, cudaStream_t st);

@@ -44,6 +44,7 @@ struct TUArgs {
   const float* scores;  // [Hkv][nq][nblk], rows q_begin .. q_end-1 of the call
   int64_t nq, q_begin, q_end, T, off, nblk;
   int B, Ks, W, Hkv;
+  int lgB;              // log2(B): block sizes are powers of two
   int32_t* sel;         // [Hkv][nq][Ks]
   int64_t* uoff;        // [Hkv][lay_ntiles]
   int32_t* ulen;
@@ -63,7 +64,7 @@ __device__ __forceinline__ int64_t cap_of_tile(const TUArgs& a, int64_t tau) {
   const int64_t first = tau * a.W;
   int64_t len = a.T - first;
   if (len > a.W) len = a.W;
-  int64_t nh = (a.off + first + len - 1) / a.B;
+  int64_t nh = (a.off + first + len - 1) >> a.lgB;
   if (nh > a.nblk) nh = a.nblk;
   const int64_t k = len * a.Ks;
   return k < nh ? k : nh;
@@ -448,6 +449,7 @@ __device__ void select_row_fast(const TUArgs& a, const float* __restrict__ row, 
 constexpr int CAND_NEED_MAX = 768;
 constexpr int CAND_MAX = 1024;
 constexpr int CAND_OFF = 1024;      // words: candidates / samples start 4 KB into the scratch
+                                    // (the first 4 KB: pass staging, then select histogram)
 constexpr int SAMP_MAX = 2048;
 static_assert(CAND_OFF * 4 + CAND_MAX * 8 <= WARP_BYTES, "candidate path scratch");
 static_assert(CAND_OFF * 4 + SAMP_MAX * 4 <= WARP_BYTES, "sample scratch");
@@ -552,9 +554,14 @@ __device__ uint32_t sample_tau(const float* __restrict__ row, int64_t nh, uint32
 // Compact every block with score >= tf into cand (key, block), in block order.
 // Returns the count (stops early once it exceeds CAND_MAX).  A batch gives
 // each lane 32 consecutive blocks (8 float4), so a lane's candidates are
-// contiguous in block order and one warp prefix sum per batch places them;
-// loads run one batch ahead of their use.
-__device__ uint32_t cand_pass(const float* __restrict__ row, int64_t nh, float tf, uint2* cand) {
+// contiguous in block order and one warp prefix sum per batch places them.
+// The batch is staged in shared memory (rows swizzled by lane, so the 16-byte
+// stores of 8 lanes hit distinct banks), and the warp then writes the
+// batch's candidates 32 at a time, lane i taking the i-th: its source lane
+// comes from a binary search over the prefix sums and its block from the
+// source lane's flag word.  Loads run one batch ahead of their use.
+__device__ uint32_t cand_pass(const float* __restrict__ row, int64_t nh, float tf, uint2* cand,
+                              float* stage) {
   const int lane = lane_id();
   const uint32_t lt = lanemask_lt();
   const float4* r4 = reinterpret_cast<const float4*>(row);
@@ -578,31 +585,39 @@ __device__ uint32_t cand_pass(const float* __restrict__ row, int64_t nh, float t
       fl |= (uint32_t)(v[u].z >= tf) << (4 * u + 2);
       fl |= (uint32_t)(v[u].w >= tf) << (4 * u + 3);
     }
-    if (__any_sync(FULL, fl != 0u)) {
-      const uint32_t c = __popc(fl);
-      uint32_t incl = c;
+    if (!__any_sync(FULL, fl != 0u)) return;
+    const uint32_t c = __popc(fl);
+    uint32_t incl = c;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(FULL, incl, o);
-        if (lane >= o) incl += y;
-      }
-      uint32_t pos = C + incl - c;
-      const uint32_t j0 = (uint32_t)(4 * (bi * (32 * BATCH) + lane * BATCH));
-      if (fl) {
-#pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-          const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if ((fl >> (4 * u + e)) & 1u) {
-              if (pos < (uint32_t)CAND_MAX)
-                cand[pos] = make_uint2(order_key(x[e]), j0 + 4 * u + e);
-              ++pos;
-            }
-        }
-      }
-      C += __shfl_sync(FULL, incl, 31);
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += y;
     }
+    const uint32_t tot = __shfl_sync(FULL, incl, 31);
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u)
+      *reinterpret_cast<float4*>(stage + lane * 32 + ((u ^ (lane & 7)) << 2)) = v[u];
+    __syncwarp();
+    const uint32_t jb = (uint32_t)(4 * bi * (32 * BATCH));
+    for (uint32_t r0 = 0; r0 < tot; r0 += 32) {
+      const uint32_t i = r0 + lane;  // the batch's i-th candidate
+      int src = 0;                   // first lane whose inclusive count exceeds i
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const uint32_t pv = __shfl_sync(FULL, incl, src + o - 1);
+        if (pv <= i) src += o;
+      }
+      const uint32_t ex = __shfl_sync(FULL, incl, src) - __shfl_sync(FULL, c, src);
+      const uint32_t fs = __shfl_sync(FULL, fl, src);
+      if (i < tot) {
+        const uint32_t k = __fns(fs, 0, (int)(i - ex) + 1);  // bit of the (i-ex)-th set flag
+        const float x = stage[src * 32 + (((k >> 2) ^ (src & 7)) << 2) + (k & 3)];
+        if (C + i < (uint32_t)CAND_MAX)
+          cand[C + i] = make_uint2(order_key(x), jb + (uint32_t)src * 32 + k);
+      }
+    }
+    __syncwarp();
+    C += tot;
   };
   float4 va[BATCH], vb[BATCH];
   if (nbat > 0) load(va, 0);
@@ -665,7 +680,7 @@ __device__ uint32_t cand_select(const TUArgs& a, const uint2* cand, uint32_t C, 
 __device__ void select_row(const TUArgs& a, int g, int64_t t, uint32_t* warp_smem, Pred& pr) {
   const int lane = lane_id();
   const int64_t tl = t - a.q_begin;
-  int64_t nh = (a.off + t) / a.B;
+  int64_t nh = (a.off + t) >> a.lgB;
   if (nh > a.nblk) nh = a.nblk;
   const uint32_t need = (uint32_t)(nh < a.Ks ? nh : a.Ks);
   const float* row = a.scores + ((int64_t)g * a.nq + tl) * a.nblk;
@@ -688,7 +703,7 @@ __device__ void select_row(const TUArgs& a, int g, int64_t t, uint32_t* warp_sme
       } else {
         tf = key_to_float(sample_tau(row, nh, need, hist, warp_smem + CAND_OFF));
       }
-      const uint32_t C = cand_pass(row, nh, tf, cand);
+      const uint32_t C = cand_pass(row, nh, tf, cand, reinterpret_cast<float*>(warp_smem));
       if (C >= need && C <= (uint32_t)CAND_MAX) {
         const float kappa = key_to_float(cand_select(a, cand, C, need, out, hist, t));
         // keep about 1.3 k/B candidates for the next row
@@ -793,7 +808,7 @@ __device__ void finish_tile(const TUArgs& a, int g, int64_t tau, int64_t base, i
   const int64_t first = tau * a.W;
   for (int i = warp; i < len; i += nw) {
     const int64_t t = first + i;
-    int64_t nh = (a.off + t) / a.B;
+    int64_t nh = (a.off + t) >> a.lgB;
     if (nh > a.nblk) nh = a.nblk;
     const int64_t need = nh < a.Ks ? nh : a.Ks;
     const int32_t* lst = a.sel + ((int64_t)g * a.nq + (t - a.q_begin)) * a.Ks;
@@ -823,6 +838,19 @@ __device__ void finish_tile(const TUArgs& a, int g, int64_t tau, int64_t base, i
 // (persistent CTAs, so all SMs stay busy however many tiles there are), and
 // carries its threshold predictor from row to row within a block.
 constexpr int ROW_BLOCK = 8;
+
+// Bulk prefetch into L2 of the scores of local row r of group g (the blocks
+// the select reads, rounded up to 16 bytes; rows start 16-byte aligned when
+// nblk % 4 == 0, otherwise nothing is prefetched).
+__device__ __forceinline__ void prefetch_row_l2(const TUArgs& a, int g, int64_t r) {
+  if (a.nblk & 3) return;
+  int64_t nh = (a.off + a.q_begin + r) >> a.lgB;
+  if (nh > a.nblk) nh = a.nblk;
+  if (nh <= a.Ks) return;  // rows that take every block read no scores
+  const uint32_t bytes = (uint32_t)(((nh + 3) & ~int64_t(3)) * 4);
+  const float* p = a.scores + ((int64_t)g * a.nq + r) * a.nblk;
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 constexpr int ROW_WARPS = 4;  // per CTA: 4 x 12 KB of scratch, four CTAs per SM
 
 __global__ void __launch_bounds__(ROW_WARPS * 32, 4) k_topk_rows(TUArgs a) {
@@ -837,7 +865,12 @@ __global__ void __launch_bounds__(ROW_WARPS * 32, 4) k_topk_rows(TUArgs a) {
     const int64_t r1 = r0 + ROW_BLOCK < a.nq ? r0 + ROW_BLOCK : a.nq;
     Pred pr;
     pr.valid = false;
-    for (int64_t r = r0; r < r1; ++r) select_row(a, g, a.q_begin + r, wsm, pr);
+    if (lane_id() == 0) prefetch_row_l2(a, g, r0);
+    for (int64_t r = r0; r < r1; ++r) {
+      // the next row streams into L2 while this one is selected
+      if (lane_id() == 0 && r + 1 < r1) prefetch_row_l2(a, g, r + 1);
+      select_row(a, g, a.q_begin + r, wsm, pr);
+    }
   }
 }
 
@@ -862,7 +895,7 @@ __global__ void __launch_bounds__(UNION_THREADS) k_tile_union(TUArgs a, int64_t 
   const int len = (int)((a.T - first) < a.W ? (a.T - first) : a.W);
   for (int i = warp; i < len; i += nw) {
     const int64_t t = first + i;
-    int64_t nh = (a.off + t) / a.B;
+    int64_t nh = (a.off + t) >> a.lgB;
     if (nh > a.nblk) nh = a.nblk;
     const int need = (int)(nh < a.Ks ? nh : a.Ks);
     const int32_t* lst = a.sel + ((int64_t)g * a.nq + (t - a.q_begin)) * a.Ks;
@@ -886,6 +919,8 @@ __global__ void __launch_bounds__(UNION_THREADS) k_tile_union(TUArgs a, int64_t 
 
 }  // namespace
 
+int topk_union_launches(const Dims&) { return 2; }
+
 size_t topk_union_ws_bytes(const Dims& dm, int64_t nq) {
   return (size_t)dm.Hkv * nq * (dm.Ks > 0 ? dm.Ks : 1) * sizeof(int32_t);
 }
@@ -907,6 +942,7 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
   a.off = dm.off;
   a.nblk = dm.nblk;
   a.B = dm.B;
+  a.lgB = __builtin_ctz((unsigned)dm.B);
   a.Ks = dm.Ks;
   a.W = dm.W;
   a.sel = sel;
@@ -923,6 +959,7 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
   a.status = status;
   a.Hkv = dm.Hkv;
   a.nw = ROW_WARPS;
+  const int64_t tau_end = (q_end + dm.W - 1) / dm.W;
   // rows: persistent CTAs, at most four per SM
   int dev = 0, nsm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -933,7 +970,6 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
       std::min<int64_t>((row_blocks + ROW_WARPS - 1) / ROW_WARPS, (int64_t)nsm * 4);
   const size_t row_smem = (size_t)ROW_WARPS * WARP_BYTES;
   // tiles: bitmask + word prefix + member masks (shared while they fit)
-  const int64_t tau_end = (q_end + dm.W - 1) / dm.W;
   const size_t fixed = (size_t)(((a.nwords + 3) & ~3) + ((a.nwords + 1 + 3) & ~3)) * 4;
   const size_t budget = 200 * 1024;
   if (fixed + 1024 > budget) return SGQA_ERR_UNSUPPORTED;

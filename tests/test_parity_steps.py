@@ -179,13 +179,18 @@ def test_topk_union_degenerate_scores(s, case):
 
 @pytest.mark.parametrize("case", ["clustered", "clustered_ties", "iid", "sample_low", "sample_high"])
 @pytest.mark.parametrize("Ks", [512, 37])
-def test_topk_union_long_rows(s, case, Ks):
-    """Rows of 10000+ blocks: the sampled-threshold select (a sample of 8 in
-    every 64 blocks sets a candidate threshold), including samples that are
-    unrepresentative on purpose, so the candidates miss or overflow and the row
-    falls back to the histogram select.  Bit-exact against the oracle."""
+@pytest.mark.parametrize("kv_extra", [0, 80000])
+def test_topk_union_long_rows(s, case, Ks, kv_extra):
+    """Rows of 10000+ blocks, bit-exact against the oracle.  With kv_extra = 0
+    the rows fit the shared-memory row kernel (threshold predicted from the
+    previous row, else the exact radix select on the row); with a longer key
+    range (20016 blocks) the warp-per-row kernel runs its candidate path (a
+    sample of 8 in every 64 blocks, or the previous row, sets the threshold).
+    Some scores are unrepresentative on purpose, so that candidates miss or
+    overflow and rows fall back to the exact selects."""
     T, B, off, Hkv, W = 128, 8, 80000, 2, 64
-    wl = synth.Workload("long", T, off + T, off, 8, Hkv, 128, B, Ks * B, W, "bf16", "normal")
+    wl = synth.Workload("long", T, off + T + kv_extra, off, 8, Hkv, 128, B, Ks * B, W, "bf16",
+                        "normal")
     p = s.params_for(wl)
     nb = wl.n_blocks
     rng = np.random.default_rng(11)
