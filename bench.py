@@ -423,7 +423,7 @@ def main(argv=None):
     dominant = max(kernels, key=lambda n: kernels[n]["ms_per_step"])
     dk = kernels[dominant]
     src_of = {"sparse_attn": "attn.cu", "index_scores": "index_gemm.cu",
-              "topk_union": "topk_union.cu", "merge": "merge.cu"}
+              "topk_union": "topk_union.cu", "tile_union": "topk_union.cu", "merge": "merge.cu"}
     traffic = traffic_from_profiles(src_of.get(dominant, ""), wl.name)
     if dominant in ("sparse_attn", "index_scores"):
         roofline = {"kernel": dominant, "bound": "tensor", "achieved": dk["achieved_tflops"],

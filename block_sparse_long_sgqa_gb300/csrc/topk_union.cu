@@ -122,7 +122,7 @@ __device__ __forceinline__ void zero_hist(uint32_t* hist, int nbins) {
 
 // Histogram of (key >> shift) & (nbins-1) over row keys whose key >> pshift == pval
 // (no filter when pshift == 32).  Loads 8 float4 per lane before using them.
-__device__ void hist_row(const float* __restrict__ row, int64_t nh, bool vec, uint32_t* hist,
+__device__ __noinline__ void hist_row(const float* __restrict__ row, int64_t nh, bool vec, uint32_t* hist,
                          int shift, int nbins, int pshift, uint32_t pval) {
   const int lane = lane_id();
   const uint32_t bm = nbins - 1;
@@ -197,7 +197,7 @@ __device__ __forceinline__ void ordered_pass(const float* __restrict__ row, int6
 // it, cnt0 keys in it).  Refines inside the bucket (from shared memory when
 // the bucket fits, else by re-reading the row) and emits the list with a
 // full ascending pass over the row.
-__device__ void select_row_general(const TUArgs& a, const float* __restrict__ row, int64_t nh,
+__device__ __noinline__ void select_row_general(const TUArgs& a, const float* __restrict__ row, int64_t nh,
                                    uint32_t need, int32_t* out, bool vec, uint32_t b0,
                                    uint32_t above0, uint32_t cnt0, uint32_t* warp_smem,
                                    int64_t t) {
@@ -293,7 +293,7 @@ __device__ __forceinline__ int lower_bound_smem(const int32_t* v, int n, int32_t
   return lo;
 }
 
-__device__ void select_row_fast(const TUArgs& a, const float* __restrict__ row, int64_t nh,
+__device__ __noinline__ void select_row_fast(const TUArgs& a, const float* __restrict__ row, int64_t nh,
                                 uint32_t need, int32_t* out, uint32_t b0, uint32_t above0,
                                 uint32_t cnt0, uint32_t* warp_smem, int64_t t) {
   const int lane = lane_id();
@@ -520,7 +520,7 @@ __device__ Sel warp_radix_select(const uint32_t* keys, int stride, uint32_t n, u
 // Sampled threshold (as a key): 8 adjacent blocks of every 64 (two lanes per
 // group), ranked at the expected count of the selection in the sample plus
 // three standard deviations.
-__device__ uint32_t sample_tau(const float* __restrict__ row, int64_t nh, uint32_t need,
+__device__ __noinline__ uint32_t sample_tau(const float* __restrict__ row, int64_t nh, uint32_t need,
                                uint32_t* hist, uint32_t* samp) {
   const int lane = lane_id();
   const float4* r4 = reinterpret_cast<const float4*>(row);
@@ -619,15 +619,15 @@ __device__ uint32_t cand_pass(const float* __restrict__ row, int64_t nh, float t
     __syncwarp();
     C += tot;
   };
-  float4 va[BATCH], vb[BATCH];
-  if (nbat > 0) load(va, 0);
-  for (int64_t bi = 0; bi < nbat && C <= (uint32_t)CAND_MAX; bi += 2) {
-    if (bi + 1 < nbat) load(vb, bi + 1);
-    proc(va, bi);
-    if (bi + 1 < nbat && C <= (uint32_t)CAND_MAX) {
-      if (bi + 2 < nbat) load(va, bi + 2);
-      proc(vb, bi + 1);
-    }
+  // one copy of the batch body (a compact loop keeps the instruction cache warm)
+  float4 cur[BATCH], nxt[BATCH];
+  if (nbat > 0) load(cur, 0);
+#pragma unroll 1
+  for (int64_t bi = 0; bi < nbat && C <= (uint32_t)CAND_MAX; ++bi) {
+    if (bi + 1 < nbat) load(nxt, bi + 1);
+    proc(cur, bi);
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) cur[u] = nxt[u];
   }
   {  // the last nh % 4 blocks
     const int64_t j = n4 * 4 + lane;
@@ -644,7 +644,7 @@ __device__ uint32_t cand_pass(const float* __restrict__ row, int64_t nh, float t
 
 // Exact selection among C candidates (need <= C <= CAND_MAX, block order):
 // writes the list and returns the k-th key rounded down to its resolved prefix.
-__device__ uint32_t cand_select(const TUArgs& a, const uint2* cand, uint32_t C, uint32_t need,
+__device__ __noinline__ uint32_t cand_select(const TUArgs& a, const uint2* cand, uint32_t C, uint32_t need,
                                 int32_t* out, uint32_t* hist, int64_t t) {
   const int lane = lane_id();
   const uint32_t lt = lanemask_lt();
@@ -753,7 +753,7 @@ __device__ int64_t tile_slot_base(const TUArgs& a, int g, int64_t tau, int64_t* 
 // for the masks; longer unions use global atomics.  Starts with a barrier.
 __device__ void finish_tile(const TUArgs& a, int g, int64_t tau, int64_t base, int len,
                             uint32_t* tile_bits, uint32_t* wprefix, uint32_t* mspace,
-                            int64_t mask_pairs) {
+                            int64_t mask_pairs, const uint16_t* lists = nullptr) {
   const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
   const int nthr = blockDim.x, nw = nthr >> 5;
   __syncthreads();
@@ -812,14 +812,24 @@ __device__ void finish_tile(const TUArgs& a, int g, int64_t tau, int64_t base, i
     if (nh > a.nblk) nh = a.nblk;
     const int64_t need = nh < a.Ks ? nh : a.Ks;
     const int32_t* lst = a.sel + ((int64_t)g * a.nq + (t - a.q_begin)) * a.Ks;
-    for (int64_t x = lane; x < need; x += 32) {
-      const int32_t j = lst[x];
-      const int w = j >> 5;
-      const int64_t slot = wprefix[w] + __popc(tile_bits[w] & ((1u << (j & 31)) - 1u));
-      if (in_smem) {
-        atomicOr(i < 32 ? &mlo[slot] : &mhi[slot], 1u << (i & 31));
-      } else {
-        atomicOr(reinterpret_cast<unsigned long long*>(&a.umask[base + slot]), 1ull << i);
+    for (int64_t xb = 0; xb < need; xb += 32 * 8) {  // 8 coalesced loads in flight per lane
+      int32_t jj[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t x = xb + u * 32 + lane;
+        jj[u] = x < need ? (lists ? (int32_t)lists[(int64_t)i * a.Ks + x] : lst[x]) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int32_t j = jj[u];
+        if (j < 0) continue;
+        const int w = j >> 5;
+        const int64_t slot = wprefix[w] + __popc(tile_bits[w] & ((1u << (j & 31)) - 1u));
+        if (in_smem) {
+          atomicOr(i < 32 ? &mlo[slot] : &mhi[slot], 1u << (i & 31));
+        } else {
+          atomicOr(reinterpret_cast<unsigned long long*>(&a.umask[base + slot]), 1ull << i);
+        }
       }
     }
   }
@@ -878,7 +888,8 @@ __global__ void __launch_bounds__(ROW_WARPS * 32, 4) k_topk_rows(TUArgs a) {
 // bitmask and writes the union and the member masks.
 constexpr int UNION_THREADS = 256;
 
-__global__ void __launch_bounds__(UNION_THREADS) k_tile_union(TUArgs a, int64_t mask_pairs) {
+__global__ void __launch_bounds__(UNION_THREADS) k_tile_union(TUArgs a, int64_t mask_pairs,
+                                                              int cache_lists) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int g = blockIdx.y;
   const int64_t tau = a.tau_begin + blockIdx.x;
@@ -886,7 +897,8 @@ __global__ void __launch_bounds__(UNION_THREADS) k_tile_union(TUArgs a, int64_t 
   constexpr int nw = UNION_THREADS / 32;
   uint32_t* tile_bits = reinterpret_cast<uint32_t*>(smem);
   uint32_t* wprefix = tile_bits + ((a.nwords + 3) & ~3);          // nwords + 1 entries
-  uint32_t* mspace = wprefix + ((a.nwords + 1 + 3) & ~3);
+  uint32_t* mspace = wprefix + ((a.nwords + 1 + 3) & ~3);         // mask_pairs lo/hi pairs
+  uint16_t* lists = cache_lists ? reinterpret_cast<uint16_t*>(mspace + 2 * mask_pairs) : nullptr;
   __shared__ int64_t s_red[32];
 
   for (int i = tid; i < a.nwords; i += UNION_THREADS) tile_bits[i] = 0;
@@ -899,12 +911,29 @@ __global__ void __launch_bounds__(UNION_THREADS) k_tile_union(TUArgs a, int64_t 
     if (nh > a.nblk) nh = a.nblk;
     const int need = (int)(nh < a.Ks ? nh : a.Ks);
     const int32_t* lst = a.sel + ((int64_t)g * a.nq + (t - a.q_begin)) * a.Ks;
+    uint16_t* my = lists ? lists + (int64_t)i * a.Ks : nullptr;
+    if (my) {  // one coalesced read of the list into shared memory
+      for (int xb = 0; xb < need; xb += 32 * 8) {
+        int32_t jj[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int x = xb + u * 32 + lane;
+          jj[u] = x < need ? lst[x] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int x = xb + u * 32 + lane;
+          if (x < need) my[x] = (uint16_t)jj[u];
+        }
+      }
+      __syncwarp();
+    }
     // each lane ORs a contiguous piece of the ascending list, one atomic per word run
     const int per = (need + 31) / 32;
-    const int x1 = min(need, (lane + 1) * per);
+    const int xa = lane * per, x1 = min(need, xa + per);
     uint32_t word = 0xffffffffu, bits = 0;
-    for (int x = lane * per; x < x1; ++x) {
-      const int32_t j = lst[x];
+    for (int x = xa; x < x1; ++x) {
+      const int32_t j = my ? (int32_t)my[x] : lst[x];
       if ((uint32_t)(j >> 5) != word) {
         if (bits) atomicOr(&tile_bits[word], bits);
         word = (uint32_t)(j >> 5);
@@ -914,7 +943,7 @@ __global__ void __launch_bounds__(UNION_THREADS) k_tile_union(TUArgs a, int64_t 
     }
     if (bits) atomicOr(&tile_bits[word], bits);
   }
-  finish_tile(a, g, tau, base, len, tile_bits, wprefix, mspace, mask_pairs);
+  finish_tile(a, g, tau, base, len, tile_bits, wprefix, mspace, mask_pairs, lists);
 }
 
 }  // namespace
@@ -974,8 +1003,13 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
   const size_t budget = 200 * 1024;
   if (fixed + 1024 > budget) return SGQA_ERR_UNSUPPORTED;
   const int64_t u_max = std::min<int64_t>((int64_t)dm.W * dm.Ks, dm.nblk);  // slots of a tile
-  const int64_t mask_pairs = std::min<int64_t>(u_max, (int64_t)((budget - fixed) / 8));
-  const size_t union_smem = fixed + (size_t)mask_pairs * 8;
+  // the tile's lists as 16-bit block indices when they fit, so they are read once
+  const size_t list_bytes = ((size_t)dm.W * dm.Ks * 2 + 15) & ~(size_t)15;
+  const int cache_lists = (dm.nblk <= 65536 && list_bytes + fixed + 8 * 1024 <= budget) ? 1 : 0;
+  const size_t mask_budget = budget - fixed - (cache_lists ? list_bytes : 0);
+  const int64_t mask_pairs =
+      std::min<int64_t>(std::min<int64_t>(u_max, 4096), (int64_t)(mask_budget / 8));
+  const size_t union_smem = fixed + (size_t)mask_pairs * 8 + (cache_lists ? list_bytes : 0);
   if (cudaFuncSetAttribute(k_topk_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)row_smem) != cudaSuccess ||
       cudaFuncSetAttribute(k_tile_union, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -985,9 +1019,9 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
   k_topk_rows<<<(unsigned)row_ctas, ROW_WARPS * 32, row_smem, st>>>(a);
   log_end(st);
   if (cudaGetLastError() != cudaSuccess) return SGQA_ERR_CUDA;
-  log_begin(SGQA_K_TOPK_UNION, st);
+  log_begin(SGQA_K_TILE_UNION, st);
   k_tile_union<<<dim3((unsigned)(tau_end - a.tau_begin), (unsigned)dm.Hkv), UNION_THREADS,
-                 union_smem, st>>>(a, mask_pairs);
+                 union_smem, st>>>(a, mask_pairs, cache_lists);
   log_end(st);
   return cudaGetLastError() == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA;
 }

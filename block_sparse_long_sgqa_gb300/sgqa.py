@@ -34,9 +34,10 @@ EXPORTED = ("sgqa_workspace_bytes", "sgqa_union_capacity", "sgqa_block_merge", "
             "sgqa_prefill_plan",
             "sgqa_set_launch_log", "sgqa_reset_status", "sgqa_read_status", "sgqa_status_string",
             "sgqa_version")
-K_MERGE, K_SPLIT, K_INDEX_QUERY, K_INDEX_SCORES, K_TOPK_UNION, K_ATTN, K_STAGE = 1, 2, 3, 4, 5, 6, 7
+K_MERGE, K_SPLIT, K_INDEX_QUERY, K_INDEX_SCORES, K_TOPK_UNION, K_ATTN, K_STAGE, K_TILE_UNION = (
+    1, 2, 3, 4, 5, 6, 7, 8)
 KERNEL_NAMES = {1: "merge", 2: "split", 3: "index_query", 4: "index_scores", 5: "topk_union",
-                6: "sparse_attn", 7: "stage_bf16"}
+                6: "sparse_attn", 7: "stage_bf16", 8: "tile_union"}
 
 
 class Params(ctypes.Structure):

@@ -231,9 +231,10 @@ enum sgqa_kernel_kind {
   SGQA_K_SPLIT = 2,        /* bf16 hi/lo split of cached block keys */
   SGQA_K_INDEX_QUERY = 3,  /* group index query (mean of heads, hi/lo split) */
   SGQA_K_INDEX_SCORES = 4, /* tensor-core indexer GEMM */
-  SGQA_K_TOPK_UNION = 5,   /* top-k selection and tile union */
+  SGQA_K_TOPK_UNION = 5,   /* top-k selection (per query row) */
   SGQA_K_ATTN = 6,         /* sparse attention */
-  SGQA_K_STAGE = 7         /* attention operand staging: bf16 rounding, K/V block packing */
+  SGQA_K_STAGE = 7,        /* attention operand staging: bf16 rounding, K/V block packing */
+  SGQA_K_TILE_UNION = 8    /* tile union and member masks */
 };
 
 /* Optional launch log for measurement.  While a log is installed, every
