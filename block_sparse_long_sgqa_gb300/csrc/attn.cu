@@ -15,22 +15,25 @@
 // sub-tile's first current block, followed by the sub-tile's current blocks.
 // Keys are gathered 128 per stage.
 //
-// Roles (7 warps):
+// Roles (12 warps):
 //  warp 0   builds each stage's block list from the union entries (a 4-deep
-//           ring), with each query's selected blocks as a bitmask, and issues
-//           the K loads: for B >= 8 one contiguous bulk copy per block from the
-//           block-packed, pre-swizzled K (see k_kv_pack), for B < 8 a cp.async
-//           row gather from the original layout;
-//  warp 1   issues the V loads;
+//           ring, so the lists run ahead of the loads), with each query's
+//           selected blocks as a bitmask;
+//  warp 11  issues the K loads: for B >= 8 one contiguous bulk copy per block
+//           from the block-packed, pre-swizzled K (see k_kv_pack), for B < 8 a
+//           cp.async row gather from the original layout;
+//  warp 1   issues the V loads the same way;
 //  warp 2   one thread issues S = Q K^T into a double-buffered TMEM tile
-//           (K slots are released as soon as their QK product is done) and
-//           O += P V into the TMEM accumulator (V as an MN-major operand);
+//           (K slots, three of them, are released as soon as their QK product
+//           is done) and O += P V into the TMEM accumulator, with P read from
+//           TMEM as the A operand and V from shared memory (MN-major);
 //  warps 3-10 two threads per query-head row, each owning 64 of the stage's
 //           128 keys (and 64 of O's columns): read S from TMEM, apply the
 //           per-query block masks (the causal cut only on current blocks),
 //           exchange partial maxima through shared memory, run the fp32 online
 //           softmax in base 2 (O is rescaled in TMEM only when the running
-//           maximum grows by more than 2^8), write P (bf16) to shared memory,
+//           maximum grows by more than 2^8), write P (bf16) into TMEM over the
+//           S values already read (the S buffer is released by the PV product),
 //           and finally normalise O and write O and the log-sum-exp.
 #include "common.cuh"
 #include "internal.h"
@@ -57,24 +60,22 @@ struct AttnCfg {
   static constexpr int KB = 128;  // keys per stage
   static constexpr int NBPS = KB / B;
   static constexpr bool TMA = B >= 8;  // blocks are whole 8-row swizzle atoms
-  static constexpr int SK = 2;            // K slots
+  static constexpr int SK = 3;            // K slots
   static constexpr int SV = 2;            // V slots
   static constexpr int NM = 4;            // stage block-list slots
   static constexpr int KC = D / 64;
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_TILE = KB * D * 2;
-  static constexpr int P_BYTES = BM * KB * 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + SK * KV_TILE;
-  static constexpr int OFF_P = OFF_V + SV * KV_TILE;
-  static constexpr int OFF_META = OFF_P + P_BYTES;
+  static constexpr int OFF_META = OFF_V + SV * KV_TILE;
   static constexpr int META_BYTES = (int)((sizeof(MetaT<NBPS>) + 15) / 16 * 16);
-  static constexpr int OFF_X = OFF_META + NM * META_BYTES;  // softmax half-row exchange
-  static constexpr int OFF_BAR = OFF_X + (2 * 2 + 2) * BM * 4;
+  static constexpr int OFF_X = OFF_META + NM * META_BYTES;  // epilogue max / sum exchange
+  static constexpr int OFF_BAR = OFF_X + 2 * 2 * BM * 4;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
-  static constexpr uint32_t TMEM_COLS = 512;  // S[2] at 0 / 128, O at 256
-  static constexpr int NTHREADS = 352;        // 3 pipeline warps + 8 softmax warps
+  static constexpr uint32_t TMEM_COLS = 512;  // S[2] at 0 / 128, O[2] at 256 / 384
+  static constexpr int NTHREADS = 384;        // 3 pipeline warps, 8 softmax warps, K loads
   static_assert(SMEM <= 232448, "shared memory plan");
 };
 
@@ -257,7 +258,7 @@ __device__ __forceinline__ const __nv_bfloat16* kv_row(const AttnArgs& a, const 
 }
 
 template <int D, int B>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     k_sparse_attn(const __grid_constant__ CUtensorMap mq, AttnArgs a) {
   using C = AttnCfg<D, B>;
   using Meta = MetaT<C::NBPS>;
@@ -279,15 +280,15 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* m_empty = bars + 15;   // [NM]
   uint64_t* s_full = bars + 19;    // [2]
   uint64_t* s_empty = bars + 21;   // [2]
-  uint64_t* p_full = bars + 23;
-  uint64_t* p_empty = bars + 24;
+  uint64_t* p_full = bars + 23;    // [2] P of a stage of softmax group g written
   uint64_t* mma_done = bars + 25;
-  uint64_t* x_bar = bars + 26;     // [2] half-row maxima exchanged
-  uint64_t* l_bar = bars + 28;     // half-row sums exchanged (epilogue)
+  uint64_t* p_empty = bars + 26;   // [2] PV product into O[g] done
+  uint64_t* l_bar = bars + 28;     // both groups' maxima and sums exchanged (epilogue)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 29);
   int* abort_flag = reinterpret_cast<int*>(bars + 30);
-  float* xmax = reinterpret_cast<float*>(smem + C::OFF_X);          // [2 parity][2 half][BM]
-  float* xsum = xmax + 2 * 2 * C::BM;                                 // [2 half][BM]
+  volatile int* n_stages = reinterpret_cast<volatile int*>(bars + 31);  // set once known
+  float* xmax = reinterpret_cast<float*>(smem + C::OFF_X);  // [2 group][BM]
+  float* xsum = xmax + 2 * C::BM;                            // [2 group][BM]
 
   // ---- work item
   const int64_t item = blockIdx.x;
@@ -316,16 +317,16 @@ __global__ void __launch_bounds__(352, 1)
     }
     for (int i = 0; i < C::NM; ++i) {
       mbar_init(&m_full[i], 1);
-      mbar_init(&m_empty[i], 9);  // 8 softmax warps + the V producer
+      mbar_init(&m_empty[i], 6);  // the stage's 4 softmax warps + the K and V producers
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 8);
-      mbar_init(&x_bar[i], 8);
+      mbar_init(&s_empty[i], 1);  // committed after the PV product that reads P
+      mbar_init(&p_full[i], 4);
+      mbar_init(&p_empty[i], 1);
     }
     mbar_init(l_bar, 8);
-    mbar_init(p_full, 8);
-    mbar_init(p_empty, 1);
+    *n_stages = 0x7fffffff;
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -358,16 +359,30 @@ __global__ void __launch_bounds__(352, 1)
     gs.pf_at = -1;
     const int sh = s * a.QS;
     const uint64_t qmask = nq_sub >= 64 ? ~0ull : ((1ull << nq_sub) - 1ull);
-    int issued_k[C::SK] = {};
     for (int i = 0;; ++i) {
-      const int ms = i % C::NM, ks = i % C::SK;
-      bool w = mbar_wait(&m_empty[ms], (uint32_t)(((i / C::NM) & 1) ^ 1), ab, a.status, 201);
+      const int ms = i % C::NM;
+      const bool w = mbar_wait(&m_empty[ms], (uint32_t)(((i / C::NM) & 1) ^ 1), ab, a.status, 201);
       if (!__all_sync(FULL, w)) break;
       Meta& m = meta_at(ms);
       gen_stage(a, gs, m, NBPS, sh, qmask, nq_sub);
+      if (lane == 0 && m.last) {
+        *n_stages = i + 1;  // lets the softmax group without a further stage stop
+        __threadfence_block();
+      }
       if (lane == 0) mbar_arrive(&m_full[ms]);
-      w = mbar_wait(&k_empty[ks], (uint32_t)(((i / C::SK) & 1) ^ 1), ab, a.status, 202);
+      if (m.last) break;
+    }
+    if (lane == 0 && ab.set()) mbar_wait_drain(q_full, 0, a.status, 291);
+  } else if (warp == 11) {
+    // ============================================================= K loads
+    int issued_k[C::SK] = {};
+    for (int i = 0;; ++i) {
+      const int ms = i % C::NM, ks = i % C::SK;
+      bool w = mbar_wait(&m_full[ms], (uint32_t)((i / C::NM) & 1), ab, a.status, 219) &&
+               mbar_wait(&k_empty[ks], (uint32_t)(((i / C::SK) & 1) ^ 1), ab, a.status, 202);
       if (!__all_sync(FULL, w)) break;
+      const Meta& m = meta_at(ms);
+      const bool last = m.last != 0;
       uint8_t* sK = smem + C::OFF_K + ks * C::KV_TILE;
       if constexpr (kTma) {
         // lane bs copies block slot bs (one contiguous packed block each)
@@ -394,14 +409,14 @@ __global__ void __launch_bounds__(352, 1)
         mbar_arrive(&k_full[ks]);
         cp_async_arrive(&k_full[ks]);
       }
-      if (m.last) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m_empty[ms]);
+      if (last) break;
     }
     if constexpr (kTma) {
-      if (lane == 0 && ab.set()) {  // let in-flight copies land before the CTA exits
-        mbar_wait_drain(q_full, 0, a.status, 291);
+      if (lane == 0 && ab.set())  // let in-flight copies land before the CTA exits
         for (int k = 0; k < C::SK; ++k)
           if (issued_k[k] > 0) mbar_wait_drain(&k_full[k], (issued_k[k] - 1) & 1, a.status, 292);
-      }
     } else {
       cp_async_wait_all();
     }
@@ -457,8 +472,6 @@ __global__ void __launch_bounds__(352, 1)
       constexpr uint32_t idesc_qk = idesc_bf16_f32(C::BM, C::KB, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(C::BM, D, 0, 1);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q);
-      const uint32_t sP = smem_u32(smem + C::OFF_P);
-      const uint32_t tO = tmem + 256;
       bool ok = mbar_wait(q_full, 0, ab, a.status, 205);
       // S_j = Q K_j^T into TMEM buffer j % 2; returns the stage's `last` flag
       auto issue_qk = [&](int j, bool& last) -> bool {
@@ -492,7 +505,7 @@ __global__ void __launch_bounds__(352, 1)
         bool last_next = false;
         if (!last_i && !issue_qk(i + 1, last_next)) break;
         const int vs = i % C::SV;
-        if (!mbar_wait(p_full, (uint32_t)(i & 1), ab, a.status, 209) ||
+        if (!mbar_wait(&p_full[i & 1], (uint32_t)((i >> 1) & 1), ab, a.status, 209) ||
             !mbar_wait(&v_full[vs], (uint32_t)((i / C::SV) & 1), ab, a.status, 210))
           break;
         if (!kTma) fence_proxy_async_smem();
@@ -500,27 +513,34 @@ __global__ void __launch_bounds__(352, 1)
         const uint32_t sV = smem_u32(smem + C::OFF_V + vs * C::KV_TILE);
 #pragma unroll
         for (int kk = 0; kk < C::KB / 16; ++kk) {
-          const uint32_t poff = (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
+          // P (bf16) fills columns 0..63 of S buffer i % 2: keys 16 kk .. 16 kk + 15
+          // are 8 columns
+          const uint32_t pt = tmem + (i & 1) * 128 + kk * 8;
           // V as an MN-major operand: LBO = stride between head-dim halves,
           // SBO = stride between 8-key groups
           const uint64_t vdesc =
               kTma ? sdesc_sw128(sV + kk * 2 * (C::KC * 1024), 1024, C::KC * 1024)
                    : sdesc_sw128(sV + kk * 16 * 128, C::KB * 128, 1024);
-          umma_f16(tO, sdesc_sw128(sP + poff, 16, 1024), vdesc, idesc_pv,
-                   (i > 0 || kk > 0) ? 1u : 0u);
+          // stage i accumulates into O[i % 2], the running sum of softmax group i % 2
+          umma_f16_ts(tmem + 256 + (i & 1) * 128, pt, vdesc, idesc_pv, (i > 1 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(p_empty);
+        umma_commit(&p_empty[i & 1]);
         umma_commit(&v_empty[vs]);
+        umma_commit(&s_empty[i & 1]);  // S/P buffer free for QK_{i+2}
         if (last_i) break;
         last_i = last_next;
       }
       umma_commit(mma_done);
       mbar_wait_drain(mma_done, 0, a.status, 299);
     }
-  } else {
+  } else if (warp >= 3 && warp <= 10) {
     // =============================================================== softmax
-    const int q = warp & 3;          // TMEM lane quadrant of this warp
-    const int half = (warp - 3) >> 2;  // keys [64 * half, 64 * half + 64) of each stage
+    // Group grp (4 warps, one thread per query-head row) takes stages grp,
+    // grp + 2, ...: all 128 keys of each, with its own running maximum and sum
+    // and its own accumulator O[grp], so the two groups work independently and
+    // are combined once at the end.
+    const int q = warp & 3;           // TMEM lane quadrant of this warp
+    const int grp = (warp - 3) >> 2;  // softmax group
     const int r = q * 32 + lane;
     const bool row_ok = r < rows;
     const int qi = r / a.G, h = r % a.G;
@@ -528,20 +548,45 @@ __global__ void __launch_bounds__(352, 1)
     const int64_t pos = a.off + t;
     const int64_t cur = pos / B;
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t tS = tl + grp * 128;         // this group's S buffer (P over its first 64 columns)
+    const uint32_t tOg = tl + 256 + grp * 128;  // this group's O
     const float ninf = -__int_as_float(0x7f800000);
     const float sl2 = a.scale_log2;
-    uint8_t* sP = smem + C::OFF_P;
-    float m_used = ninf, l = 0.0f;  // l: this half-row's share of the denominator
-    int i = 0;
+    float m_used = ninf, l = 0.0f;
     bool ok = true;
-    constexpr int BPH = 64 / B < 1 ? 1 : 64 / B;  // blocks per half stage
-    for (;; ++i) {
+    for (int i = grp;; i += 2) {
       const int ms = i % C::NM;
-      // waits are polled per thread but their outcome is made warp-uniform:
-      // the tcgen05.ld/st below are warp-collective
-      bool w = mbar_wait(&s_full[i & 1], (uint32_t)((i >> 1) & 1), ab, a.status, 211) &&
-               mbar_wait(&m_full[ms], (uint32_t)((i / C::NM) & 1), ab, a.status, 212);
+      // the block list of stage i, or the news that the item has no stage i
+      bool have = true, w = true;
+      {
+        const uint64_t t0 = globaltimer();
+        for (uint32_t it = 0;; ++it) {
+          if (mbar_try_wait_ns(&m_full[ms], (uint32_t)((i / C::NM) & 1), 500)) break;
+          if (*n_stages <= i) {
+            have = false;
+            break;
+          }
+          if ((it & 15) == 15) {
+            if (ab.set()) {
+              w = false;
+              break;
+            }
+            if (globaltimer() - t0 > kWaitLimitNs) {
+              ab.raise(a.status, 212);
+              w = false;
+              break;
+            }
+          }
+        }
+      }
+      // outcomes made warp-uniform: the tcgen05.ld/st below are warp-collective
       if (!__all_sync(FULL, w)) {
+        ok = false;
+        break;
+      }
+      if (!__any_sync(FULL, have)) break;
+      const bool ws = mbar_wait(&s_full[grp], (uint32_t)((i >> 1) & 1), ab, a.status, 211);
+      if (!__all_sync(FULL, ws)) {
         ok = false;
         break;
       }
@@ -549,29 +594,31 @@ __global__ void __launch_bounds__(352, 1)
       const Meta& m = meta_at(ms);
       const int nb = m.nb;
       const bool last = m.last != 0;
-      // Allowed keys of this row among this half's 64 keys, as a 64-bit mask:
-      // a whole block when the query selected it (bit qi of the block's mask)
-      // and it is historical, the causal prefix of the query's own block.
-      uint32_t allow0 = 0u, allow1 = 0u;
+      // Allowed keys of this row among the stage's 128 keys (4 words): a whole
+      // block when the query selected it and it is historical, the causal
+      // prefix of the query's own block.
+      uint32_t al0 = 0u, al1 = 0u, al2 = 0u, al3 = 0u;
       if (row_ok) {
-        const int bs0 = half * BPH;
-        const int bs1 = min(nb, bs0 + BPH);
-        int bsd = bs0;  // first slot handled block by block
+        int bsd = 0;  // first slot handled block by block
         if constexpr (kTma) {
           // historical blocks: the query's bitmask, one bit per block -> B keys
-          const uint32_t hb = (m.qbits[qi] >> bs0) & ((1u << BPH) - 1u);
+          const uint32_t hb = m.qbits[qi];
           if constexpr (B == 8) {
-            allow0 = ((((hb & 0xFu) * 0x00204081u) & 0x01010101u) * 0xFFu);
-            allow1 = (((((hb >> 4) & 0xFu) * 0x00204081u) & 0x01010101u) * 0xFFu);
-          } else {  // B == 16: four blocks of 16 keys
-            allow0 = ((hb & 1u) ? 0x0000FFFFu : 0u) | ((hb & 2u) ? 0xFFFF0000u : 0u);
-            allow1 = ((hb & 4u) ? 0x0000FFFFu : 0u) | ((hb & 8u) ? 0xFFFF0000u : 0u);
+            al0 = ((((hb >> 0) & 0xFu) * 0x00204081u) & 0x01010101u) * 0xFFu;
+            al1 = ((((hb >> 4) & 0xFu) * 0x00204081u) & 0x01010101u) * 0xFFu;
+            al2 = ((((hb >> 8) & 0xFu) * 0x00204081u) & 0x01010101u) * 0xFFu;
+            al3 = ((((hb >> 12) & 0xFu) * 0x00204081u) & 0x01010101u) * 0xFFu;
+          } else {  // B == 16: two blocks of 16 keys per word
+            al0 = ((hb & 1u) ? 0x0000FFFFu : 0u) | ((hb & 2u) ? 0xFFFF0000u : 0u);
+            al1 = ((hb & 4u) ? 0x0000FFFFu : 0u) | ((hb & 8u) ? 0xFFFF0000u : 0u);
+            al2 = ((hb & 16u) ? 0x0000FFFFu : 0u) | ((hb & 32u) ? 0xFFFF0000u : 0u);
+            al3 = ((hb & 64u) ? 0x0000FFFFu : 0u) | ((hb & 128u) ? 0xFFFF0000u : 0u);
           }
-          bsd = max(bs0, (int)m.diag);
+          bsd = m.diag;
         }
         // current blocks of the sub-tile (and, without the bitmask, every block)
 #pragma unroll 1
-        for (int bs = bsd; bs < bs1; ++bs) {
+        for (int bs = bsd; bs < nb; ++bs) {
           const int64_t b = m.blk[bs];
           int lim = 0;
           if (((m.mask[bs] >> qi) & 1ull) && b < cur)
@@ -579,23 +626,25 @@ __global__ void __launch_bounds__(352, 1)
           else if (b == cur)
             lim = (int)(pos - b * B + 1);
           if (lim > 0) {
-            const int k0 = bs * B - half * 64;  // key offset within this half
+            const int k0 = bs * B;  // a block never straddles a 32-key word
             const uint32_t bits = lim >= 32 ? 0xffffffffu : ((1u << lim) - 1u);
             const uint32_t wv = bits << (uint32_t)(k0 & 31);
-            allow0 |= (k0 >> 5) == 0 ? wv : 0u;
-            allow1 |= (k0 >> 5) == 1 ? wv : 0u;
+            const int wd = k0 >> 5;
+            al0 |= wd == 0 ? wv : 0u;
+            al1 |= wd == 1 ? wv : 0u;
+            al2 |= wd == 2 ? wv : 0u;
+            al3 |= wd == 3 ? wv : 0u;
           }
         }
       }
-      const uint32_t sbase = tl + (i & 1) * 128 + half * 64;
-      // pass 1: masked maximum over this half (32 keys per TMEM load)
+      // pass 1: masked maximum over the 128 keys (32 per TMEM load)
       float mx0 = ninf, mx1 = ninf, mx2 = ninf, mx3 = ninf;
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < 4; ++cc) {
         uint32_t v[32];
-        tmem_ld32(sbase + cc * 32, v);
+        tmem_ld32(tS + cc * 32, v);
         tmem_wait_ld();
-        const uint32_t am = cc == 0 ? allow0 : allow1;
+        const uint32_t am = cc == 0 ? al0 : cc == 1 ? al1 : cc == 2 ? al2 : al3;
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           mx0 = fmaxf(mx0, ((am >> e) & 1u) ? __uint_as_float(v[e]) : ninf);
@@ -604,27 +653,16 @@ __global__ void __launch_bounds__(352, 1)
           mx3 = fmaxf(mx3, ((am >> (e + 3)) & 1u) ? __uint_as_float(v[e + 3]) : ninf);
         }
       }
-      // combine with the other half of the row
-      const float pmx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      float* xm = xmax + (i & 1) * 2 * C::BM;
-      xm[half * C::BM + r] = pmx;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&x_bar[i & 1]);
-      bool wx = mbar_wait(&x_bar[i & 1], (uint32_t)((i >> 1) & 1), ab, a.status, 216);
-      if (!__all_sync(FULL, wx)) {
-        ok = false;
-        break;
-      }
-      const float smax = fmaxf(pmx, xm[(1 - half) * C::BM + r]) * sl2;
+      const float smax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
       // Raise the reference maximum when this stage exceeds it by more than 2^8.
-      // O holds contributions under the old maximum, so it is rescaled once
-      // PV_{i-1} is done; both threads of a row decide alike, each warp takes
-      // that path together (rows that do not need it scale by 1), and each half
-      // rescales its own 64 columns of O.
+      // O[grp] holds the group's earlier stages under the old maximum: it is
+      // rescaled once the group's previous PV product (stage i - 2) is done;
+      // each warp takes that path together (rows that do not need it scale by 1).
       const bool raise = smax > m_used + 8.0f;
       const bool rescale = raise && m_used != ninf;
       if (__any_sync(FULL, rescale)) {
-        bool w2 = mbar_wait(p_empty, (uint32_t)((i - 1) & 1), ab, a.status, 213);
+        const bool w2 =
+            mbar_wait(&p_empty[grp], (uint32_t)(((i >> 1) - 1) & 1), ab, a.status, 213);
         if (!__all_sync(FULL, w2)) {
           ok = false;
           break;
@@ -632,111 +670,115 @@ __global__ void __launch_bounds__(352, 1)
         tc_fence_after();
         const float f = rescale ? ex2(m_used - smax) : 1.0f;
 #pragma unroll 1
-        for (int cc = 0; cc < D / 64; ++cc) {
+        for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t ov[32];
-          const uint32_t oc = tl + 256 + half * (D / 2) + cc * 32;
-          tmem_ld32(oc, ov);
+          tmem_ld32(tOg + cc * 32, ov);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
-          tmem_st32(oc, ov);
+          tmem_st32(tOg + cc * 32, ov);
         }
         tmem_wait_st();
         l *= f;
       }
       if (raise) m_used = smax;
-      // P buffer is free once PV_{i-1} is done
-      if (i > 0) {
-        bool w3 = mbar_wait(p_empty, (uint32_t)((i - 1) & 1), ab, a.status, 214);
-        if (!__all_sync(FULL, w3)) {
-          ok = false;
-          break;
-        }
-      }
-      // pass 2: probabilities p = 2^(s * scale * log2(e) - m), bf16, into P.
-      // A row with nothing allowed so far has m_used = -inf and writes zeros.
+      // pass 2: probabilities p = 2^(s * scale * log2(e) - m) as bf16; keys
+      // 64 hh .. 64 hh + 63 go to P columns 32 hh .. 32 hh + 31, whose S values
+      // have been read by then.  A row with nothing allowed so far has
+      // m_used = -inf and writes zeros.
       const float msub = m_used == ninf ? 0.0f : m_used;
       float rs0 = 0.0f, rs1 = 0.0f;
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t v[32];
-        tmem_ld32(sbase + cc * 32, v);
-        tmem_wait_ld();
-        const uint32_t am = cc == 0 ? allow0 : allow1;
-        uint32_t pk[16];
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float p0 = ((am >> e) & 1u) ? ex2(fmaf(__uint_as_float(v[e]), sl2, -msub)) : 0.0f;
-          const float p1 =
-              ((am >> (e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -msub)) : 0.0f;
-          rs0 += p0;
-          rs1 += p1;
-          pk[e >> 1] = pack_bf16x2(p0, p1);
-        }
-        // keys 64*half + 32*cc .. +31 are 16-byte units 4*cc .. 4*cc+3 of chunk `half`
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t v[32];
+          tmem_ld32(tS + (2 * hh + c2) * 32, v);
+          tmem_wait_ld();
+          const uint32_t am = hh == 0 ? (c2 == 0 ? al0 : al1) : (c2 == 0 ? al2 : al3);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint4 vv = make_uint4(pk[u * 4 + 0], pk[u * 4 + 1], pk[u * 4 + 2], pk[u * 4 + 3]);
-          *reinterpret_cast<uint4*>(sP + half * (C::BM * 128) + sw128(r, cc * 4 + u)) = vv;
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 =
+                ((am >> e) & 1u) ? ex2(fmaf(__uint_as_float(v[e]), sl2, -msub)) : 0.0f;
+            const float p1 =
+                ((am >> (e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -msub)) : 0.0f;
+            rs0 += p0;
+            rs1 += p1;
+            pk[c2 * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
+          }
         }
+        tmem_st32(tS + hh * 32, pk);
       }
       l += rs0 + rs1;
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&s_empty[i & 1]);  // S buffer read twice, now free
-        mbar_arrive(&m_empty[ms]);     // done with this stage's block list
-        mbar_arrive(p_full);
+        mbar_arrive(&m_empty[ms]);  // done with this stage's block list
+        mbar_arrive(&p_full[grp]);
       }
       if (last) break;
     }
-    // ---- epilogue: O / l and the log-sum-exp
-    bool fin = ok && mbar_wait(p_empty, (uint32_t)(i & 1), ab, a.status, 215);
+    // ---- epilogue: combine the groups, O / l and the log-sum-exp
+    const int ns = *n_stages;
+    const int n0 = (ns + 1) / 2, n1 = ns / 2;  // stages of group 0 and of group 1
+    bool fin = ok && ns != 0x7fffffff;
+    if (fin && n0 > 0) fin = mbar_wait(&p_empty[0], (uint32_t)((n0 - 1) & 1), ab, a.status, 215);
+    if (fin && n1 > 0) fin = mbar_wait(&p_empty[1], (uint32_t)((n1 - 1) & 1), ab, a.status, 218);
     if (__all_sync(FULL, fin)) {
-      xsum[half * C::BM + r] = l;
+      xmax[grp * C::BM + r] = m_used;
+      xsum[grp * C::BM + r] = l;
       __syncwarp();
       if (lane == 0) mbar_arrive(l_bar);
       fin = mbar_wait(l_bar, 0, ab, a.status, 217);
     }
     if (__all_sync(FULL, fin)) {
-      const float lt = xsum[r] + xsum[C::BM + r];
+      const float m0 = xmax[r], m1 = xmax[C::BM + r];
+      const float mm = fmaxf(m0, m1);
+      const float f0 = m0 == ninf ? 0.0f : ex2(m0 - mm);
+      const float f1 = m1 == ninf ? 0.0f : ex2(m1 - mm);
+      const float lt = xsum[r] * f0 + xsum[C::BM + r] * f1;
       tc_fence_after();
       const float inv = row_ok && lt > 0.0f ? 1.0f / lt : 0.0f;
+      const float g0 = f0 * inv, g1 = f1 * inv;
       const int64_t hq = (int64_t)g * a.G + h;
+      // this thread writes head-dim columns [grp * D / 2, grp * D / 2 + D / 2)
 #pragma unroll 1
       for (int cc = 0; cc < D / 64; ++cc) {
-        uint32_t ov[32];
-        const int col = half * (D / 2) + cc * 32;
-        tmem_ld32(tl + 256 + col, ov);
+        const int col = grp * (D / 2) + cc * 32;
+        uint32_t o0[32], o1[32];
+        tmem_ld32(tl + 256 + col, o0);
+        if (n1 > 0) tmem_ld32(tl + 384 + col, o1);
         tmem_wait_ld();
+        float ov[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          ov[e] = __uint_as_float(o0[e]) * g0 + (n1 > 0 ? __uint_as_float(o1[e]) * g1 : 0.0f);
         if (row_ok) {
           if (a.out_f32) {
             float* dst = static_cast<float*>(a.O) + (t * a.H + hq) * D + col;
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(dst + e) =
-                  make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
-                              __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
+              *reinterpret_cast<float4*>(dst + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
           } else {
             __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.O) + (t * a.H + hq) * D + col;
 #pragma unroll
             for (int e = 0; e < 32; e += 8) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(ov[e + 4]) * inv, __uint_as_float(ov[e + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(ov[e + 6]) * inv, __uint_as_float(ov[e + 7]) * inv);
-              *reinterpret_cast<uint4*>(dst + e) = v;
+              uint4 vv;
+              vv.x = pack_bf16x2(ov[e], ov[e + 1]);
+              vv.y = pack_bf16x2(ov[e + 2], ov[e + 3]);
+              vv.z = pack_bf16x2(ov[e + 4], ov[e + 5]);
+              vv.w = pack_bf16x2(ov[e + 6], ov[e + 7]);
+              *reinterpret_cast<uint4*>(dst + e) = vv;
             }
           }
         }
       }
-      if (row_ok && half == 0) a.lse[hq * a.T + t] = (m_used + __log2f(lt)) * 0.69314718055994531f;
+      if (row_ok && grp == 0) a.lse[hq * a.T + t] = (mm + __log2f(lt)) * 0.69314718055994531f;
     }
     tc_fence_before();
   }
-
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();
