@@ -637,78 +637,124 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
-      // pass 1: masked maximum over the 128 keys (32 per TMEM load)
-      float mx0 = ninf, mx1 = ninf, mx2 = ninf, mx3 = ninf;
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tmem_ld32(tS + cc * 32, v);
-        tmem_wait_ld();
-        const uint32_t am = cc == 0 ? al0 : cc == 1 ? al1 : cc == 2 ? al2 : al3;
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          mx0 = fmaxf(mx0, ((am >> e) & 1u) ? __uint_as_float(v[e]) : ninf);
-          mx1 = fmaxf(mx1, ((am >> (e + 1)) & 1u) ? __uint_as_float(v[e + 1]) : ninf);
-          mx2 = fmaxf(mx2, ((am >> (e + 2)) & 1u) ? __uint_as_float(v[e + 2]) : ninf);
-          mx3 = fmaxf(mx3, ((am >> (e + 3)) & 1u) ? __uint_as_float(v[e + 3]) : ninf);
-        }
-      }
-      const float smax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-      // Raise the reference maximum when this stage exceeds it by more than 2^8.
-      // O[grp] holds the group's earlier stages under the old maximum: it is
-      // rescaled once the group's previous PV product (stage i - 2) is done;
-      // each warp takes that path together (rows that do not need it scale by 1).
-      const bool raise = smax > m_used + 8.0f;
-      const bool rescale = raise && m_used != ninf;
-      if (__any_sync(FULL, rescale)) {
-        const bool w2 =
-            mbar_wait(&p_empty[grp], (uint32_t)(((i >> 1) - 1) & 1), ab, a.status, 213);
-        if (!__all_sync(FULL, w2)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float f = rescale ? ex2(m_used - smax) : 1.0f;
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t ov[32];
-          tmem_ld32(tOg + cc * 32, ov);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
-          tmem_st32(tOg + cc * 32, ov);
-        }
-        tmem_wait_st();
-        l *= f;
-      }
-      if (raise) m_used = smax;
-      // pass 2: probabilities p = 2^(s * scale * log2(e) - m) as bf16; keys
-      // 64 hh .. 64 hh + 63 go to P columns 32 hh .. 32 hh + 31, whose S values
-      // have been read by then.  A row with nothing allowed so far has
-      // m_used = -inf and writes zeros.
-      const float msub = m_used == ninf ? 0.0f : m_used;
+      // One pass when possible: p = 2^(s * scale * log2(e) - m_used) with the
+      // running reference maximum, as long as no allowed key of the stage
+      // exceeds it by more than 2^8 (checked per 64 keys before their
+      // exponentials); otherwise the stage is redone in two passes below.
       float rs0 = 0.0f, rs1 = 0.0f;
+      bool fast = __all_sync(FULL, m_used != ninf || (al0 | al1 | al2 | al3) == 0u);
+      if (fast) {
 #pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t v[32];
-          tmem_ld32(tS + (2 * hh + c2) * 32, v);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tS + (2 * hh) * 32, v0);
+          tmem_ld32(tS + (2 * hh + 1) * 32, v1);
           tmem_wait_ld();
-          const uint32_t am = hh == 0 ? (c2 == 0 ? al0 : al1) : (c2 == 0 ? al2 : al3);
+          const uint32_t a0 = hh == 0 ? al0 : al2, a1 = hh == 0 ? al1 : al3;
+          float cm0 = ninf, cm1 = ninf;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            cm0 = fmaxf(cm0, ((a0 >> e) & 1u) ? __uint_as_float(v0[e]) : ninf);
+            cm1 = fmaxf(cm1, ((a1 >> e) & 1u) ? __uint_as_float(v1[e]) : ninf);
+          }
+          if (__any_sync(FULL, fmaxf(cm0, cm1) * sl2 > m_used + 8.0f)) {
+            fast = false;
+            break;
+          }
+          uint32_t pk[32];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float p0 =
-                ((am >> e) & 1u) ? ex2(fmaf(__uint_as_float(v[e]), sl2, -msub)) : 0.0f;
+            const float p0 = ((a0 >> e) & 1u) ? ex2(fmaf(__uint_as_float(v0[e]), sl2, -m_used)) : 0.0f;
             const float p1 =
-                ((am >> (e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -msub)) : 0.0f;
-            rs0 += p0;
-            rs1 += p1;
-            pk[c2 * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
+                ((a0 >> (e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v0[e + 1]), sl2, -m_used)) : 0.0f;
+            const float p2 = ((a1 >> e) & 1u) ? ex2(fmaf(__uint_as_float(v1[e]), sl2, -m_used)) : 0.0f;
+            const float p3 =
+                ((a1 >> (e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v1[e + 1]), sl2, -m_used)) : 0.0f;
+            rs0 += p0 + p2;
+            rs1 += p1 + p3;
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+            pk[16 + (e >> 1)] = pack_bf16x2(p2, p3);
+          }
+          tmem_st32(tS + hh * 32, pk);  // S columns 0..63 have been read by now
+        }
+      }
+      if (!fast) {
+        tmem_wait_st();
+        rs0 = 0.0f;
+        rs1 = 0.0f;
+        // pass 1: masked maximum over the 128 keys
+        float mx0 = ninf, mx1 = ninf, mx2 = ninf, mx3 = ninf;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(tS + cc * 32, v);
+          tmem_wait_ld();
+          const uint32_t am = cc == 0 ? al0 : cc == 1 ? al1 : cc == 2 ? al2 : al3;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            mx0 = fmaxf(mx0, ((am >> e) & 1u) ? __uint_as_float(v[e]) : ninf);
+            mx1 = fmaxf(mx1, ((am >> (e + 1)) & 1u) ? __uint_as_float(v[e + 1]) : ninf);
+            mx2 = fmaxf(mx2, ((am >> (e + 2)) & 1u) ? __uint_as_float(v[e + 2]) : ninf);
+            mx3 = fmaxf(mx3, ((am >> (e + 3)) & 1u) ? __uint_as_float(v[e + 3]) : ninf);
           }
         }
-        tmem_st32(tS + hh * 32, pk);
+        const float smax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        // Raise the reference maximum when this stage exceeds it by more than
+        // 2^8.  O[grp] holds the group's earlier stages under the old maximum:
+        // it is rescaled once the group's previous PV product (stage i - 2) is
+        // done; each warp takes that path together (rows that do not need it
+        // scale by 1).
+        const bool raise = smax > m_used + 8.0f;
+        const bool rescale = raise && m_used != ninf;
+        if (__any_sync(FULL, rescale)) {
+          const bool w2 =
+              mbar_wait(&p_empty[grp], (uint32_t)(((i >> 1) - 1) & 1), ab, a.status, 213);
+          if (!__all_sync(FULL, w2)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float f = rescale ? ex2(m_used - smax) : 1.0f;
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t ov[32];
+            tmem_ld32(tOg + cc * 32, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+            tmem_st32(tOg + cc * 32, ov);
+          }
+          tmem_wait_st();
+          l *= f;
+        }
+        if (raise) m_used = smax;
+        // pass 2: keys 64 hh .. 64 hh + 63 go to P columns 32 hh .. 32 hh + 31,
+        // whose S values have been read by then.  A row with nothing allowed so
+        // far has m_used = -inf and writes zeros.
+        const float msub = m_used == ninf ? 0.0f : m_used;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tS + (2 * hh) * 32, v0);
+          tmem_ld32(tS + (2 * hh + 1) * 32, v1);
+          tmem_wait_ld();
+          const uint32_t a0 = hh == 0 ? al0 : al2, a1 = hh == 0 ? al1 : al3;
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = ((a0 >> e) & 1u) ? ex2(fmaf(__uint_as_float(v0[e]), sl2, -msub)) : 0.0f;
+            const float p1 =
+                ((a0 >> (e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v0[e + 1]), sl2, -msub)) : 0.0f;
+            const float p2 = ((a1 >> e) & 1u) ? ex2(fmaf(__uint_as_float(v1[e]), sl2, -msub)) : 0.0f;
+            const float p3 =
+                ((a1 >> (e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v1[e + 1]), sl2, -msub)) : 0.0f;
+            rs0 += p0 + p2;
+            rs1 += p1 + p3;
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+            pk[16 + (e >> 1)] = pack_bf16x2(p2, p3);
+          }
+          tmem_st32(tS + hh * 32, pk);
+        }
       }
       l += rs0 + rs1;
       tmem_wait_st();
