@@ -643,7 +643,47 @@ __global__ void __launch_bounds__(384, 1)
       // exponentials); otherwise the stage is redone in two passes below.
       float rs0 = 0.0f, rs1 = 0.0f;
       bool fast = __all_sync(FULL, m_used != ninf || (al0 | al1 | al2 | al3) == 0u);
-      if (fast) {
+      // Stages whose blocks are all historical (B >= 8) take the mask per
+      // block: block maxima, and -m or -inf as the exponent's additive term.
+      bool by_block = false;
+      if constexpr (kTma) by_block = m.diag >= nb;
+      if (fast && by_block) {
+        constexpr int BPHh = 64 / B;  // blocks per 64 keys
+        const uint32_t hb = row_ok ? m.qbits[qi] : 0u;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v[64];
+          tmem_ld32(tS + (2 * hh) * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(tS + (2 * hh + 1) * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_wait_ld();
+          const uint32_t hbh = hb >> (hh * BPHh);
+          float cm = ninf;
+          float cb[BPHh];
+#pragma unroll
+          for (int jj = 0; jj < BPHh; ++jj) {
+            float bm = __uint_as_float(v[jj * B]);
+#pragma unroll
+            for (int k = 1; k < B; ++k) bm = fmaxf(bm, __uint_as_float(v[jj * B + k]));
+            const bool al = (hbh >> jj) & 1u;
+            cm = fmaxf(cm, al ? bm : ninf);
+            cb[jj] = al ? -m_used : ninf;
+          }
+          if (__any_sync(FULL, cm * sl2 > m_used + 8.0f)) {
+            fast = false;
+            break;
+          }
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            const float p0 = ex2(fmaf(__uint_as_float(v[e]), sl2, cb[e / B]));
+            const float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl2, cb[(e + 1) / B]));
+            rs0 += p0;
+            rs1 += p1;
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(tS + hh * 32, pk);  // S columns 0..63 have been read by now
+        }
+      } else if (fast) {
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t v0[32], v1[32];
