@@ -473,14 +473,9 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t idesc_pv = idesc_bf16_f32(C::BM, D, 0, 1);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q);
       bool ok = mbar_wait(q_full, 0, ab, a.status, 205);
-      // S_j = Q K_j^T into TMEM buffer j % 2; returns the stage's `last` flag
-      auto issue_qk = [&](int j, bool& last) -> bool {
+      // S_j = Q K_j^T into TMEM buffer j % 2 (operands ready)
+      auto do_qk = [&](int j) {
         const int ks = j % C::SK;
-        if (!mbar_wait(&m_full[j % C::NM], (uint32_t)((j / C::NM) & 1), ab, a.status, 206) ||
-            !mbar_wait(&k_full[ks], (uint32_t)((j / C::SK) & 1), ab, a.status, 207) ||
-            !mbar_wait(&s_empty[j & 1], (uint32_t)(((j >> 1) & 1) ^ 1), ab, a.status, 208))
-          return false;
-        last = meta_at(j % C::NM).last != 0;
         if (!kTma) fence_proxy_async_smem();  // cp.async writes -> tensor-core reads
         tc_fence_after();
         const uint32_t sK = smem_u32(smem + C::OFF_K + ks * C::KV_TILE);
@@ -497,17 +492,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         umma_commit(&s_full[j & 1]);
         umma_commit(&k_empty[ks]);  // the K slot is free once this product is done
-        return true;
       };
-      bool last_i = false;
-      if (ok) ok = issue_qk(0, last_i);
-      for (int i = 0; ok; ++i) {
-        bool last_next = false;
-        if (!last_i && !issue_qk(i + 1, last_next)) break;
+      // O[i % 2] += P_i V_i, P read from TMEM (operands ready)
+      auto do_pv = [&](int i) {
         const int vs = i % C::SV;
-        if (!mbar_wait(&p_full[i & 1], (uint32_t)((i >> 1) & 1), ab, a.status, 209) ||
-            !mbar_wait(&v_full[vs], (uint32_t)((i / C::SV) & 1), ab, a.status, 210))
-          break;
         if (!kTma) fence_proxy_async_smem();
         tc_fence_after();
         const uint32_t sV = smem_u32(smem + C::OFF_V + vs * C::KV_TILE);
@@ -527,8 +515,45 @@ __global__ void __launch_bounds__(384, 1)
         umma_commit(&p_empty[i & 1]);
         umma_commit(&v_empty[vs]);
         umma_commit(&s_empty[i & 1]);  // S/P buffer free for QK_{i+2}
-        if (last_i) break;
-        last_i = last_next;
+      };
+      // Issue each product as soon as its operands are ready (the two softmax
+      // groups' chains are independent), PV first since it frees an S buffer.
+      // QK_j is tested only once PV_{j-2} has been issued, so every phase
+      // tested is at most one ahead of the last one completed.
+      int qn = 0, pn = 0;  // next QK and PV to issue
+      int n_st = -1;       // stages of the item, once the last list has been seen
+      uint64_t t_prog = globaltimer();
+      uint32_t idle = 0;
+      while (ok && (n_st < 0 || pn < n_st)) {
+        bool progress = false;
+        if (pn < qn && mbar_test(&p_full[pn & 1], (uint32_t)((pn >> 1) & 1)) &&
+            mbar_test(&v_full[pn % C::SV], (uint32_t)((pn / C::SV) & 1))) {
+          do_pv(pn);
+          ++pn;
+          progress = true;
+        }
+        if ((n_st < 0 || qn < n_st) && qn <= pn + 1 &&
+            mbar_test(&m_full[qn % C::NM], (uint32_t)((qn / C::NM) & 1)) &&
+            mbar_test(&k_full[qn % C::SK], (uint32_t)((qn / C::SK) & 1)) &&
+            mbar_test(&s_empty[qn & 1], (uint32_t)(((qn >> 1) & 1) ^ 1))) {
+          if (meta_at(qn % C::NM).last) n_st = qn + 1;
+          do_qk(qn);
+          ++qn;
+          progress = true;
+        }
+        if (progress) {
+          t_prog = globaltimer();
+          idle = 0;
+        } else {
+          __nanosleep(32);
+          if ((++idle & 63) == 0) {
+            if (ab.set()) break;
+            if (globaltimer() - t_prog > kWaitLimitNs) {
+              ab.raise(a.status, 206);
+              break;
+            }
+          }
+        }
       }
       umma_commit(mma_done);
       mbar_wait_drain(mma_done, 0, a.status, 299);

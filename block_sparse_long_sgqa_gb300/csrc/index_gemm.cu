@@ -15,9 +15,10 @@
 // (persistent CTAs), so every SM gets the same number of tiles however the
 // causal row lengths vary; consecutive items share the query operand, which
 // is reloaded only when the (row tile, group) pair changes.  Warp 0 issues
-// the TMA loads (B double-buffered), warp 1 the MMAs into a double-buffered
-// TMEM accumulator (2 x 128 fp32 columns), and warps 2-5 drain TMEM (one query
-// row per thread), apply the causal block mask and write the tile.  Stores go
+// the TMA loads (B double-buffered), warp 1 the MMAs into two TMEM
+// accumulators (128 fp32 columns each), and warps 2-9 drain TMEM (one query
+// row per thread, two warps per TMEM lane quadrant taking 64 columns each),
+// apply the causal block mask and write the tile.  Stores go
 // through a 128-byte-swizzled shared staging buffer and TMA, so each tile
 // leaves as full 128-byte rows instead of 16-byte pieces of 32 rows.
 #include <algorithm>
@@ -29,9 +30,11 @@
 namespace sgqa {
 namespace {
 
+constexpr int IDX_BN = 128;  // blocks per output tile
+
 template <int D>
 struct IdxCfg {
-  static constexpr int BM = 128, BN = 128, STAGES = 2;
+  static constexpr int BM = 128, BN = IDX_BN, STAGES = 2, NACC = 2;
   static constexpr int KC = D / 64;          // 128-byte (64-element) chunks along d
   static constexpr int A_TILE = BM * 128;    // bytes of one chunk of A
   static constexpr int B_TILE = BN * 128;
@@ -42,11 +45,11 @@ struct IdxCfg {
   static constexpr int OFF_B = 2 * A_BYTES;
   static constexpr int STAGE_BYTES = 2 * B_BYTES;  // hi + lo
   static constexpr int STG_BYTES = 32 * 128;       // one 32 x 32 fp32 store box
-  static constexpr int OFF_STG = OFF_B + STAGES * STAGE_BYTES;  // [4 warps][2]
+  static constexpr int OFF_STG = OFF_B + STAGES * STAGE_BYTES;  // one per epilogue warp
   static constexpr int OFF_BAR = OFF_STG + 8 * STG_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + slack for 1024-byte alignment
-  static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr int NTHREADS = 192;
+  static constexpr uint32_t TMEM_COLS = NACC * BN;
+  static constexpr int NTHREADS = 320;  // producer, MMA, 8 epilogue warps
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -67,7 +70,7 @@ __device__ __forceinline__ int64_t ntiles_of(const IdxArgs& a, int64_t rt) {
   const int64_t t_last = (t0 + 128 < a.q_end ? t0 + 128 : a.q_end) - 1;
   int64_t nh = (a.q_offset + t_last) / a.B;
   if (nh > a.nblk) nh = a.nblk;
-  const int64_t nt = (nh + 127) / 128;
+  const int64_t nt = (nh + IDX_BN - 1) / IDX_BN;
   return nt > 0 ? nt : 1;
 }
 
@@ -101,7 +104,7 @@ __device__ __forceinline__ void item_next(const IdxArgs& a, Item& w) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     k_index_scores(const __grid_constant__ CUtensorMap mq_hi, const __grid_constant__ CUtensorMap mq_lo,
                    const __grid_constant__ CUtensorMap mk_hi, const __grid_constant__ CUtensorMap mk_lo,
                    const __grid_constant__ CUtensorMap ms, IdxArgs a) {
@@ -111,14 +114,14 @@ __global__ void __launch_bounds__(192, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* a_full = bars + 0;
-  uint64_t* b_full = bars + 1;     // [2]
-  uint64_t* b_empty = bars + 3;    // [2]
-  uint64_t* acc_full = bars + 5;   // [2]
-  uint64_t* acc_empty = bars + 7;  // [2]
-  uint64_t* mma_done = bars + 9;
-  uint64_t* a_empty = bars + 10;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
-  int* abort_flag = reinterpret_cast<int*>(bars + 12);
+  uint64_t* b_full = bars + 1;     // [STAGES]
+  uint64_t* b_empty = bars + 5;    // [STAGES]
+  uint64_t* acc_full = bars + 9;   // [NACC]
+  uint64_t* acc_empty = bars + 13; // [NACC]
+  uint64_t* mma_done = bars + 17;
+  uint64_t* a_empty = bars + 18;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
+  int* abort_flag = reinterpret_cast<int*>(bars + 20);
 
   const int64_t lo = (int64_t)blockIdx.x * a.total / gridDim.x;
   const int64_t hi = (int64_t)(blockIdx.x + 1) * a.total / gridDim.x;
@@ -127,11 +130,13 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     mbar_init(a_full, 1);
     mbar_init(a_empty, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
+    }
+    for (int s = 0; s < C::NACC; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 4);
+      mbar_init(&acc_empty[s], 8);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -153,10 +158,10 @@ __global__ void __launch_bounds__(192, 1)
       Item w = item_at(a, lo);
       int64_t cur_rt = -1;
       int cur_g = -1, a_loads = 0;
-      int issued[2] = {0, 0};
+      int issued[C::STAGES] = {};
       for (int64_t k = 0; k < hi - lo; ++k, item_next(a, w)) {
-        const int s = (int)(k & 1);
-        if (!mbar_wait(&b_empty[s], (uint32_t)((k >> 1) & 1) ^ 1, ab, status, 101)) break;
+        const int s = (int)(k % C::STAGES);
+        if (!mbar_wait(&b_empty[s], (uint32_t)((k / C::STAGES) & 1) ^ 1, ab, status, 101)) break;
         mbar_expect_tx(&b_full[s], C::STAGE_BYTES);
         uint8_t* sb = smem + C::OFF_B + s * C::STAGE_BYTES;
         const int32_t brow = (int32_t)(w.g * a.nblk + w.n * C::BN);
@@ -180,7 +185,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       if (ab.set()) {  // let every copy this CTA started land before it exits
         if (a_loads > 0) mbar_wait_drain(a_full, (a_loads - 1) & 1, status, 198);
-        for (int s = 0; s < 2; ++s)
+        for (int s = 0; s < C::STAGES; ++s)
           if (issued[s] > 0) mbar_wait_drain(&b_full[s], (issued[s] - 1) & 1, status, 197);
       }
     }
@@ -194,7 +199,7 @@ __global__ void __launch_bounds__(192, 1)
       int64_t cur_rt = -1;
       int cur_g = -1, a_uses = 0;
       for (int64_t k = 0; k < hi - lo; ++k, item_next(a, w)) {
-        const int s = (int)(k & 1), acc = (int)(k & 1);
+        const int s = (int)(k % C::STAGES), acc = (int)(k % C::NACC);
         if (w.rt != cur_rt || w.g != cur_g) {
           if (a_uses > 0) umma_commit(a_empty);  // old operand free once its MMAs finish
           if (!mbar_wait(a_full, a_uses & 1, ab, status, 102)) break;
@@ -202,8 +207,8 @@ __global__ void __launch_bounds__(192, 1)
           cur_rt = w.rt;
           cur_g = w.g;
         }
-        if (!mbar_wait(&b_full[s], (uint32_t)((k >> 1) & 1), ab, status, 103)) break;
-        if (!mbar_wait(&acc_empty[acc], (uint32_t)((k >> 1) & 1) ^ 1, ab, status, 104)) break;
+        if (!mbar_wait(&b_full[s], (uint32_t)((k / C::STAGES) & 1), ab, status, 103)) break;
+        if (!mbar_wait(&acc_empty[acc], (uint32_t)((k / C::NACC) & 1) ^ 1, ab, status, 104)) break;
         tc_fence_after();
         const uint32_t b_hi = smem_u32(smem + C::OFF_B + s * C::STAGE_BYTES);
         const uint32_t b_lo = b_hi + C::B_BYTES;
@@ -228,16 +233,16 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // --------------------------------------------------------------- epilogue
-    const int q = warp & 3;  // TMEM lane quadrant of this warp
+    const int q = warp & 3;           // TMEM lane quadrant of this warp
+    const int eh = (warp - 2) >> 2;   // which 64 of the tile's 128 columns
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    uint8_t* stg = smem + C::OFF_STG + (warp - 2) * 2 * C::STG_BYTES;
+    uint8_t* stg = smem + C::OFF_STG + (warp - 2) * C::STG_BYTES;
     const float ninf = -__int_as_float(0x7f800000);
     const bool vec = (a.nblk & 3) == 0;
-    int sc = 0;  // boxes this warp has stored
     if (lo < hi) {
       Item w = item_at(a, lo);
       for (int64_t k = 0; k < hi - lo; ++k, item_next(a, w)) {
-        const int acc = (int)(k & 1);
+        const int acc = (int)(k % C::NACC);
         const int64_t tl_row = w.rt * C::BM + q * 32;  // first row of this warp, local
         const int64_t t = a.q_begin + tl_row + lane;
         const bool valid = t < a.q_end;
@@ -245,15 +250,15 @@ __global__ void __launch_bounds__(192, 1)
         if (nh > a.nblk) nh = a.nblk;
         float* row = a.scores + ((int64_t)w.g * a.nq + tl_row + lane) * a.nblk;
         // outcome made warp-uniform: tcgen05.ld below is warp-collective
-        const bool ok = mbar_wait(&acc_full[acc], (uint32_t)((k >> 1) & 1), ab, status, 105);
+        const bool ok = mbar_wait(&acc_full[acc], (uint32_t)((k / C::NACC) & 1), ab, status, 105);
         if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = eh * (C::BN / 64); cc < (eh + 1) * (C::BN / 64); ++cc) {
           uint32_t v[32];
           tmem_ld32(tl + acc * C::BN + cc * 32, v);
           tmem_wait_ld();
-          if (cc == 3) {
+          if (cc == (eh + 1) * (C::BN / 64) - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -264,8 +269,8 @@ __global__ void __launch_bounds__(192, 1)
             if (j0 + i >= nh) v[i] = __float_as_uint(ninf);
           if (a.tma_store) {
             if (j0 >= a.nblk || tl_row >= a.nq) continue;  // box wholly outside (warp-uniform)
-            uint8_t* buf = stg + (sc & 1) * C::STG_BYTES;
-            if (lane == 0) bulk_wait_read<1>();  // the box stored from `buf` two boxes ago
+            uint8_t* buf = stg;
+            if (lane == 0) bulk_wait_read<0>();  // the box last stored from `buf`
             __syncwarp();
 #pragma unroll
             for (int c = 0; c < 8; ++c)
@@ -277,7 +282,6 @@ __global__ void __launch_bounds__(192, 1)
               tma_store_3d(&ms, buf, (int32_t)j0, (int32_t)tl_row, w.g);
               bulk_commit_group();
             }
-            ++sc;
           } else if (valid) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
@@ -292,7 +296,7 @@ __global__ void __launch_bounds__(192, 1)
             }
           }
         }
-        if (a.fill_tail && w.n == w.nt - 1) {
+        if (a.fill_tail && w.n == w.nt - 1 && eh == 0) {
           // columns past the row tile's last computed tile are never historical
           const int64_t jt = w.nt * C::BN;
           if (a.tma_store) {
