@@ -16,9 +16,8 @@
 // Keys are gathered 128 per stage.
 //
 // Roles (12 warps):
-//  warp 0   builds each stage's block list from the union entries (a 4-deep
-//           ring, so the lists run ahead of the loads), with each query's
-//           selected blocks as a bitmask;
+//  warp 0   builds each stage's block list from the union entries (an
+//           8-deep ring, so the lists run ahead of the loads);
 //  warp 11  issues the K loads: for B >= 8 one contiguous bulk copy per block
 //           from the block-packed, pre-swizzled K (see k_kv_pack), for B < 8 a
 //           cp.async row gather from the original layout;
@@ -51,8 +50,20 @@ struct MetaT {         // one stage's block list
   int32_t pad;
   int32_t blk[NBPS];
   uint64_t mask[NBPS]; // bit qi: query qi of the sub-tile may attend the block
-  uint32_t qbits[64];  // bit bs: query qi selected the (historical) block in slot bs
 };
+
+// Bit bs (bs < diag): query qi of the sub-tile selected the historical block
+// in slot bs of this stage.
+template <typename Meta>
+__device__ __forceinline__ uint32_t qbits_of(const Meta& m, int qi) {
+  constexpr int N = (int)(sizeof(m.blk) / sizeof(m.blk[0]));
+  uint32_t hb = 0u;
+#pragma unroll
+  for (int bs = 0; bs < (N < 32 ? N : 32); ++bs)
+    hb |= (uint32_t)((m.mask[bs] >> qi) & 1ull) << bs;
+  const int diag = m.diag;
+  return diag >= 32 ? hb : (hb & ((1u << diag) - 1u));
+}
 
 template <int D, int B>
 struct AttnCfg {
@@ -62,7 +73,7 @@ struct AttnCfg {
   static constexpr bool TMA = B >= 8;  // blocks are whole 8-row swizzle atoms
   static constexpr int SK = 3;            // K slots
   static constexpr int SV = 2;            // V slots
-  static constexpr int NM = 4;            // stage block-list slots
+  static constexpr int NM = 8;            // stage block-list slots
   static constexpr int KC = D / 64;
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_TILE = KB * D * 2;
@@ -73,7 +84,7 @@ struct AttnCfg {
   static constexpr int META_BYTES = (int)((sizeof(MetaT<NBPS>) + 15) / 16 * 16);
   static constexpr int OFF_X = OFF_META + NM * META_BYTES;  // epilogue max / sum exchange
   static constexpr int OFF_BAR = OFF_X + 2 * 2 * BM * 4;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;  // S[2] at 0 / 128, O[2] at 256 / 384
   static constexpr int NTHREADS = 384;        // 3 pipeline warps, 8 softmax warps, K loads
   static_assert(SMEM <= 232448, "shared memory plan");
@@ -230,20 +241,30 @@ __device__ void gen_stage(const AttnArgs& a, Gen& gs, Meta& m, int nbps, int sh,
   }
   __syncwarp();
   if (nbps <= 32) {
-    // per query of the sub-tile: the historical blocks of this stage it
-    // selected (lane = block slot; one ballot per query)
+    // first slot holding a current block of the sub-tile (the slots before it
+    // are historical; the softmax threads read their queries' bits from them)
     const bool inb = lane < n;
     const int32_t blk = inb ? m.blk[lane] : 0;
-    const uint64_t msk = inb ? m.mask[lane] : 0ull;
     const uint32_t cur_m = __ballot_sync(FULL, inb && blk >= gs.c0);
-    const int diag = cur_m ? __ffs(cur_m) - 1 : n;
-    const uint32_t hist_m = diag >= 32 ? FULL : ((1u << diag) - 1u);
-    for (int qi = 0; qi < nq; ++qi) {
-      const uint32_t bits = __ballot_sync(FULL, (msk >> qi) & 1ull) & hist_m;
-      if (lane == 0) m.qbits[qi] = bits;
-    }
-    if (lane == 0) m.diag = diag;
+    if (lane == 0) m.diag = cur_m ? __ffs(cur_m) - 1 : n;
     __syncwarp();
+  }
+}
+
+// Bulk-copy a stage's packed blocks into shared slots 0..NBPS-1 (warp-wide):
+// lane bs copies block blk[bs] (the zero block `zb` past nb).  One copy per
+// block measured faster than merging runs of neighbouring blocks into one
+// copy or splitting blocks into smaller copies.
+template <int NBPS>
+__device__ __forceinline__ void copy_blocks(uint8_t* dst, const __nv_bfloat16* base,
+                                            const int32_t* blk, int nb, int64_t zb,
+                                            int blk_elems, uint64_t* bar) {
+  static_assert(NBPS <= 32, "one lane per slot");
+  const int lane = lane_id();
+  if (lane < NBPS) {
+    const int64_t b = lane < nb ? (int64_t)blk[lane] : zb;
+    bulk_load(dst + (size_t)lane * blk_elems * 2, base + b * blk_elems,
+              (uint32_t)blk_elems * 2u, bar);
   }
 }
 
@@ -277,16 +298,16 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* v_full = bars + 7;     // [SV]
   uint64_t* v_empty = bars + 9;    // [SV]
   uint64_t* m_full = bars + 11;    // [NM]
-  uint64_t* m_empty = bars + 15;   // [NM]
-  uint64_t* s_full = bars + 19;    // [2]
-  uint64_t* s_empty = bars + 21;   // [2]
-  uint64_t* p_full = bars + 23;    // [2] P of a stage of softmax group g written
-  uint64_t* mma_done = bars + 25;
-  uint64_t* p_empty = bars + 26;   // [2] PV product into O[g] done
-  uint64_t* l_bar = bars + 28;     // both groups' maxima and sums exchanged (epilogue)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 29);
-  int* abort_flag = reinterpret_cast<int*>(bars + 30);
-  volatile int* n_stages = reinterpret_cast<volatile int*>(bars + 31);  // set once known
+  uint64_t* m_empty = bars + 19;   // [NM]
+  uint64_t* s_full = bars + 27;    // [2]
+  uint64_t* s_empty = bars + 29;   // [2]
+  uint64_t* p_full = bars + 31;    // [2] P of a stage of softmax group g written
+  uint64_t* mma_done = bars + 33;
+  uint64_t* p_empty = bars + 34;   // [2] PV product into O[g] done
+  uint64_t* l_bar = bars + 36;     // both groups' maxima and sums exchanged (epilogue)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 37);
+  int* abort_flag = reinterpret_cast<int*>(bars + 38);
+  volatile int* n_stages = reinterpret_cast<volatile int*>(bars + 39);  // set once known
   float* xmax = reinterpret_cast<float*>(smem + C::OFF_X);  // [2 group][BM]
   float* xsum = xmax + 2 * C::BM;                            // [2 group][BM]
 
@@ -389,11 +410,8 @@ __global__ void __launch_bounds__(384, 1)
         constexpr uint32_t BLK = B * D * 2;
         if (lane == 0) mbar_expect_tx(&k_full[ks], C::KV_TILE);
         __syncwarp();
-        if (lane < NBPS) {
-          const __nv_bfloat16* kg = a.Kp + (int64_t)g * (a.nblkp + 1) * (B * D);
-          const int64_t b = lane < m.nb ? (int64_t)m.blk[lane] : a.nblkp;  // zero block
-          bulk_load(sK + lane * BLK, kg + b * (B * D), BLK, &k_full[ks]);
-        }
+        copy_blocks<NBPS>(sK, a.Kp + (int64_t)g * (a.nblkp + 1) * (B * D), m.blk, m.nb,
+                              a.nblkp, B * D, &k_full[ks]);
         ++issued_k[ks];
       } else {
         const int nkeys = m.nb * B;
@@ -435,11 +453,8 @@ __global__ void __launch_bounds__(384, 1)
         constexpr uint32_t BLK = B * D * 2;
         if (lane == 0) mbar_expect_tx(&v_full[vs], C::KV_TILE);
         __syncwarp();
-        if (lane < NBPS) {
-          const __nv_bfloat16* vg = a.Vp + (int64_t)g * (a.nblkp + 1) * (B * D);
-          const int64_t b = lane < m.nb ? (int64_t)m.blk[lane] : a.nblkp;
-          bulk_load(sV + lane * BLK, vg + b * (B * D), BLK, &v_full[vs]);
-        }
+        copy_blocks<NBPS>(sV, a.Vp + (int64_t)g * (a.nblkp + 1) * (B * D), m.blk, m.nb,
+                              a.nblkp, B * D, &v_full[vs]);
         ++issued_v[vs];
       } else {
         const int nkeys = m.nb * B;
@@ -627,7 +642,7 @@ __global__ void __launch_bounds__(384, 1)
         int bsd = 0;  // first slot handled block by block
         if constexpr (kTma) {
           // historical blocks: the query's bitmask, one bit per block -> B keys
-          const uint32_t hb = m.qbits[qi];
+          const uint32_t hb = qbits_of(m, qi);
           if constexpr (B == 8) {
             al0 = ((((hb >> 0) & 0xFu) * 0x00204081u) & 0x01010101u) * 0xFFu;
             al1 = ((((hb >> 4) & 0xFu) * 0x00204081u) & 0x01010101u) * 0xFFu;
@@ -674,7 +689,7 @@ __global__ void __launch_bounds__(384, 1)
       if constexpr (kTma) by_block = m.diag >= nb;
       if (fast && by_block) {
         constexpr int BPHh = 64 / B;  // blocks per 64 keys
-        const uint32_t hb = row_ok ? m.qbits[qi] : 0u;
+        const uint32_t hb = row_ok ? qbits_of(m, qi) : 0u;
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t v[64];
