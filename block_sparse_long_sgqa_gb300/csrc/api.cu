@@ -15,7 +15,8 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
                              int32_t* sel, int64_t* union_off, int32_t* union_len,
                              int32_t* union_blk, uint64_t* union_mask, int64_t union_cap,
                              int64_t lay_tau0, int64_t lay_ntiles, int64_t capG,
-                             int32_t* status, cudaStream_t st);
+                             int32_t* status, cudaStream_t st, const uint2* cand,
+                             const int32_t* ccnt, int caph, int32_t* rest, int32_t* nrest);
 int launch_sparse_attn_layout(const Dims& dm, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                               const __nv_bfloat16* V, const __nv_bfloat16* Kp,
                               const __nv_bfloat16* Vp, const int32_t* page_table,
@@ -193,9 +194,25 @@ AttnWs carve_attn(Carve& c, const Dims& dm) {
   return w;
 }
 
+// Whether some query of [q0, q1) selects from threshold candidates (nh grows
+// with the query, so the range's ends bound it).
+bool chunk_filtered(const Dims& dm, int64_t q0, int64_t q1) {
+  if (q1 <= q0 || dm.Ks > kFiltMaxNeed || sampled_cols(dm) == 0) return false;
+  const int64_t lo = nh_of(dm, q0), hi = nh_of(dm, q1 - 1);
+  return hi >= kFiltMinNh && lo <= kFiltMaxNh;
+}
+
 struct PrefillWs {
   IndexWs ix;
   AttnWs at;
+  bool filt;              // some chunk selects from threshold candidates
+  __nv_bfloat16 *shi, *slo;  // sampled block keys [Hkv][sampled_cols][d]
+  float* ssc;             // sampled scores [Hkv][chunk][sampled_cols]
+  float* tau;             // thresholds [Hkv][chunk]
+  uint2* cand;            // candidates [Hkv][chunk][2][kCandHalf]
+  int32_t* ccnt;          // counts [Hkv][chunk][2][2]
+  int32_t* rest;          // rows left for the full-row select [Hkv][chunk]
+  int32_t* nrest;         // their count
   float* scores;
   int32_t* sel;
   int64_t* uoff;
@@ -210,6 +227,23 @@ PrefillWs carve_prefill(Carve& c, const Dims& dm) {
   w.chunk_tiles = w.chunk / dm.W;
   w.ix = carve_index(c, dm, w.chunk);
   w.at = carve_attn(c, dm);
+  w.filt = dm.nblk > 0 && chunk_filtered(dm, 0, dm.T);
+  w.shi = w.slo = nullptr;
+  w.ssc = w.tau = nullptr;
+  w.cand = nullptr;
+  w.ccnt = nullptr;
+  w.rest = w.nrest = nullptr;
+  if (w.filt) {
+    const int64_t ns = sampled_cols(dm), rows = (int64_t)dm.Hkv * w.chunk;
+    w.shi = c.take<__nv_bfloat16>((size_t)dm.Hkv * ns * dm.d);
+    w.slo = c.take<__nv_bfloat16>((size_t)dm.Hkv * ns * dm.d);
+    w.ssc = c.take<float>((size_t)rows * ns);
+    w.tau = c.take<float>((size_t)rows);
+    w.cand = c.take<uint2>((size_t)rows * 2 * kCandHalf);
+    w.ccnt = c.take<int32_t>((size_t)rows * 4);
+    w.rest = c.take<int32_t>((size_t)rows);
+    w.nrest = c.take<int32_t>(1);
+  }
   w.scores = c.take<float>((size_t)dm.Hkv * w.chunk * std::max<int64_t>(dm.nblk, 1));
   w.sel = c.take<int32_t>((size_t)dm.Hkv * w.chunk * std::max(dm.Ks, 1));
   // slot layout of one chunk: the largest chunk's caps
@@ -426,6 +460,7 @@ SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, co
       e = launch_split_kbar(part, Kbar + o, w.ix.khi + o, w.ix.klo + o, st);
     }
   }
+  if (e == cudaSuccess && w.filt) e = launch_sample_keys(dm, w.ix.khi, w.ix.klo, w.shi, w.slo, st);
   const __nv_bfloat16 *q, *k, *v;
   if (e == cudaSuccess) e = stage_attn(dm, Q, K, V, page_table, w.at, &q, &k, &v, st);
   if (e != cudaSuccess) return SGQA_ERR_CUDA;
@@ -433,15 +468,31 @@ SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, co
   for (int64_t q0 = 0; q0 < dm.T; q0 += w.chunk) {
     const int64_t q1 = std::min<int64_t>(dm.T, q0 + w.chunk);
     const int64_t tau0 = q0 / dm.W, tau1 = (q1 + dm.W - 1) / dm.W;
+    const bool filt = w.filt && chunk_filtered(dm, q0, q1);
     if (dm.nblk > 0) {
       e = launch_index_query(dm, Q, q0, q1, w.ix.qhi, w.ix.qlo, st);
       if (e != cudaSuccess) return SGQA_ERR_CUDA;
+      IndexMode mode{};
+      if (filt) {  // thresholds from the sampled blocks' scores, then candidates
+        IndexMode ms{};
+        ms.sample = 1;
+        rc = launch_index_scores(dm, w.ix.qhi, w.ix.qlo, w.shi, w.slo, q0, q1, w.ssc, false,
+                                 status, st, &ms);
+        if (rc == SGQA_OK) rc = launch_row_tau(dm, w.ssc, q0, q1, w.tau, st);
+        if (rc != SGQA_OK) return rc;
+        mode.tau = w.tau;
+        mode.cand = w.cand;
+        mode.ccnt = w.ccnt;
+        mode.caph = kCandHalf;
+      }
       rc = launch_index_scores(dm, w.ix.qhi, w.ix.qlo, w.ix.khi, w.ix.klo, q0, q1, w.scores,
-                               false, status, st);
+                               false, status, st, &mode);
       if (rc != SGQA_OK) return rc;
     }
     rc = launch_topk_union_layout(dm, w.scores, q0, q1, w.sel, w.uoff, w.ulen, w.ublk, w.umask,
-                                  w.ucap, tau0, w.chunk_tiles, w.capG, status, st);
+                                  w.ucap, tau0, w.chunk_tiles, w.capG, status, st,
+                                  filt ? w.cand : nullptr, filt ? w.ccnt : nullptr, kCandHalf,
+                                  w.rest, w.nrest);
     if (rc != SGQA_OK) return rc;
     rc = launch_sparse_attn_layout(dm, q, k, v, w.at.Kp, w.at.Vp, page_table, w.uoff, w.ulen,
                                    w.ublk, w.umask, O, lse, tau0, tau1, tau0, w.chunk_tiles,
@@ -461,10 +512,18 @@ SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int
     // with an empty block-key cache: merge, operand staging (fp32 rounding,
     // K/V block packing), then per chunk the index query and indexer GEMM
     // (when there are blocks), top-k rows, tile union and attention
+    // (plus, where some rows select from threshold candidates, the sampled-key
+    // gather once and per such chunk the sampled-block GEMM, the thresholds
+    // and the candidate select)
     const int64_t nchunks = (dm.T + chunk - 1) / chunk;
     int64_t n = (dm.nblk > 0 ? 1 : 0) + (dm.dtype == SGQA_FP32 ? (dm.B >= 8 ? 1 : 3) : 0) +
                 (dm.B >= 8 ? 2 : 0);
     n += nchunks * ((dm.nblk > 0 ? 2 : 0) + topk_union_launches(dm) + 1);
+    if (dm.nblk > 0 && chunk_filtered(dm, 0, dm.T)) {
+      n += 1;
+      for (int64_t q0 = 0; q0 < dm.T; q0 += chunk)
+        if (chunk_filtered(dm, q0, std::min<int64_t>(dm.T, q0 + chunk))) n += 3;
+    }
     *launches = (int32_t)n;
   }
   return SGQA_OK;

@@ -21,6 +21,16 @@
 // apply the causal block mask and write the tile.  Stores go
 // through a 128-byte-swizzled shared staging buffer and TMA, so each tile
 // leaves as full 128-byte rows instead of 16-byte pieces of 32 rows.
+//
+// Two further modes serve the fused prefill.  Sampled mode scores only the
+// sampled blocks (8 adjacent blocks of every 64, gathered into their own key
+// array beforehand), so a row has (nh / 64) * 8 columns.  Filter mode also
+// compares each score with its row's candidate threshold (derived from the
+// sampled scores) and appends every score at or above it, with its block
+// index, to the row's candidate list: one list per 64-column half of the
+// tile, and per half a front part (the CTA that starts the row tile, written
+// upwards) and a back part (the CTA that finishes it, written downwards from
+// the end of the list), so no two threads ever share a counter.
 #include <algorithm>
 #include <cstring>
 
@@ -54,22 +64,37 @@ struct IdxCfg {
 };
 
 struct IdxArgs {
-  int64_t nq, q_begin, q_end, q_offset, nblk;
+  int64_t nq, q_begin, q_end, q_offset;
+  int64_t nblk;       // columns of a score row (key rows per group)
+  int64_t nblk_full;  // complete blocks of the call (bounds nh)
   int B, Hkv;
+  int sample;      // columns are the sampled blocks: a row has (nh / 64) * 8 of them
   int64_t total;   // work items of the launch
   int fill_tail;   // write -inf for the columns past a row tile's last item
   int tma_store;   // scores rows are 16-byte multiples: store through the tensor map
   float* scores;
+  // filter mode (tau != nullptr): candidates at or above the row's threshold
+  const float* tau;  // [Hkv][nq]; NaN: the row takes no candidates
+  uint2* cand;       // [Hkv][nq][2 halves][caph] (score bits, block)
+  int32_t* ccnt;     // [Hkv][nq][2 halves][front, back] counts
+  int caph;
   int32_t* status;
 };
+
+// Valid columns of row t: its historical blocks, or in sampled mode the
+// samples of its complete 64-block groups.
+__device__ __forceinline__ int64_t bound_of(const IdxArgs& a, int64_t t) {
+  int64_t nh = (a.q_offset + t) / a.B;
+  if (nh > a.nblk_full) nh = a.nblk_full;
+  return a.sample ? ((nh >> 6) << 3) : nh;
+}
 
 // Column tiles of row tile rt (at least one, so rows with no complete block
 // still get their -inf row).
 __device__ __forceinline__ int64_t ntiles_of(const IdxArgs& a, int64_t rt) {
   const int64_t t0 = a.q_begin + rt * 128;
   const int64_t t_last = (t0 + 128 < a.q_end ? t0 + 128 : a.q_end) - 1;
-  int64_t nh = (a.q_offset + t_last) / a.B;
-  if (nh > a.nblk) nh = a.nblk;
+  const int64_t nh = bound_of(a, t_last);
   const int64_t nt = (nh + IDX_BN - 1) / IDX_BN;
   return nt > 0 ? nt : 1;
 }
@@ -239,16 +264,25 @@ __global__ void __launch_bounds__(320, 1)
     uint8_t* stg = smem + C::OFF_STG + (warp - 2) * C::STG_BYTES;
     const float ninf = -__int_as_float(0x7f800000);
     const bool vec = (a.nblk & 3) == 0;
+    const bool filt = a.tau != nullptr;
     if (lo < hi) {
       Item w = item_at(a, lo);
+      float tau_r = 0.f;     // this thread's row threshold (filter mode)
+      int64_t seg_n0 = 0;    // first column tile of the current segment
+      int cn = 0;            // candidates of the current segment
       for (int64_t k = 0; k < hi - lo; ++k, item_next(a, w)) {
         const int acc = (int)(k % C::NACC);
         const int64_t tl_row = w.rt * C::BM + q * 32;  // first row of this warp, local
         const int64_t t = a.q_begin + tl_row + lane;
         const bool valid = t < a.q_end;
-        int64_t nh = (a.q_offset + t) / a.B;
-        if (nh > a.nblk) nh = a.nblk;
+        const int64_t nh = bound_of(a, t);
         float* row = a.scores + ((int64_t)w.g * a.nq + tl_row + lane) * a.nblk;
+        const int64_t crow = ((int64_t)w.g * a.nq + tl_row + lane) * 2 + eh;  // candidate list
+        if (filt && (k == 0 || w.n == 0)) {  // a new (row tile, group) segment
+          seg_n0 = w.n;
+          cn = 0;
+          tau_r = valid ? a.tau[(int64_t)w.g * a.nq + tl_row + lane] : __int_as_float(0x7fffffff);
+        }
         // outcome made warp-uniform: tcgen05.ld below is warp-collective
         const bool ok = mbar_wait(&acc_full[acc], (uint32_t)((k / C::NACC) & 1), ab, status, 105);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -267,6 +301,11 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (j0 + i >= nh) v[i] = __float_as_uint(ninf);
+          uint32_t fm = 0u;  // this thread's candidates among the 32 columns
+          if (filt) {        // (NaN thresholds and -inf scores take nothing)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) fm |= (uint32_t)(__uint_as_float(v[i]) >= tau_r) << i;
+          }
           if (a.tma_store) {
             if (j0 >= a.nblk || tl_row >= a.nq) continue;  // box wholly outside (warp-uniform)
             uint8_t* buf = stg;
@@ -294,6 +333,38 @@ __global__ void __launch_bounds__(320, 1)
                   if (j + e < a.nblk) row[j + e] = __uint_as_float(v[i + e]);
               }
             }
+          }
+          if (fm != 0u) {
+            // the candidates' scores are read back from this thread's row of
+            // the staging box (the TMA path staged it above; otherwise the box
+            // is free and staged here)
+            uint8_t* mine = stg + lane * 128;
+            if (!a.tma_store) {
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(mine + ((c ^ (lane & 7)) << 4)) =
+                    make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            }
+            uint2* cl = a.cand + crow * a.caph;
+            const bool front = seg_n0 == 0;
+            do {
+              const int i = __ffs(fm) - 1;
+              fm &= fm - 1u;
+              const uint32_t x =
+                  *reinterpret_cast<const uint32_t*>(mine + (((i >> 2) ^ (lane & 7)) << 4) + (i & 3) * 4);
+              if (cn < a.caph) cl[front ? cn : a.caph - 1 - cn] = make_uint2(x, (uint32_t)(j0 + i));
+              ++cn;
+            } while (fm != 0u);
+          }
+        }
+        if (filt && valid && (w.n == w.nt - 1 || k == hi - lo - 1)) {  // segment ends
+          int32_t* cc = a.ccnt + crow * 2;
+          if (seg_n0 == 0) {
+            cc[0] = cn;
+            if (w.n == w.nt - 1) cc[1] = 0;  // one CTA covered the whole row tile
+          } else {
+            cc[1] = cn;
+            if (w.n != w.nt - 1) report(status, SGQA_ERR_BOUNDS, (int)t);  // a third segment
           }
         }
         if (a.fill_tail && w.n == w.nt - 1 && eh == 0) {
@@ -352,37 +423,48 @@ bool make_tmap_scores(CUtensorMap* map, float* base, int64_t nblk, int64_t nq, i
 template <int D>
 int launch_impl(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* qlo,
                 const __nv_bfloat16* khi, const __nv_bfloat16* klo, int64_t q_begin,
-                int64_t q_end, float* scores, bool fill_tail, int32_t* status, cudaStream_t st) {
+                int64_t q_end, float* scores, bool fill_tail, int32_t* status, cudaStream_t st,
+                const IndexMode& mode) {
   using C = IdxCfg<D>;
   IdxArgs a;
   a.nq = q_end - q_begin;
   a.q_begin = q_begin;
   a.q_end = q_end;
   a.q_offset = dm.off;
-  a.nblk = dm.nblk;
+  a.nblk_full = dm.nblk;
+  a.sample = mode.sample ? 1 : 0;
+  a.nblk = mode.sample ? sampled_cols(dm) : dm.nblk;
   a.B = dm.B;
   a.Hkv = dm.Hkv;
   a.fill_tail = fill_tail ? 1 : 0;
-  a.tma_store = (dm.nblk % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) & 15u) == 0) ? 1 : 0;
+  a.tma_store = (a.nblk % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) & 15u) == 0) ? 1 : 0;
   a.scores = scores;
+  a.tau = mode.tau;
+  a.cand = mode.cand;
+  a.ccnt = mode.ccnt;
+  a.caph = mode.caph;
   a.status = status;
   // items: sum over row tiles of Hkv * column tiles (same count as the kernel)
-  int64_t total = 0;
+  int64_t total = 0, max_nt = 1;
   for (int64_t t0 = q_begin; t0 < q_end; t0 += C::BM) {
     const int64_t t_last = std::min(t0 + C::BM, q_end) - 1;
-    const int64_t nh = std::min((dm.off + t_last) / dm.B, dm.nblk);
-    total += dm.Hkv * std::max<int64_t>(1, (nh + C::BN - 1) / C::BN);
+    int64_t nh = std::min((dm.off + t_last) / dm.B, dm.nblk);
+    if (a.sample) nh = (nh >> 6) << 3;
+    const int64_t nt = std::max<int64_t>(1, (nh + C::BN - 1) / C::BN);
+    total += dm.Hkv * nt;
+    max_nt = std::max(max_nt, nt);
   }
+  if (a.nblk == 0) return SGQA_OK;
   a.total = total;
   CUtensorMap m_qhi, m_qlo, m_khi, m_klo, m_s;
   const uint64_t row_bytes = (uint64_t)D * 2;
   if (!make_tmap_2d_bf16(&m_qhi, qhi, D, (uint64_t)dm.Hkv * a.nq, row_bytes, 64, C::BM) ||
       !make_tmap_2d_bf16(&m_qlo, qlo, D, (uint64_t)dm.Hkv * a.nq, row_bytes, 64, C::BM) ||
-      !make_tmap_2d_bf16(&m_khi, khi, D, (uint64_t)dm.Hkv * dm.nblk, row_bytes, 64, C::BN) ||
-      !make_tmap_2d_bf16(&m_klo, klo, D, (uint64_t)dm.Hkv * dm.nblk, row_bytes, 64, C::BN))
+      !make_tmap_2d_bf16(&m_khi, khi, D, (uint64_t)dm.Hkv * a.nblk, row_bytes, 64, C::BN) ||
+      !make_tmap_2d_bf16(&m_klo, klo, D, (uint64_t)dm.Hkv * a.nblk, row_bytes, 64, C::BN))
     return SGQA_ERR_CUDA;
   if (a.tma_store) {
-    if (!make_tmap_scores(&m_s, scores, dm.nblk, a.nq, dm.Hkv)) return SGQA_ERR_CUDA;
+    if (!make_tmap_scores(&m_s, scores, a.nblk, a.nq, dm.Hkv)) return SGQA_ERR_CUDA;
   } else {
     std::memset(&m_s, 0, sizeof(m_s));
   }
@@ -393,8 +475,12 @@ int launch_impl(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* q
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
     return SGQA_ERR_CUDA;
-  const unsigned grid = (unsigned)std::min<int64_t>(total, nsm);
-  log_begin(SGQA_K_INDEX_SCORES, st);
+  int64_t ctas = std::min<int64_t>(total, nsm);
+  // filter mode: every CTA takes at least a whole row tile's items, so a row
+  // tile is split between at most two CTAs (front and back candidate parts)
+  if (a.tau != nullptr) ctas = std::max<int64_t>(1, std::min<int64_t>(ctas, total / max_nt));
+  const unsigned grid = (unsigned)ctas;
+  log_begin(a.sample ? SGQA_K_SAMPLE_SCORES : SGQA_K_INDEX_SCORES, st);
   k_index_scores<D><<<grid, C::NTHREADS, C::SMEM, st>>>(m_qhi, m_qlo, m_khi, m_klo, m_s, a);
   log_end(st);
   return cudaGetLastError() == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA;
@@ -405,12 +491,18 @@ int launch_impl(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* q
 int launch_index_scores(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* qlo,
                         const __nv_bfloat16* khi, const __nv_bfloat16* klo, int64_t q_begin,
                         int64_t q_end, float* scores, bool fill_tail, int32_t* status,
-                        cudaStream_t st) {
+                        cudaStream_t st, const IndexMode* mode) {
   if (q_end <= q_begin || dm.nblk == 0) return SGQA_OK;  // nothing to score
+  const IndexMode plain{};
+  const IndexMode& m = mode ? *mode : plain;
+  if (m.tau != nullptr && (m.cand == nullptr || m.ccnt == nullptr || m.caph < 1))
+    return SGQA_ERR_INVALID_ARG;
   if (dm.d == 128)
-    return launch_impl<128>(dm, qhi, qlo, khi, klo, q_begin, q_end, scores, fill_tail, status, st);
+    return launch_impl<128>(dm, qhi, qlo, khi, klo, q_begin, q_end, scores, fill_tail, status, st,
+                            m);
   if (dm.d == 64)
-    return launch_impl<64>(dm, qhi, qlo, khi, klo, q_begin, q_end, scores, fill_tail, status, st);
+    return launch_impl<64>(dm, qhi, qlo, khi, klo, q_begin, q_end, scores, fill_tail, status, st,
+                           m);
   return SGQA_ERR_UNSUPPORTED;
 }
 

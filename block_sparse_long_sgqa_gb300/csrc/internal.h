@@ -68,6 +68,35 @@ inline int64_t kv_pack_elems(const Dims& dm) {
   return (int64_t)dm.Hkv * ((dm.Tkv + dm.B - 1) / dm.B + 1) * dm.B * dm.d;
 }
 
+// ---- threshold candidates of the fused prefill
+// A row (query, group) selects from candidates when it has 2048 .. 16384
+// historical blocks and keeps at most 768 of them: its threshold comes from
+// the scores of the sampled blocks (8 adjacent blocks of every 64; the row's
+// complete 64-block groups give (nh / 64) * 8 samples), the indexer keeps
+// every score at or above it, and the row is selected from those candidates
+// unless they miss the selection or overflow (then from its full scores).
+constexpr int64_t kFiltMinNh = 2048, kFiltMaxNh = 16384;
+constexpr int64_t kFiltMaxNeed = 768;
+constexpr int kCandHalf = 1024;  // candidates per half-row list
+__host__ __device__ inline bool filter_row(int64_t nh, int64_t need) {
+  return nh >= kFiltMinNh && nh <= kFiltMaxNh && need <= kFiltMaxNeed && need < nh;
+}
+// Sampled key rows per group.
+inline int64_t sampled_cols(const Dims& dm) { return (dm.nblk >> 6) << 3; }
+
+// Gather the sampled blocks' hi/lo keys: [Hkv][sampled_cols][d] each.
+cudaError_t launch_sample_keys(const Dims& dm, const __nv_bfloat16* khi, const __nv_bfloat16* klo,
+                               __nv_bfloat16* shi, __nv_bfloat16* slo, cudaStream_t st);
+
+// Optional modes of the indexer GEMM (all zero: plain scores).
+struct IndexMode {
+  int sample;        // khi/klo are the sampled keys; scores [Hkv][nq][sampled_cols]
+  const float* tau;  // filter mode: [Hkv][nq] thresholds (NaN: no candidates)
+  uint2* cand;       // [Hkv][nq][2][caph] (score bits, block index)
+  int32_t* ccnt;     // [Hkv][nq][2][2] front / back counts per half
+  int caph;
+};
+
 // scores [Hkv][q_end-q_begin][nblk]; qhi/qlo are [Hkv][q_end-q_begin][d].
 // Every score of a causal block is written, and -inf for the other blocks of
 // each row's last 128-block tile; fill_tail also writes -inf for all blocks
@@ -75,7 +104,13 @@ inline int64_t kv_pack_elems(const Dims& dm) {
 int launch_index_scores(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* qlo,
                         const __nv_bfloat16* khi, const __nv_bfloat16* klo, int64_t q_begin,
                         int64_t q_end, float* scores, bool fill_tail, int32_t* status,
-                        cudaStream_t st);
+                        cudaStream_t st, const IndexMode* mode = nullptr);
+
+// Candidate thresholds [Hkv][nq] of the call's queries [q_begin, q_end) from
+// their sampled scores [Hkv][nq][sampled_cols] (NaN for rows that do not
+// select from candidates).
+int launch_row_tau(const Dims& dm, const float* sample_scores, int64_t q_begin, int64_t q_end,
+                   float* tau, cudaStream_t st);
 
 size_t topk_union_ws_bytes(const Dims& dm, int64_t nq);
 // Kernel launches of one top-k/union call (aligned score buffers).

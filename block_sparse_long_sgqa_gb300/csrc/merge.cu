@@ -200,6 +200,25 @@ __global__ void __launch_bounds__(256) k_kv_pack(const T* __restrict__ X,
   }
 }
 
+// Sampled block keys for the candidate thresholds of the fused prefill: of
+// every 64 blocks of a group, the first 8 (the hi and lo halves, 16 bytes per
+// thread): out[g][s] = in[g][(s / 8) * 64 + s % 8].
+__global__ void __launch_bounds__(256) k_sample_keys(const uint4* __restrict__ khi,
+                                                     const uint4* __restrict__ klo, int64_t nblk,
+                                                     int64_t ns, int Hkv, int c16,
+                                                     uint4* __restrict__ shi,
+                                                     uint4* __restrict__ slo) {
+  const int64_t n = (int64_t)Hkv * ns * c16;
+  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < n;
+       x += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t c = x % c16, r = x / c16;
+    const int64_t g = r / ns, si = r % ns;
+    const int64_t src = (g * nblk + (si >> 3) * 64 + (si & 7)) * c16 + c;
+    shi[x] = khi[src];
+    slo[x] = klo[src];
+  }
+}
+
 int grid_for(int64_t work) {
   // enough CTAs to cover every SM several times; grid-stride loops do the rest
   int64_t g = (work + 255) / 256;
@@ -252,6 +271,21 @@ cudaError_t launch_split_kbar(const Dims& dm, const float* Kbar, __nv_bfloat16* 
   if (n8 == 0) return cudaSuccess;
   log_begin(SGQA_K_SPLIT, st);
   k_split_kbar<<<grid_for(n8), 256, 0, st>>>(Kbar, n8, khi, klo);
+  log_end(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sample_keys(const Dims& dm, const __nv_bfloat16* khi, const __nv_bfloat16* klo,
+                               __nv_bfloat16* shi, __nv_bfloat16* slo, cudaStream_t st) {
+  const int64_t ns = sampled_cols(dm);
+  const int c16 = dm.d / 8;
+  const int64_t n = (int64_t)dm.Hkv * ns * c16;
+  if (n == 0) return cudaSuccess;
+  log_begin(SGQA_K_SPLIT, st);
+  k_sample_keys<<<grid_for(n), 256, 0, st>>>(reinterpret_cast<const uint4*>(khi),
+                                             reinterpret_cast<const uint4*>(klo), dm.nblk, ns,
+                                             dm.Hkv, c16, reinterpret_cast<uint4*>(shi),
+                                             reinterpret_cast<uint4*>(slo));
   log_end(st);
   return cudaGetLastError();
 }

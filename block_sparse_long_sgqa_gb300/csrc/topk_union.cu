@@ -57,6 +57,11 @@ struct TUArgs {
   int64_t tau_begin;    // first tile of this launch
   int nwords;           // ceil(nblk / 32)
   int nw;               // warps per CTA
+  const uint2* cand;    // fused prefill: threshold candidates [Hkv][nq][2][caph] (null: none)
+  const int32_t* ccnt;  // their front / back counts per half [Hkv][nq][2][2]
+  int caph;
+  int32_t* rest;        // rows (g * nq + local row) left for the full-row select
+  int32_t* nrest;       // their count
   int32_t* status;
 };
 
@@ -517,9 +522,21 @@ __device__ Sel warp_radix_select(const uint32_t* keys, int stride, uint32_t n, u
   return s;
 }
 
+// Threshold key from ns >= 1 sample keys in shared memory: the key ranked at
+// the expected count of the selection in the sample plus nsd standard
+// deviations, rounded down to the prefix the radix select resolved.
+__device__ uint32_t sample_rank_key(const uint32_t* samp, int ns, int64_t nh, uint32_t need,
+                                    uint32_t* hist, float nsd) {
+  const float e = (float)need * (float)ns / (float)nh;
+  uint32_t r = (uint32_t)ceilf(e + nsd * sqrtf(e));
+  if (r > (uint32_t)ns) r = ns;
+  if (r < 1) r = 1;
+  const Sel sl = warp_radix_select(samp, 1, ns, r, hist, 2);
+  return sl.sh >= 32 ? sl.kmin : (sl.T << sl.sh);
+}
+
 // Sampled threshold (as a key): 8 adjacent blocks of every 64 (two lanes per
-// group), ranked at the expected count of the selection in the sample plus
-// three standard deviations.
+// group) read from the row itself.
 __device__ __noinline__ uint32_t sample_tau(const float* __restrict__ row, int64_t nh, uint32_t need,
                                uint32_t* hist, uint32_t* samp) {
   const int lane = lane_id();
@@ -543,12 +560,7 @@ __device__ __noinline__ uint32_t sample_tau(const float* __restrict__ row, int64
     }
   }
   __syncwarp();
-  const float e = (float)need * (float)ns / (float)nh;
-  uint32_t r = (uint32_t)ceilf(e + 3.f * sqrtf(e));
-  if (r > (uint32_t)ns) r = ns;
-  if (r < 1) r = 1;
-  const Sel sl = warp_radix_select(samp, 1, ns, r, hist, 2);
-  return sl.sh >= 32 ? sl.kmin : (sl.T << sl.sh);
+  return sample_rank_key(samp, ns, nh, need, hist, 3.f);
 }
 
 // Compact every block with score >= tf into cand (key, block), in block order.
@@ -868,6 +880,19 @@ __global__ void __launch_bounds__(ROW_WARPS * 32, 4) k_topk_rows(TUArgs a) {
   const int warp = warp_id();
   uint32_t* wsm = reinterpret_cast<uint32_t*>(smem + (size_t)warp * WARP_BYTES);
   const int64_t nwt = (int64_t)gridDim.x * ROW_WARPS;
+  if (a.rest != nullptr) {  // the rows the candidate select left, one at a time
+    const int64_t nr = *a.nrest;
+    for (int64_t i = (int64_t)blockIdx.x * ROW_WARPS + warp; i < nr; i += nwt) {
+      const int64_t rr = a.rest[i];
+      const int g = (int)(rr / a.nq);
+      const int64_t lr = rr % a.nq;
+      Pred pr;
+      pr.valid = false;
+      if (lane_id() == 0) prefetch_row_l2(a, g, lr);
+      select_row(a, g, a.q_begin + lr, wsm, pr);
+    }
+    return;
+  }
   const int64_t bpg = (a.nq + ROW_BLOCK - 1) / ROW_BLOCK;  // row blocks per group
   for (int64_t b = (int64_t)blockIdx.x * ROW_WARPS + warp; b < bpg * a.Hkv; b += nwt) {
     const int g = (int)(b / bpg);
@@ -948,7 +973,266 @@ __global__ void __launch_bounds__(UNION_THREADS) k_tile_union(TUArgs a, int64_t 
 
 }  // namespace
 
+namespace {
+
+// Candidate thresholds: one warp per row loads the row's sampled scores as
+// keys into shared memory and ranks them (sample_rank_key).
+constexpr int TAU_WARPS = 8;
+constexpr float TAU_NSD = 5.f;
+// five standard deviations: about 1.6 k/B candidates, and on the clustered
+// 128K workload no row with fewer than k/B or more than 2.5 k/B of them
+constexpr int TAU_SAMP = 2048;  // (kFiltMaxNh / 64) * 8 samples at most
+constexpr int TAU_WARP_BYTES = 1024 + TAU_SAMP * 4;
+static_assert((kFiltMaxNh >> 6) << 3 <= TAU_SAMP, "sample buffer");
+
+__global__ void __launch_bounds__(TAU_WARPS * 32) k_row_tau(const float* __restrict__ ssc,
+                                                            float* __restrict__ tau, int64_t nq,
+                                                            int64_t q_begin, int64_t off,
+                                                            int64_t nblk, int64_t ns_max, int lgB,
+                                                            int Ks, int Hkv) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int warp = warp_id(), lane = lane_id();
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + (size_t)warp * TAU_WARP_BYTES);
+  uint32_t* samp = hist + 256;
+  const int64_t rg = (int64_t)blockIdx.x * TAU_WARPS + warp;  // g * nq + local row
+  if (rg >= nq * Hkv) return;
+  const int64_t t = q_begin + rg % nq;
+  int64_t nh = (off + t) >> lgB;
+  if (nh > nblk) nh = nblk;
+  const int64_t need = nh < Ks ? nh : Ks;
+  float out = __int_as_float(0x7fffffff);
+  if (filter_row(nh, need)) {
+    const int ns = (int)((nh >> 6) << 3);
+    const float4* r4 = reinterpret_cast<const float4*>(ssc + rg * ns_max);
+    for (int i0 = 0; i0 < ns / 4; i0 += 128) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * 32 + lane;
+        v[u] = i < ns / 4 ? __ldg(r4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * 32 + lane;
+        if (i < ns / 4)
+          *reinterpret_cast<uint4*>(samp + 4 * i) = make_uint4(
+              order_key(v[u].x), order_key(v[u].y), order_key(v[u].z), order_key(v[u].w));
+      }
+    }
+    __syncwarp();
+    out = key_to_float(sample_rank_key(samp, ns, nh, (uint32_t)need, hist, TAU_NSD));
+  }
+  if (lane == 0) tau[rg] = out;
+}
+
+// Selection from the indexer's threshold candidates (fused prefill): one warp
+// per row, rows dealt out round-robin.  The row's four candidate parts (front
+// and back of each half-row list) are gathered into shared memory as keys and
+// 16-bit block indices; a radix select finds the k-th key; the taken blocks
+// (above it, and of those equal to it the lowest-indexed ones) are marked in a
+// bitmap over the row's blocks; a prefix sum of the bitmap's word popcounts
+// then gives each taken block its place in the ascending list.  While a row is
+// selected, the next row's counts are loaded and its parts prefetched into L2.
+// A row whose candidates cannot decide it (a half-row list overflowed, fewer
+// than `need` or more than CR_CMAX of them), or that has too few or too many
+// blocks for the candidate scheme, is appended to the rest list for the
+// full-row select.
+constexpr int CR_WARPS = 8;
+constexpr int CR_CMAX = 1280;  // candidates a row can select from
+// per-warp scratch (32-bit words): radix histogram, taken bitmap A and tie
+// bitmap E (padded, one spare word per 32 so that a lane's 16 consecutive
+// words sit in distinct banks), keys, then 16-bit block indices
+constexpr int CR_HIST = 0, CR_A = 256, CR_E = CR_A + 528, CR_KEYS = CR_E + 528;
+constexpr int CR_IDX = CR_KEYS + CR_CMAX;
+constexpr int CR_WORDS = CR_IDX + CR_CMAX / 2;
+static_assert(kFiltMaxNh / 32 <= 512, "bitmap words");
+
+__device__ __forceinline__ int padw(int w) { return w + (w >> 5); }
+
+// Lanes 0-3: L2 prefetch of part `lane` of row rn's candidate lists (16-byte
+// rounded; the lists are 16-byte aligned and caph is even).
+__device__ __forceinline__ void prefetch_cands(const TUArgs& a, int64_t rn, int32_t cnt) {
+  const int lane = lane_id();
+  if (lane >= 4 || cnt <= 0 || cnt > a.caph) return;
+  const int start = (lane & 1) ? a.caph - cnt : 0;
+  const int s0 = start & ~1, s1 = (start + cnt + 1) & ~1;
+  const uint2* p = a.cand + (rn * 2 + (lane >> 1)) * a.caph + s0;
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"((uint32_t)(s1 - s0) * 8u)
+               : "memory");
+}
+
+__device__ __noinline__ bool cand_row(const TUArgs& a, int64_t r, int64_t nh, uint32_t need,
+                                      int32_t cv, int64_t rn, int32_t cv_next, uint32_t* wsm,
+                                      int32_t* out, int64_t t) {
+  const int lane = lane_id();
+  const int f0 = __shfl_sync(FULL, cv, 0), b0 = __shfl_sync(FULL, cv, 1);
+  const int f1 = __shfl_sync(FULL, cv, 2), b1 = __shfl_sync(FULL, cv, 3);
+  const int C = f0 + b0 + f1 + b1;
+  if (min(min(f0, b0), min(f1, b1)) < 0 || f0 + b0 > a.caph || f1 + b1 > a.caph ||
+      C < (int)need || C > CR_CMAX) {
+    prefetch_cands(a, rn, cv_next);
+    return false;
+  }
+  uint32_t* keys = wsm + CR_KEYS;
+  uint16_t* idx = reinterpret_cast<uint16_t*>(wsm + CR_IDX);
+  const uint2* l0 = a.cand + r * 2 * a.caph;
+  const uint2* l1 = l0 + a.caph;
+  const int e0 = f0, e1 = f0 + b0, e2 = e1 + f1;  // ends of the parts in gather order
+  bool bad = false;
+  for (int base = 0; base < C; base += 512) {
+    uint2 v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = base + u * 32 + lane;
+      const uint2* src = i < e0 ? l0 + i
+                         : i < e1 ? l0 + (a.caph - b0) + (i - e0)
+                         : i < e2 ? l1 + (i - e1)
+                                  : l1 + (a.caph - b1) + (i - e2);
+      v[u] = i < C ? __ldg(src) : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = base + u * 32 + lane;
+      if (i < C) {
+        bad |= v[u].y >= (uint32_t)nh;
+        keys[i] = order_key(__uint_as_float(v[u].x));
+        idx[i] = (uint16_t)v[u].y;
+      }
+    }
+  }
+  prefetch_cands(a, rn, cv_next);
+  if (__any_sync(FULL, bad)) {  // not a list this indexer wrote
+    if (lane == 0) report(a.status, SGQA_ERR_BOUNDS, (int)t);
+    return false;
+  }
+  uint32_t* A = wsm + CR_A;
+  uint32_t* E = wsm + CR_E;
+  for (int w = lane; w < 528; w += 32) A[w] = 0u;
+  __syncwarp();
+  const Sel sl = warp_radix_select(keys, 1, (uint32_t)C, need, wsm + CR_HIST, 4);
+  const bool ties = sl.cnt != sl.rem;
+  if (ties)
+    for (int w = lane; w < 528; w += 32) E[w] = 0u;
+  __syncwarp();
+  for (int i = lane; i < C; i += 32) {
+    const uint32_t kp = sl.sh >= 32 ? 0u : (keys[i] >> sl.sh);
+    const uint32_t j = idx[i];
+    if (kp > sl.T || (kp == sl.T && !ties)) atomicOr(&A[padw(j >> 5)], 1u << (j & 31));
+    else if (kp == sl.T) atomicOr(&E[padw(j >> 5)], 1u << (j & 31));
+  }
+  __syncwarp();
+  if (ties) {  // the first sl.rem tied blocks in ascending order join A
+    int left = (int)sl.rem;
+    for (int w0 = 0; w0 < 512 && left > 0; w0 += 32) {
+      const int w = padw(w0 + lane);
+      const uint32_t e = E[w];
+      const int n = __popc(e);
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int take = max(0, min(n, left - (incl - n)));
+      if (take == n) {
+        if (n) A[w] |= e;
+      } else if (take > 0) {
+        A[w] |= e & ((2u << __fns(e, 0, take)) - 1u);  // its lowest `take` set bits
+      }
+      left -= __shfl_sync(FULL, incl, 31);
+    }
+    __syncwarp();
+  }
+  // exclusive prefix of the word popcounts (lane: words 16 lane .. 16 lane + 15) into E
+  uint32_t* P = E;
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) sum += __popc(A[padw(16 * lane + i)]);
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int total = __shfl_sync(FULL, incl, 31);
+  int run = incl - sum;
+  __syncwarp();  // the tie pass's reads of E are done
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int w = padw(16 * lane + i);
+    P[w] = (uint32_t)run;
+    run += __popc(A[w]);
+  }
+  __syncwarp();
+  for (int i = lane; i < C; i += 32) {
+    const uint32_t j = idx[i];
+    const int w = padw(j >> 5);
+    const uint32_t m = A[w], bit = 1u << (j & 31);
+    if (m & bit) {
+      const uint32_t pos = P[w] + __popc(m & (bit - 1u));
+      if (pos < need) out[pos] = (int32_t)j;
+    }
+  }
+  for (int64_t x = need + lane; x < a.Ks; x += 32) out[x] = -1;
+  if (lane == 0 && total != (int)need) report(a.status, SGQA_ERR_BOUNDS, (int)t);
+  __syncwarp();
+  return true;
+}
+
+__global__ void __launch_bounds__(CR_WARPS * 32, 2) k_cand_rows(TUArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int warp = warp_id(), lane = lane_id();
+  uint32_t* wsm = reinterpret_cast<uint32_t*>(smem) + warp * CR_WORDS;
+  const int64_t W = (int64_t)gridDim.x * CR_WARPS;
+  const int64_t nrows = a.nq * a.Hkv;
+  int64_t r = (int64_t)blockIdx.x * CR_WARPS + warp;
+  int32_t cv = (r < nrows && lane < 4) ? a.ccnt[r * 4 + lane] : 0;
+  for (; r < nrows; r += W) {
+    const int64_t rn = r + W;
+    const int32_t cv_next = (rn < nrows && lane < 4) ? a.ccnt[rn * 4 + lane] : 0;
+    const int64_t t = a.q_begin + r % a.nq;
+    int64_t nh = (a.off + t) >> a.lgB;
+    if (nh > a.nblk) nh = a.nblk;
+    const uint32_t need = (uint32_t)(nh < a.Ks ? nh : a.Ks);
+    int32_t* out = a.sel + r * a.Ks;
+    bool done;
+    if ((int64_t)need == nh) {  // every historical block (or none)
+      for (int64_t x = lane; x < a.Ks; x += 32) out[x] = x < nh ? (int32_t)x : -1;
+      prefetch_cands(a, rn, cv_next);
+      done = true;
+    } else if (filter_row(nh, need)) {
+      done = cand_row(a, r, nh, need, cv, rn, cv_next, wsm, out, t);
+    } else {
+      prefetch_cands(a, rn, cv_next);
+      done = false;
+    }
+    if (!done && lane == 0) a.rest[atomicAdd(a.nrest, 1)] = (int32_t)r;
+    cv = cv_next;
+  }
+}
+
+}  // namespace
+
 int topk_union_launches(const Dims&) { return 2; }
+
+int launch_row_tau(const Dims& dm, const float* sample_scores, int64_t q_begin, int64_t q_end,
+                   float* tau, cudaStream_t st) {
+  const int64_t nq = q_end - q_begin;
+  if (nq <= 0) return SGQA_OK;
+  const int64_t ns_max = sampled_cols(dm);
+  if ((ns_max & 3) || (reinterpret_cast<uintptr_t>(sample_scores) & 15u)) return SGQA_ERR_ALIGNMENT;
+  const int64_t rows = nq * dm.Hkv;
+  const size_t smem = (size_t)TAU_WARPS * TAU_WARP_BYTES;
+  if (cudaFuncSetAttribute(k_row_tau, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return SGQA_ERR_CUDA;
+  log_begin(SGQA_K_ROW_TAU, st);
+  k_row_tau<<<(unsigned)((rows + TAU_WARPS - 1) / TAU_WARPS), TAU_WARPS * 32, smem, st>>>(
+      sample_scores, tau, nq, q_begin, dm.off, dm.nblk, ns_max, __builtin_ctz((unsigned)dm.B),
+      dm.Ks, dm.Hkv);
+  log_end(st);
+  return cudaGetLastError() == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA;
+}
 
 size_t topk_union_ws_bytes(const Dims& dm, int64_t nq) {
   return (size_t)dm.Hkv * nq * (dm.Ks > 0 ? dm.Ks : 1) * sizeof(int32_t);
@@ -960,9 +1244,18 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
                              int32_t* sel, int64_t* union_off, int32_t* union_len,
                              int32_t* union_blk, uint64_t* union_mask, int64_t union_cap,
                              int64_t lay_tau0, int64_t lay_ntiles, int64_t capG,
-                             int32_t* status, cudaStream_t st) {
+                             int32_t* status, cudaStream_t st, const uint2* cand,
+                             const int32_t* ccnt, int caph, int32_t* rest, int32_t* nrest) {
   if (q_end <= q_begin) return SGQA_OK;
+  if (cand != nullptr && (ccnt == nullptr || rest == nullptr || nrest == nullptr || caph < 2 ||
+                          (caph & 1)))
+    return SGQA_ERR_INVALID_ARG;
   TUArgs a;
+  a.cand = cand;
+  a.ccnt = ccnt;
+  a.caph = caph;
+  a.rest = nullptr;
+  a.nrest = nrest;
   a.scores = scores;
   a.nq = q_end - q_begin;
   a.q_begin = q_begin;
@@ -1010,11 +1303,26 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
   const int64_t mask_pairs =
       std::min<int64_t>(std::min<int64_t>(u_max, 4096), (int64_t)(mask_budget / 8));
   const size_t union_smem = fixed + (size_t)mask_pairs * 8 + (cache_lists ? list_bytes : 0);
+  const size_t cand_smem = (size_t)CR_WARPS * CR_WORDS * 4;
   if (cudaFuncSetAttribute(k_topk_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)row_smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k_cand_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)cand_smem) != cudaSuccess ||
       cudaFuncSetAttribute(k_tile_union, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)union_smem) != cudaSuccess)
     return SGQA_ERR_CUDA;
+  if (cand != nullptr) {
+    // candidate select for every row, then the full-row select of the rows it left
+    a.rest = rest;
+    if (cudaMemsetAsync(nrest, 0, sizeof(int32_t), st) != cudaSuccess) return SGQA_ERR_CUDA;
+    const int64_t nrows = a.nq * dm.Hkv;
+    const int64_t cand_ctas =
+        std::min<int64_t>((nrows + CR_WARPS - 1) / CR_WARPS, (int64_t)nsm * 2);
+    log_begin(SGQA_K_TOPK_UNION, st);
+    k_cand_rows<<<(unsigned)cand_ctas, CR_WARPS * 32, cand_smem, st>>>(a);
+    log_end(st);
+    if (cudaGetLastError() != cudaSuccess) return SGQA_ERR_CUDA;
+  }
   log_begin(SGQA_K_TOPK_UNION, st);
   k_topk_rows<<<(unsigned)row_ctas, ROW_WARPS * 32, row_smem, st>>>(a);
   log_end(st);
@@ -1031,7 +1339,7 @@ int launch_topk_union(const Dims& dm, const float* scores, int64_t q_begin, int6
                       uint64_t* union_mask, int64_t union_cap, int32_t* status, cudaStream_t st) {
   return launch_topk_union_layout(dm, scores, q_begin, q_end, sel, union_off, union_len,
                                   union_blk, union_mask, union_cap, 0, dm.ntiles, group_cap(dm),
-                                  status, st);
+                                  status, st, nullptr, nullptr, 0, nullptr, nullptr);
 }
 
 }  // namespace sgqa

@@ -34,10 +34,11 @@ EXPORTED = ("sgqa_workspace_bytes", "sgqa_union_capacity", "sgqa_block_merge", "
             "sgqa_prefill_plan",
             "sgqa_set_launch_log", "sgqa_reset_status", "sgqa_read_status", "sgqa_status_string",
             "sgqa_version")
-K_MERGE, K_SPLIT, K_INDEX_QUERY, K_INDEX_SCORES, K_TOPK_UNION, K_ATTN, K_STAGE, K_TILE_UNION = (
-    1, 2, 3, 4, 5, 6, 7, 8)
+(K_MERGE, K_SPLIT, K_INDEX_QUERY, K_INDEX_SCORES, K_TOPK_UNION, K_ATTN, K_STAGE, K_TILE_UNION,
+ K_SAMPLE_SCORES, K_ROW_TAU) = (1, 2, 3, 4, 5, 6, 7, 8, 9, 10)
 KERNEL_NAMES = {1: "merge", 2: "split", 3: "index_query", 4: "index_scores", 5: "topk_union",
-                6: "sparse_attn", 7: "stage_bf16", 8: "tile_union"}
+                6: "sparse_attn", 7: "stage_bf16", 8: "tile_union", 9: "sample_scores",
+                10: "row_tau"}
 
 
 class Params(ctypes.Structure):

@@ -228,13 +228,15 @@ SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int
 /* Kernel classes named in the launch log. */
 enum sgqa_kernel_kind {
   SGQA_K_MERGE = 1,        /* block merge */
-  SGQA_K_SPLIT = 2,        /* bf16 hi/lo split of cached block keys */
+  SGQA_K_SPLIT = 2,        /* bf16 hi/lo split of cached block keys; sampled-key gather */
   SGQA_K_INDEX_QUERY = 3,  /* group index query (mean of heads, hi/lo split) */
   SGQA_K_INDEX_SCORES = 4, /* tensor-core indexer GEMM */
   SGQA_K_TOPK_UNION = 5,   /* top-k selection (per query row) */
   SGQA_K_ATTN = 6,         /* sparse attention */
   SGQA_K_STAGE = 7,        /* attention operand staging: bf16 rounding, K/V block packing */
-  SGQA_K_TILE_UNION = 8    /* tile union and member masks */
+  SGQA_K_TILE_UNION = 8,   /* tile union and member masks */
+  SGQA_K_SAMPLE_SCORES = 9, /* indexer GEMM over the sampled blocks (fused prefill) */
+  SGQA_K_ROW_TAU = 10       /* candidate thresholds from the sampled scores */
 };
 
 /* Optional launch log for measurement.  While a log is installed, every

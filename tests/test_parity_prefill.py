@@ -155,3 +155,54 @@ def test_prefill_full_size_sampled(s, name):
     rows = rows[rows >= wl.seq_q - 4096]  # one contiguous range for the standalone selection
     _, frac = check_end_to_end(s, wl, inp, O, lse, rows, Kbar, d)
     assert frac > 0.8
+
+
+def composition(s, p, d, Kbar):
+    """The fused prefill's steps called one by one through the C ABI: full
+    score rows, the row select on them, the tile union and the attention."""
+    nblk = p.seq_kv // p.block_size
+    scores = torch.empty(p.n_kv_heads, p.seq_q, nblk, device="cuda")
+    s.sgqa_index_scores(p, d["Q"], Kbar, 0, p.seq_q, scores, s.alloc_workspace(p, s.WS_INDEX_SCORES))
+    sel = torch.empty(p.n_kv_heads, p.seq_q, p.topk_tokens // p.block_size, dtype=torch.int32,
+                      device="cuda")
+    uo, ul, ub, um = s.alloc_union(p)
+    st = s.new_status()
+    s.sgqa_topk_union(p, scores, 0, p.seq_q, sel, uo, ul, ub, um, status=st)
+    O, lse = s.alloc_outputs(p)
+    s.sgqa_sparse_attn_fwd(p, d["Q"], d["K"], d["V"], uo, ul, ub, um, O, lse,
+                           page_table=d["page_table"], ws=s.alloc_workspace(p, s.WS_SPARSE_ATTN),
+                           status=st)
+    assert s.read_status(st)[0] == 0
+    return O, lse
+
+
+# Rows of 2560 .. 2815 blocks: every row of the fused call selects from the
+# indexer's threshold candidates.  "period61" repeats the block keys with a
+# period of 61 blocks, so each score value occurs about 45 times and the k-th
+# score is tied (the lowest-index rule decides); "period2" leaves two distinct
+# scores, so the candidates overflow and every row falls back to its full
+# score row.
+FILT = synth.WORKLOADS["gqa_32k"].replace(name="filt", seq_q=2048, seq_kv=22528, q_offset=20480)
+
+
+def periodic_keys(inp, period):
+    K = inp["K"]
+    pos = np.arange(K.shape[0])
+    return dict(inp, K=np.ascontiguousarray(K[(pos // 8 % period) * 8 + pos % 8]))
+
+
+@pytest.mark.parametrize("case", ["clustered", "period61", "period2", "gqa_32k"])
+def test_prefill_candidates_equal_full_select(s, case):
+    """The fused prefill selects rows of 2048 .. 16384 blocks from threshold
+    candidates; those lists must be the ones the full score rows give, so the
+    fused output equals the step-by-step composition bit for bit."""
+    wl = synth.WORKLOADS["gqa_32k"] if case == "gqa_32k" else FILT
+    inp = synth.make_inputs(wl)
+    if case.startswith("period"):
+        inp = periodic_keys(inp, int(case[6:]))
+    p = s.params_for(wl)
+    d = dev_inputs(inp)
+    O, lse, Kbar = run_prefill(s, p, d)
+    O2, lse2 = composition(s, p, d, Kbar)
+    assert torch.equal(O, O2)
+    assert torch.equal(lse, lse2)
