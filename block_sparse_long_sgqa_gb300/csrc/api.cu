@@ -15,8 +15,8 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
                              int32_t* sel, int64_t* union_off, int32_t* union_len,
                              int32_t* union_blk, uint64_t* union_mask, int64_t union_cap,
                              int64_t lay_tau0, int64_t lay_ntiles, int64_t capG,
-                             int32_t* status, cudaStream_t st, const uint2* cand,
-                             const int32_t* ccnt, int caph, int32_t* rest, int32_t* nrest);
+                             int32_t* status, cudaStream_t st, int32_t* rest,
+                             int32_t* nrest);
 int launch_sparse_attn_layout(const Dims& dm, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                               const __nv_bfloat16* V, const __nv_bfloat16* Kp,
                               const __nv_bfloat16* Vp, const int32_t* page_table,
@@ -212,7 +212,8 @@ struct PrefillWs {
   uint2* cand;            // candidates [Hkv][chunk][2][kCandHalf]
   int32_t* ccnt;          // counts [Hkv][chunk][2][2]
   int32_t* rest;          // rows left for the full-row select [Hkv][chunk]
-  int32_t* nrest;         // their count
+  int32_t* counters;      // [0]: rows in rest, [1]: row tiles in flist
+  int32_t *tflag, *flist;  // row tiles to score in full [Hkv][ceil(chunk / 128)]
   float* scores;
   int32_t* sel;
   int64_t* uoff;
@@ -232,7 +233,7 @@ PrefillWs carve_prefill(Carve& c, const Dims& dm) {
   w.ssc = w.tau = nullptr;
   w.cand = nullptr;
   w.ccnt = nullptr;
-  w.rest = w.nrest = nullptr;
+  w.rest = w.counters = w.tflag = w.flist = nullptr;
   if (w.filt) {
     const int64_t ns = sampled_cols(dm), rows = (int64_t)dm.Hkv * w.chunk;
     w.shi = c.take<__nv_bfloat16>((size_t)dm.Hkv * ns * dm.d);
@@ -242,7 +243,10 @@ PrefillWs carve_prefill(Carve& c, const Dims& dm) {
     w.cand = c.take<uint2>((size_t)rows * 2 * kCandHalf);
     w.ccnt = c.take<int32_t>((size_t)rows * 4);
     w.rest = c.take<int32_t>((size_t)rows);
-    w.nrest = c.take<int32_t>(1);
+    w.counters = c.take<int32_t>(2);
+    const size_t nrt = (size_t)dm.Hkv * ((w.chunk + 127) / 128);
+    w.tflag = c.take<int32_t>(nrt);
+    w.flist = c.take<int32_t>(nrt);
   }
   w.scores = c.take<float>((size_t)dm.Hkv * w.chunk * std::max<int64_t>(dm.nblk, 1));
   w.sel = c.take<int32_t>((size_t)dm.Hkv * w.chunk * std::max(dm.Ks, 1));
@@ -488,11 +492,22 @@ SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, co
       rc = launch_index_scores(dm, w.ix.qhi, w.ix.qlo, w.ix.khi, w.ix.klo, q0, q1, w.scores,
                                false, status, st, &mode);
       if (rc != SGQA_OK) return rc;
+      if (filt) {  // candidate select; row tiles it could not decide get full score rows
+        rc = launch_cand_rows(dm, q0, q1, w.sel, w.cand, w.ccnt, kCandHalf, w.rest, w.counters,
+                              w.tflag, w.flist, status, st);
+        if (rc != SGQA_OK) return rc;
+        IndexMode mr{};
+        mr.flist = w.flist;
+        mr.nflist = w.counters + 1;
+        rc = launch_index_scores(dm, w.ix.qhi, w.ix.qlo, w.ix.khi, w.ix.klo, q0, q1, w.scores,
+                                 false, status, st, &mr);
+        if (rc != SGQA_OK) return rc;
+      }
     }
+    // full-row select (in a filtered chunk: of the rows the candidates left) and union
     rc = launch_topk_union_layout(dm, w.scores, q0, q1, w.sel, w.uoff, w.ulen, w.ublk, w.umask,
                                   w.ucap, tau0, w.chunk_tiles, w.capG, status, st,
-                                  filt ? w.cand : nullptr, filt ? w.ccnt : nullptr, kCandHalf,
-                                  w.rest, w.nrest);
+                                  filt ? w.rest : nullptr, filt ? w.counters : nullptr);
     if (rc != SGQA_OK) return rc;
     rc = launch_sparse_attn_layout(dm, q, k, v, w.at.Kp, w.at.Vp, page_table, w.uoff, w.ulen,
                                    w.ublk, w.umask, O, lse, tau0, tau1, tau0, w.chunk_tiles,
@@ -513,8 +528,8 @@ SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int
     // K/V block packing), then per chunk the index query and indexer GEMM
     // (when there are blocks), top-k rows, tile union and attention
     // (plus, where some rows select from threshold candidates, the sampled-key
-    // gather once and per such chunk the sampled-block GEMM, the thresholds
-    // and the candidate select)
+    // gather once and per such chunk the sampled-block GEMM, the thresholds,
+    // the candidate select and the refill GEMM of the row tiles it left)
     const int64_t nchunks = (dm.T + chunk - 1) / chunk;
     int64_t n = (dm.nblk > 0 ? 1 : 0) + (dm.dtype == SGQA_FP32 ? (dm.B >= 8 ? 1 : 3) : 0) +
                 (dm.B >= 8 ? 2 : 0);
@@ -522,7 +537,7 @@ SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int
     if (dm.nblk > 0 && chunk_filtered(dm, 0, dm.T)) {
       n += 1;
       for (int64_t q0 = 0; q0 < dm.T; q0 += chunk)
-        if (chunk_filtered(dm, q0, std::min<int64_t>(dm.T, q0 + chunk))) n += 3;
+        if (chunk_filtered(dm, q0, std::min<int64_t>(dm.T, q0 + chunk))) n += 4;
     }
     *launches = (int32_t)n;
   }

@@ -78,6 +78,11 @@ struct IdxArgs {
   uint2* cand;       // [Hkv][nq][2 halves][caph] (score bits, block)
   int32_t* ccnt;     // [Hkv][nq][2 halves][front, back] counts
   int caph;
+  // refill mode (flist != nullptr): only the listed (group, row tile) pairs,
+  // entries (g << 20) | rt, *nflist of them; the item count is found on the device
+  const int32_t* flist;
+  const int32_t* nflist;
+  int nfl;
   int32_t* status;
 };
 
@@ -99,14 +104,32 @@ __device__ __forceinline__ int64_t ntiles_of(const IdxArgs& a, int64_t rt) {
   return nt > 0 ? nt : 1;
 }
 
-// Items are ordered by row tile, then group, then column tile.
+// Items are ordered by row tile, then group, then column tile (in refill
+// mode: by list entry, then column tile).
 struct Item {
   int64_t rt, n, nt;
-  int g;
+  int g, li;
 };
+__device__ __forceinline__ void list_entry(const IdxArgs& a, Item& w) {
+  const int32_t e = a.flist[w.li];
+  w.g = e >> 20;
+  w.rt = e & 0xfffff;
+  w.nt = ntiles_of(a, w.rt);
+}
 __device__ Item item_at(const IdxArgs& a, int64_t i) {
   Item w;
   w.rt = 0;
+  w.li = 0;
+  if (a.flist != nullptr) {
+    for (;; ++w.li) {
+      list_entry(a, w);
+      if (i < w.nt) {
+        w.n = i;
+        return w;
+      }
+      i -= w.nt;
+    }
+  }
   for (;;) {
     const int64_t nt = ntiles_of(a, w.rt);
     if (i < nt * a.Hkv) {
@@ -122,6 +145,10 @@ __device__ Item item_at(const IdxArgs& a, int64_t i) {
 __device__ __forceinline__ void item_next(const IdxArgs& a, Item& w) {
   if (++w.n < w.nt) return;
   w.n = 0;
+  if (a.flist != nullptr) {
+    if (++w.li < a.nfl) list_entry(a, w);
+    return;
+  }
   if (++w.g < a.Hkv) return;
   w.g = 0;
   ++w.rt;
@@ -132,7 +159,14 @@ template <int D>
 __global__ void __launch_bounds__(320, 1)
     k_index_scores(const __grid_constant__ CUtensorMap mq_hi, const __grid_constant__ CUtensorMap mq_lo,
                    const __grid_constant__ CUtensorMap mk_hi, const __grid_constant__ CUtensorMap mk_lo,
-                   const __grid_constant__ CUtensorMap ms, IdxArgs a) {
+                   const __grid_constant__ CUtensorMap ms, const IdxArgs a0) {
+  IdxArgs a = a0;
+  if (a.flist != nullptr) {  // refill mode: items of the listed row tiles
+    a.nfl = *a.nflist;
+    int64_t tot = 0;
+    for (int i = 0; i < a.nfl; ++i) tot += ntiles_of(a, a.flist[i] & 0xfffff);
+    a.total = tot;
+  }
   using C = IdxCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -283,6 +317,9 @@ __global__ void __launch_bounds__(320, 1)
           cn = 0;
           tau_r = valid ? a.tau[(int64_t)w.g * a.nq + tl_row + lane] : __int_as_float(0x7fffffff);
         }
+        // filter mode keeps full score rows only for rows without a threshold
+        const bool keep = !filt || isnan(tau_r);
+        const bool store_box = __any_sync(0xffffffffu, valid && keep);
         // outcome made warp-uniform: tcgen05.ld below is warp-collective
         const bool ok = mbar_wait(&acc_full[acc], (uint32_t)((k / C::NACC) & 1), ab, status, 105);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -306,22 +343,26 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) fm |= (uint32_t)(__uint_as_float(v[i]) >= tau_r) << i;
           }
+          bool staged = false;  // this thread's row of the tile is in its staging box
           if (a.tma_store) {
-            if (j0 >= a.nblk || tl_row >= a.nq) continue;  // box wholly outside (warp-uniform)
-            uint8_t* buf = stg;
-            if (lane == 0) bulk_wait_read<0>();  // the box last stored from `buf`
-            __syncwarp();
+            if (store_box) {
+              if (j0 >= a.nblk || tl_row >= a.nq) continue;  // box wholly outside (warp-uniform)
+              uint8_t* buf = stg;
+              if (lane == 0) bulk_wait_read<0>();  // the box last stored from `buf`
+              __syncwarp();
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                  make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_3d(&ms, buf, (int32_t)j0, (int32_t)tl_row, w.g);
-              bulk_commit_group();
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                    make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(&ms, buf, (int32_t)j0, (int32_t)tl_row, w.g);
+                bulk_commit_group();
+              }
+              staged = true;
             }
-          } else if (valid) {
+          } else if (valid && keep) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
               const int64_t j = j0 + i;
@@ -334,17 +375,19 @@ __global__ void __launch_bounds__(320, 1)
               }
             }
           }
-          if (fm != 0u) {
-            // the candidates' scores are read back from this thread's row of
-            // the staging box (the TMA path staged it above; otherwise the box
-            // is free and staged here)
-            uint8_t* mine = stg + lane * 128;
-            if (!a.tma_store) {
+          // the candidates' scores are read back from this thread's row of the
+          // staging box (staged above when the box was stored, else here once
+          // the box's last store has read it)
+          uint8_t* mine = stg + lane * 128;
+          if (!staged && __any_sync(0xffffffffu, fm != 0u)) {
+            if (a.tma_store && lane == 0) bulk_wait_read<0>();
+            __syncwarp();
 #pragma unroll
-              for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(mine + ((c ^ (lane & 7)) << 4)) =
-                    make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-            }
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(mine + ((c ^ (lane & 7)) << 4)) =
+                  make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+          }
+          if (fm != 0u) {
             uint2* cl = a.cand + crow * a.caph;
             const bool front = seg_n0 == 0;
             do {
@@ -443,6 +486,9 @@ int launch_impl(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* q
   a.cand = mode.cand;
   a.ccnt = mode.ccnt;
   a.caph = mode.caph;
+  a.flist = mode.flist;
+  a.nflist = mode.nflist;
+  a.nfl = 0;
   a.status = status;
   // items: sum over row tiles of Hkv * column tiles (same count as the kernel)
   int64_t total = 0, max_nt = 1;
@@ -475,7 +521,8 @@ int launch_impl(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* q
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
     return SGQA_ERR_CUDA;
-  int64_t ctas = std::min<int64_t>(total, nsm);
+  // refill mode: the items are counted on the device; one CTA per SM
+  int64_t ctas = a.flist != nullptr ? nsm : std::min<int64_t>(total, nsm);
   // filter mode: every CTA takes at least a whole row tile's items, so a row
   // tile is split between at most two CTAs (front and back candidate parts)
   if (a.tau != nullptr) ctas = std::max<int64_t>(1, std::min<int64_t>(ctas, total / max_nt));

@@ -88,13 +88,18 @@ inline int64_t sampled_cols(const Dims& dm) { return (dm.nblk >> 6) << 3; }
 cudaError_t launch_sample_keys(const Dims& dm, const __nv_bfloat16* khi, const __nv_bfloat16* klo,
                                __nv_bfloat16* shi, __nv_bfloat16* slo, cudaStream_t st);
 
-// Optional modes of the indexer GEMM (all zero: plain scores).
+// Optional modes of the indexer GEMM (all zero: plain scores).  In filter
+// mode the full score rows are stored only for rows whose threshold is NaN.
 struct IndexMode {
   int sample;        // khi/klo are the sampled keys; scores [Hkv][nq][sampled_cols]
   const float* tau;  // filter mode: [Hkv][nq] thresholds (NaN: no candidates)
   uint2* cand;       // [Hkv][nq][2][caph] (score bits, block index)
   int32_t* ccnt;     // [Hkv][nq][2][2] front / back counts per half
   int caph;
+  // refill mode: full score rows of the listed (group, row tile) pairs only,
+  // entries (g << 20) | (local row / 128), *nflist of them (set on the device)
+  const int32_t* flist;
+  const int32_t* nflist;
 };
 
 // scores [Hkv][q_end-q_begin][nblk]; qhi/qlo are [Hkv][q_end-q_begin][d].
@@ -105,6 +110,15 @@ int launch_index_scores(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfl
                         const __nv_bfloat16* khi, const __nv_bfloat16* klo, int64_t q_begin,
                         int64_t q_end, float* scores, bool fill_tail, int32_t* status,
                         cudaStream_t st, const IndexMode* mode = nullptr);
+
+// Candidate select of every row of [q_begin, q_end) (lists into sel
+// [Hkv][nq][Ks]); rows it leaves go to rest (counters[0] of them), and the
+// row tiles of those that had candidates to flist (counters[1]; tflag
+// [Hkv][ceil(nq / 128)] marks them).  Zeroes counters and tflag first.
+int launch_cand_rows(const Dims& dm, int64_t q_begin, int64_t q_end, int32_t* sel,
+                     const uint2* cand, const int32_t* ccnt, int caph, int32_t* rest,
+                     int32_t* counters, int32_t* tflag, int32_t* flist, int32_t* status,
+                     cudaStream_t st);
 
 // Candidate thresholds [Hkv][nq] of the call's queries [q_begin, q_end) from
 // their sampled scores [Hkv][nq][sampled_cols] (NaN for rows that do not

@@ -26,6 +26,7 @@
 // is built from the lists with shared (or, for very long unions, global)
 // atomic ORs.
 #include <algorithm>
+#include <cstring>
 
 #include "common.cuh"
 #include "internal.h"
@@ -62,6 +63,9 @@ struct TUArgs {
   int caph;
   int32_t* rest;        // rows (g * nq + local row) left for the full-row select
   int32_t* nrest;       // their count
+  int32_t* tflag;       // [Hkv][ceil(nq / 128)]: row tile has a row the candidates left
+  int32_t* flist;       // flagged row tiles, (g << 20) | rt
+  int32_t* nflist;      // their count
   int32_t* status;
 };
 
@@ -1206,7 +1210,15 @@ __global__ void __launch_bounds__(CR_WARPS * 32, 2) k_cand_rows(TUArgs a) {
       prefetch_cands(a, rn, cv_next);
       done = false;
     }
-    if (!done && lane == 0) a.rest[atomicAdd(a.nrest, 1)] = (int32_t)r;
+    if (!done && lane == 0) {
+      a.rest[atomicAdd(a.nrest, 1)] = (int32_t)r;
+      if (filter_row(nh, need)) {  // its full score row is not stored: list its row tile
+        const int g = (int)(r / a.nq);
+        const int64_t rt = (r % a.nq) >> 7;
+        if (atomicExch(&a.tflag[(int64_t)g * ((a.nq + 127) >> 7) + rt], 1) == 0)
+          a.flist[atomicAdd(a.nflist, 1)] = (g << 20) | (int32_t)rt;
+      }
+    }
     cv = cv_next;
   }
 }
@@ -1214,6 +1226,56 @@ __global__ void __launch_bounds__(CR_WARPS * 32, 2) k_cand_rows(TUArgs a) {
 }  // namespace
 
 int topk_union_launches(const Dims&) { return 2; }
+
+int launch_cand_rows(const Dims& dm, int64_t q_begin, int64_t q_end, int32_t* sel,
+                     const uint2* cand, const int32_t* ccnt, int caph, int32_t* rest,
+                     int32_t* counters, int32_t* tflag, int32_t* flist, int32_t* status,
+                     cudaStream_t st) {
+  const int64_t nq = q_end - q_begin;
+  if (nq <= 0) return SGQA_OK;
+  if (caph < 2 || (caph & 1) || cand == nullptr || ccnt == nullptr) return SGQA_ERR_INVALID_ARG;
+  TUArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.nq = nq;
+  a.q_begin = q_begin;
+  a.q_end = q_end;
+  a.T = dm.T;
+  a.off = dm.off;
+  a.nblk = dm.nblk;
+  a.B = dm.B;
+  a.lgB = __builtin_ctz((unsigned)dm.B);
+  a.Ks = dm.Ks;
+  a.W = dm.W;
+  a.Hkv = dm.Hkv;
+  a.sel = sel;
+  a.cand = cand;
+  a.ccnt = ccnt;
+  a.caph = caph;
+  a.rest = rest;
+  a.nrest = counters;
+  a.nflist = counters + 1;
+  a.tflag = tflag;
+  a.flist = flist;
+  a.status = status;
+  const int64_t nrt = (nq + 127) / 128;
+  if (cudaMemsetAsync(counters, 0, 2 * sizeof(int32_t), st) != cudaSuccess ||
+      cudaMemsetAsync(tflag, 0, (size_t)dm.Hkv * nrt * sizeof(int32_t), st) != cudaSuccess)
+    return SGQA_ERR_CUDA;
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
+    return SGQA_ERR_CUDA;
+  const size_t smem = (size_t)CR_WARPS * CR_WORDS * 4;
+  if (cudaFuncSetAttribute(k_cand_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return SGQA_ERR_CUDA;
+  const int64_t nrows = nq * dm.Hkv;
+  const int64_t ctas = std::min<int64_t>((nrows + CR_WARPS - 1) / CR_WARPS, (int64_t)nsm * 2);
+  log_begin(SGQA_K_TOPK_UNION, st);
+  k_cand_rows<<<(unsigned)ctas, CR_WARPS * 32, smem, st>>>(a);
+  log_end(st);
+  return cudaGetLastError() == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA;
+}
 
 int launch_row_tau(const Dims& dm, const float* sample_scores, int64_t q_begin, int64_t q_end,
                    float* tau, cudaStream_t st) {
@@ -1244,17 +1306,13 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
                              int32_t* sel, int64_t* union_off, int32_t* union_len,
                              int32_t* union_blk, uint64_t* union_mask, int64_t union_cap,
                              int64_t lay_tau0, int64_t lay_ntiles, int64_t capG,
-                             int32_t* status, cudaStream_t st, const uint2* cand,
-                             const int32_t* ccnt, int caph, int32_t* rest, int32_t* nrest) {
+                             int32_t* status, cudaStream_t st, int32_t* rest,
+                             int32_t* nrest) {
   if (q_end <= q_begin) return SGQA_OK;
-  if (cand != nullptr && (ccnt == nullptr || rest == nullptr || nrest == nullptr || caph < 2 ||
-                          (caph & 1)))
-    return SGQA_ERR_INVALID_ARG;
+  if ((rest == nullptr) != (nrest == nullptr)) return SGQA_ERR_INVALID_ARG;
   TUArgs a;
-  a.cand = cand;
-  a.ccnt = ccnt;
-  a.caph = caph;
-  a.rest = nullptr;
+  std::memset(&a, 0, sizeof(a));
+  a.rest = rest;
   a.nrest = nrest;
   a.scores = scores;
   a.nq = q_end - q_begin;
@@ -1303,26 +1361,11 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
   const int64_t mask_pairs =
       std::min<int64_t>(std::min<int64_t>(u_max, 4096), (int64_t)(mask_budget / 8));
   const size_t union_smem = fixed + (size_t)mask_pairs * 8 + (cache_lists ? list_bytes : 0);
-  const size_t cand_smem = (size_t)CR_WARPS * CR_WORDS * 4;
   if (cudaFuncSetAttribute(k_topk_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)row_smem) != cudaSuccess ||
-      cudaFuncSetAttribute(k_cand_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)cand_smem) != cudaSuccess ||
       cudaFuncSetAttribute(k_tile_union, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)union_smem) != cudaSuccess)
     return SGQA_ERR_CUDA;
-  if (cand != nullptr) {
-    // candidate select for every row, then the full-row select of the rows it left
-    a.rest = rest;
-    if (cudaMemsetAsync(nrest, 0, sizeof(int32_t), st) != cudaSuccess) return SGQA_ERR_CUDA;
-    const int64_t nrows = a.nq * dm.Hkv;
-    const int64_t cand_ctas =
-        std::min<int64_t>((nrows + CR_WARPS - 1) / CR_WARPS, (int64_t)nsm * 2);
-    log_begin(SGQA_K_TOPK_UNION, st);
-    k_cand_rows<<<(unsigned)cand_ctas, CR_WARPS * 32, cand_smem, st>>>(a);
-    log_end(st);
-    if (cudaGetLastError() != cudaSuccess) return SGQA_ERR_CUDA;
-  }
   log_begin(SGQA_K_TOPK_UNION, st);
   k_topk_rows<<<(unsigned)row_ctas, ROW_WARPS * 32, row_smem, st>>>(a);
   log_end(st);
@@ -1339,7 +1382,7 @@ int launch_topk_union(const Dims& dm, const float* scores, int64_t q_begin, int6
                       uint64_t* union_mask, int64_t union_cap, int32_t* status, cudaStream_t st) {
   return launch_topk_union_layout(dm, scores, q_begin, q_end, sel, union_off, union_len,
                                   union_blk, union_mask, union_cap, 0, dm.ntiles, group_cap(dm),
-                                  status, st, nullptr, nullptr, 0, nullptr, nullptr);
+                                  status, st, nullptr, nullptr);
 }
 
 }  // namespace sgqa
