@@ -324,20 +324,26 @@ __global__ void __launch_bounds__(320, 1)
         const bool ok = mbar_wait(&acc_full[acc], (uint32_t)((k / C::NACC) & 1), ab, status, 105);
         if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int cc = eh * (C::BN / 64); cc < (eh + 1) * (C::BN / 64); ++cc) {
-          uint32_t v[32];
-          tmem_ld32(tl + acc * C::BN + cc * 32, v);
-          tmem_wait_ld();
-          if (cc == (eh + 1) * (C::BN / 64) - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
-          }
-          const int64_t j0 = w.n * C::BN + cc * 32;
+        // both 32-column pieces of this warp's half leave TMEM at once, and
+        // the accumulator is released before they are processed
+        static_assert(C::BN == 128, "two 32-column pieces per epilogue warp");
+        uint32_t va[32], vb[32];
+        tmem_ld32(tl + acc * C::BN + eh * 64, va);
+        tmem_ld32(tl + acc * C::BN + eh * 64 + 32, vb);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (j0 + i >= nh) v[i] = __float_as_uint(ninf);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t(&v)[32] = h == 0 ? va : vb;
+          const int cc = eh * 2 + h;
+          const int64_t j0 = w.n * C::BN + cc * 32;
+          if (j0 + 32 > nh) {  // the row's last tile: blocks past nh are not historical
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (j0 + i >= nh) v[i] = __float_as_uint(ninf);
+          }
           uint32_t fm = 0u;  // this thread's candidates among the 32 columns
           if (filt) {        // (NaN thresholds and -inf scores take nothing)
 #pragma unroll
