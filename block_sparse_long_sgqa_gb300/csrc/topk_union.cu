@@ -482,15 +482,11 @@ struct Sel {
   uint32_t T, rem, cnt, kmin;
   int sh;
 };
-__device__ Sel warp_radix_select(const uint32_t* keys, int stride, uint32_t n, uint32_t need,
-                                 uint32_t* hist, int max_levels) {
+// kmin / kmax: this lane's minimum and maximum of the keys (any split of the
+// keys over the lanes).
+__device__ Sel radix_select_mm(const uint32_t* keys, int stride, uint32_t n, uint32_t need,
+                               uint32_t* hist, int max_levels, uint32_t kmin, uint32_t kmax) {
   const int lane = lane_id();
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-  for (uint32_t i = lane; i < n; i += 32) {
-    const uint32_t k = keys[i * stride];
-    kmin = min(kmin, k);
-    kmax = max(kmax, k);
-  }
   kmin = __reduce_min_sync(FULL, kmin);
   kmax = __reduce_max_sync(FULL, kmax);
   Sel s;
@@ -526,16 +522,27 @@ __device__ Sel warp_radix_select(const uint32_t* keys, int stride, uint32_t n, u
   return s;
 }
 
+__device__ Sel warp_radix_select(const uint32_t* keys, int stride, uint32_t n, uint32_t need,
+                                 uint32_t* hist, int max_levels) {
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  for (uint32_t i = lane_id(); i < n; i += 32) {
+    const uint32_t k = keys[i * stride];
+    kmin = min(kmin, k);
+    kmax = max(kmax, k);
+  }
+  return radix_select_mm(keys, stride, n, need, hist, max_levels, kmin, kmax);
+}
+
 // Threshold key from ns >= 1 sample keys in shared memory: the key ranked at
 // the expected count of the selection in the sample plus nsd standard
 // deviations, rounded down to the prefix the radix select resolved.
 __device__ uint32_t sample_rank_key(const uint32_t* samp, int ns, int64_t nh, uint32_t need,
-                                    uint32_t* hist, float nsd) {
+                                    uint32_t* hist, float nsd, uint32_t kmin, uint32_t kmax) {
   const float e = (float)need * (float)ns / (float)nh;
   uint32_t r = (uint32_t)ceilf(e + nsd * sqrtf(e));
   if (r > (uint32_t)ns) r = ns;
   if (r < 1) r = 1;
-  const Sel sl = warp_radix_select(samp, 1, ns, r, hist, 2);
+  const Sel sl = radix_select_mm(samp, 1, ns, r, hist, 2, kmin, kmax);
   return sl.sh >= 32 ? sl.kmin : (sl.T << sl.sh);
 }
 
@@ -564,7 +571,12 @@ __device__ __noinline__ uint32_t sample_tau(const float* __restrict__ row, int64
     }
   }
   __syncwarp();
-  return sample_rank_key(samp, ns, nh, need, hist, 3.f);
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  for (int i = lane; i < ns; i += 32) {
+    kmin = min(kmin, samp[i]);
+    kmax = max(kmax, samp[i]);
+  }
+  return sample_rank_key(samp, ns, nh, need, hist, 3.f, kmin, kmax);
 }
 
 // Compact every block with score >= tf into cand (key, block), in block order.
@@ -1008,6 +1020,7 @@ __global__ void __launch_bounds__(TAU_WARPS * 32) k_row_tau(const float* __restr
   if (filter_row(nh, need)) {
     const int ns = (int)((nh >> 6) << 3);
     const float4* r4 = reinterpret_cast<const float4*>(ssc + rg * ns_max);
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
     for (int i0 = 0; i0 < ns / 4; i0 += 128) {
       float4 v[4];
 #pragma unroll
@@ -1018,13 +1031,17 @@ __global__ void __launch_bounds__(TAU_WARPS * 32) k_row_tau(const float* __restr
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int i = i0 + u * 32 + lane;
-        if (i < ns / 4)
-          *reinterpret_cast<uint4*>(samp + 4 * i) = make_uint4(
-              order_key(v[u].x), order_key(v[u].y), order_key(v[u].z), order_key(v[u].w));
+        if (i < ns / 4) {
+          const uint4 k4 = make_uint4(order_key(v[u].x), order_key(v[u].y), order_key(v[u].z),
+                                      order_key(v[u].w));
+          *reinterpret_cast<uint4*>(samp + 4 * i) = k4;
+          kmin = min(kmin, min(min(k4.x, k4.y), min(k4.z, k4.w)));
+          kmax = max(kmax, max(max(k4.x, k4.y), max(k4.z, k4.w)));
+        }
       }
     }
     __syncwarp();
-    out = key_to_float(sample_rank_key(samp, ns, nh, (uint32_t)need, hist, TAU_NSD));
+    out = key_to_float(sample_rank_key(samp, ns, nh, (uint32_t)need, hist, TAU_NSD, kmin, kmax));
   }
   if (lane == 0) tau[rg] = out;
 }
@@ -1080,26 +1097,29 @@ __device__ __noinline__ bool cand_row(const TUArgs& a, int64_t r, int64_t nh, ui
   uint32_t* keys = wsm + CR_KEYS;
   uint16_t* idx = reinterpret_cast<uint16_t*>(wsm + CR_IDX);
   const uint2* l0 = a.cand + r * 2 * a.caph;
-  const uint2* l1 = l0 + a.caph;
+  // gather position i of part p reads list entry i + off_p (entries counted
+  // from the row's half-0 list; half 1 follows it)
   const int e0 = f0, e1 = f0 + b0, e2 = e1 + f1;  // ends of the parts in gather order
+  const int o1 = a.caph - b0 - e0, o2 = a.caph - e1, o3 = 2 * a.caph - b1 - e2;
   bool bad = false;
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
   for (int base = 0; base < C; base += 512) {
     uint2 v[16];
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
       const int i = base + u * 32 + lane;
-      const uint2* src = i < e0 ? l0 + i
-                         : i < e1 ? l0 + (a.caph - b0) + (i - e0)
-                         : i < e2 ? l1 + (i - e1)
-                                  : l1 + (a.caph - b1) + (i - e2);
-      v[u] = i < C ? __ldg(src) : make_uint2(0u, 0u);
+      const int off = i < e0 ? 0 : i < e1 ? o1 : i < e2 ? o2 : o3;
+      v[u] = i < C ? __ldg(l0 + (i + off)) : make_uint2(0u, 0u);
     }
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
       const int i = base + u * 32 + lane;
       if (i < C) {
         bad |= v[u].y >= (uint32_t)nh;
-        keys[i] = order_key(__uint_as_float(v[u].x));
+        const uint32_t k = order_key(__uint_as_float(v[u].x));
+        kmin = min(kmin, k);
+        kmax = max(kmax, k);
+        keys[i] = k;
         idx[i] = (uint16_t)v[u].y;
       }
     }
@@ -1113,7 +1133,7 @@ __device__ __noinline__ bool cand_row(const TUArgs& a, int64_t r, int64_t nh, ui
   uint32_t* E = wsm + CR_E;
   for (int w = lane; w < 528; w += 32) A[w] = 0u;
   __syncwarp();
-  const Sel sl = warp_radix_select(keys, 1, (uint32_t)C, need, wsm + CR_HIST, 4);
+  const Sel sl = radix_select_mm(keys, 1, (uint32_t)C, need, wsm + CR_HIST, 4, kmin, kmax);
   const bool ties = sl.cnt != sl.rem;
   if (ties)
     for (int w = lane; w < 528; w += 32) E[w] = 0u;
