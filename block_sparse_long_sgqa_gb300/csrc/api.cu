@@ -206,7 +206,7 @@ struct PrefillWs {
   IndexWs ix;
   AttnWs at;
   bool filt;              // some chunk selects from threshold candidates
-  __nv_bfloat16 *shi, *slo;  // sampled block keys [Hkv][sampled_cols][d]
+  __nv_bfloat16* shi;     // sampled block keys (hi halves) [Hkv][sampled_cols][d]
   float* ssc;             // sampled scores [Hkv][chunk][sampled_cols]
   float* tau;             // thresholds [Hkv][chunk]
   uint2* cand;            // candidates [Hkv][chunk][2][kCandHalf]
@@ -229,7 +229,7 @@ PrefillWs carve_prefill(Carve& c, const Dims& dm) {
   w.ix = carve_index(c, dm, w.chunk);
   w.at = carve_attn(c, dm);
   w.filt = dm.nblk > 0 && chunk_filtered(dm, 0, dm.T);
-  w.shi = w.slo = nullptr;
+  w.shi = nullptr;
   w.ssc = w.tau = nullptr;
   w.cand = nullptr;
   w.ccnt = nullptr;
@@ -237,7 +237,6 @@ PrefillWs carve_prefill(Carve& c, const Dims& dm) {
   if (w.filt) {
     const int64_t ns = sampled_cols(dm), rows = (int64_t)dm.Hkv * w.chunk;
     w.shi = c.take<__nv_bfloat16>((size_t)dm.Hkv * ns * dm.d);
-    w.slo = c.take<__nv_bfloat16>((size_t)dm.Hkv * ns * dm.d);
     w.ssc = c.take<float>((size_t)rows * ns);
     w.tau = c.take<float>((size_t)rows);
     w.cand = c.take<uint2>((size_t)rows * 2 * kCandHalf);
@@ -464,7 +463,7 @@ SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, co
       e = launch_split_kbar(part, Kbar + o, w.ix.khi + o, w.ix.klo + o, st);
     }
   }
-  if (e == cudaSuccess && w.filt) e = launch_sample_keys(dm, w.ix.khi, w.ix.klo, w.shi, w.slo, st);
+  if (e == cudaSuccess && w.filt) e = launch_sample_keys(dm, w.ix.khi, w.ix.klo, w.shi, nullptr, st);
   const __nv_bfloat16 *q, *k, *v;
   if (e == cudaSuccess) e = stage_attn(dm, Q, K, V, page_table, w.at, &q, &k, &v, st);
   if (e != cudaSuccess) return SGQA_ERR_CUDA;
@@ -480,7 +479,7 @@ SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, co
       if (filt) {  // thresholds from the sampled blocks' scores, then candidates
         IndexMode ms{};
         ms.sample = 1;
-        rc = launch_index_scores(dm, w.ix.qhi, w.ix.qlo, w.shi, w.slo, q0, q1, w.ssc, false,
+        rc = launch_index_scores(dm, w.ix.qhi, w.ix.qlo, w.shi, w.shi, q0, q1, w.ssc, false,
                                  status, st, &ms);
         if (rc == SGQA_OK) rc = launch_row_tau(dm, w.ssc, q0, q1, w.tau, st);
         if (rc != SGQA_OK) return rc;

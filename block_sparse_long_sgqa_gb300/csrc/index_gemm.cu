@@ -22,15 +22,20 @@
 // through a 128-byte-swizzled shared staging buffer and TMA, so each tile
 // leaves as full 128-byte rows instead of 16-byte pieces of 32 rows.
 //
-// Two further modes serve the fused prefill.  Sampled mode scores only the
+// Three further modes serve the fused prefill.  Sampled mode scores only the
 // sampled blocks (8 adjacent blocks of every 64, gathered into their own key
-// array beforehand), so a row has (nh / 64) * 8 columns.  Filter mode also
-// compares each score with its row's candidate threshold (derived from the
-// sampled scores) and appends every score at or above it, with its block
-// index, to the row's candidate list: one list per 64-column half of the
+// array beforehand), so a row has (nh / 64) * 8 columns, with the single
+// product hi*hi (the sampled scores only steer a threshold; every selection
+// compares full-precision scores).  Filter mode compares each score with its
+// row's candidate threshold (derived from the sampled scores) and appends
+// every score at or above it, with its block index, to the row's candidate
+// list instead of storing the score row: one list per 64-column half of the
 // tile, and per half a front part (the CTA that starts the row tile, written
 // upwards) and a back part (the CTA that finishes it, written downwards from
-// the end of the list), so no two threads ever share a counter.
+// the end of the list), so no two threads ever share a counter; rows without
+// a threshold are stored in full.  Refill mode scores only listed row tiles
+// (those whose candidates could not decide a row), counting its items on the
+// device.
 #include <algorithm>
 #include <cstring>
 
@@ -221,21 +226,22 @@ __global__ void __launch_bounds__(320, 1)
       for (int64_t k = 0; k < hi - lo; ++k, item_next(a, w)) {
         const int s = (int)(k % C::STAGES);
         if (!mbar_wait(&b_empty[s], (uint32_t)((k / C::STAGES) & 1) ^ 1, ab, status, 101)) break;
-        mbar_expect_tx(&b_full[s], C::STAGE_BYTES);
+        // sampled mode: the hi halves only (one product)
+        mbar_expect_tx(&b_full[s], a.sample ? C::B_BYTES : C::STAGE_BYTES);
         uint8_t* sb = smem + C::OFF_B + s * C::STAGE_BYTES;
         const int32_t brow = (int32_t)(w.g * a.nblk + w.n * C::BN);
         for (int c = 0; c < C::KC; ++c) {
           tma_load_2d(sb + c * C::B_TILE, &mk_hi, &b_full[s], c * 64, brow);
-          tma_load_2d(sb + C::B_BYTES + c * C::B_TILE, &mk_lo, &b_full[s], c * 64, brow);
+          if (!a.sample) tma_load_2d(sb + C::B_BYTES + c * C::B_TILE, &mk_lo, &b_full[s], c * 64, brow);
         }
         ++issued[s];
         if (w.rt != cur_rt || w.g != cur_g) {  // new query operand
           if (a_loads > 0 && !mbar_wait(a_empty, (a_loads - 1) & 1, ab, status, 100)) break;
-          mbar_expect_tx(a_full, 2 * C::A_BYTES);
+          mbar_expect_tx(a_full, a.sample ? C::A_BYTES : 2 * C::A_BYTES);
           const int32_t arow = (int32_t)(w.g * a.nq + w.rt * C::BM);
           for (int c = 0; c < C::KC; ++c) {
             tma_load_2d(smem + C::OFF_AHI + c * C::A_TILE, &mq_hi, a_full, c * 64, arow);
-            tma_load_2d(smem + C::OFF_ALO + c * C::A_TILE, &mq_lo, a_full, c * 64, arow);
+            if (!a.sample) tma_load_2d(smem + C::OFF_ALO + c * C::A_TILE, &mq_lo, a_full, c * 64, arow);
           }
           ++a_loads;
           cur_rt = w.rt;
@@ -281,8 +287,10 @@ __global__ void __launch_bounds__(320, 1)
           const uint64_t bhi = sdesc_sw128(b_hi + boff, 16, 1024);
           const uint64_t blo = sdesc_sw128(b_lo + boff, 16, 1024);
           umma_f16(d_t, ahi, bhi, idesc, kk > 0 ? 1u : 0u);
-          umma_f16(d_t, ahi, blo, idesc, 1u);
-          umma_f16(d_t, alo, bhi, idesc, 1u);
+          if (!a.sample) {
+            umma_f16(d_t, ahi, blo, idesc, 1u);
+            umma_f16(d_t, alo, bhi, idesc, 1u);
+          }
         }
         umma_commit(&b_empty[s]);
         umma_commit(&acc_full[acc]);

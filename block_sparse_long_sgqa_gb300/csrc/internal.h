@@ -84,14 +84,16 @@ __host__ __device__ inline bool filter_row(int64_t nh, int64_t need) {
 // Sampled key rows per group.
 inline int64_t sampled_cols(const Dims& dm) { return (dm.nblk >> 6) << 3; }
 
-// Gather the sampled blocks' hi/lo keys: [Hkv][sampled_cols][d] each.
+// Gather the sampled blocks' hi keys (and lo keys when slo is not null):
+// [Hkv][sampled_cols][d] each.
 cudaError_t launch_sample_keys(const Dims& dm, const __nv_bfloat16* khi, const __nv_bfloat16* klo,
                                __nv_bfloat16* shi, __nv_bfloat16* slo, cudaStream_t st);
 
 // Optional modes of the indexer GEMM (all zero: plain scores).  In filter
 // mode the full score rows are stored only for rows whose threshold is NaN.
 struct IndexMode {
-  int sample;        // khi/klo are the sampled keys; scores [Hkv][nq][sampled_cols]
+  int sample;        // khi holds the sampled keys (klo unread): scores [Hkv][nq][sampled_cols]
+                     // of the single product hi * hi
   const float* tau;  // filter mode: [Hkv][nq] thresholds (NaN: no candidates)
   uint2* cand;       // [Hkv][nq][2][caph] (score bits, block index)
   int32_t* ccnt;     // [Hkv][nq][2][2] front / back counts per half

@@ -201,8 +201,8 @@ __global__ void __launch_bounds__(256) k_kv_pack(const T* __restrict__ X,
 }
 
 // Sampled block keys for the candidate thresholds of the fused prefill: of
-// every 64 blocks of a group, the first 8 (the hi and lo halves, 16 bytes per
-// thread): out[g][s] = in[g][(s / 8) * 64 + s % 8].
+// every 64 blocks of a group, the first 8 (the hi half, and the lo half when
+// slo is given; 16 bytes per thread): out[g][s] = in[g][(s / 8) * 64 + s % 8].
 __global__ void __launch_bounds__(256) k_sample_keys(const uint4* __restrict__ khi,
                                                      const uint4* __restrict__ klo, int64_t nblk,
                                                      int64_t ns, int Hkv, int c16,
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(256) k_sample_keys(const uint4* __restrict__ k
     const int64_t g = r / ns, si = r % ns;
     const int64_t src = (g * nblk + (si >> 3) * 64 + (si & 7)) * c16 + c;
     shi[x] = khi[src];
-    slo[x] = klo[src];
+    if (slo != nullptr) slo[x] = klo[src];
   }
 }
 
