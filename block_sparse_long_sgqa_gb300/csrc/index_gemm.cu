@@ -171,6 +171,7 @@ __global__ void __launch_bounds__(320, 1)
     int64_t tot = 0;
     for (int i = 0; i < a.nfl; ++i) tot += ntiles_of(a, a.flist[i] & 0xfffff);
     a.total = tot;
+    if (tot == 0) return;  // nothing listed: leave before any setup (uniform over the CTA)
   }
   using C = IdxCfg<D>;
   extern __shared__ uint8_t smem_raw[];

@@ -781,7 +781,7 @@ __device__ int64_t tile_slot_base(const TUArgs& a, int g, int64_t tau, int64_t* 
 // for the masks; longer unions use global atomics.  Starts with a barrier.
 __device__ void finish_tile(const TUArgs& a, int g, int64_t tau, int64_t base, int len,
                             uint32_t* tile_bits, uint32_t* wprefix, uint32_t* mspace,
-                            int64_t mask_pairs, const uint16_t* lists = nullptr) {
+                            int64_t mask_pairs) {
   const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
   const int nthr = blockDim.x, nw = nthr >> 5;
   __syncthreads();
@@ -845,7 +845,7 @@ __device__ void finish_tile(const TUArgs& a, int g, int64_t tau, int64_t base, i
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int64_t x = xb + u * 32 + lane;
-        jj[u] = x < need ? (lists ? (int32_t)lists[(int64_t)i * a.Ks + x] : lst[x]) : -1;
+        jj[u] = x < need ? lst[x] : -1;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -929,8 +929,7 @@ __global__ void __launch_bounds__(ROW_WARPS * 32, 4) k_topk_rows(TUArgs a) {
 // bitmask and writes the union and the member masks.
 constexpr int UNION_THREADS = 256;
 
-__global__ void __launch_bounds__(UNION_THREADS) k_tile_union(TUArgs a, int64_t mask_pairs,
-                                                              int cache_lists) {
+__global__ void __launch_bounds__(UNION_THREADS) k_tile_union(TUArgs a, int64_t mask_pairs) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int g = blockIdx.y;
   const int64_t tau = a.tau_begin + blockIdx.x;
@@ -939,7 +938,6 @@ __global__ void __launch_bounds__(UNION_THREADS) k_tile_union(TUArgs a, int64_t 
   uint32_t* tile_bits = reinterpret_cast<uint32_t*>(smem);
   uint32_t* wprefix = tile_bits + ((a.nwords + 3) & ~3);          // nwords + 1 entries
   uint32_t* mspace = wprefix + ((a.nwords + 1 + 3) & ~3);         // mask_pairs lo/hi pairs
-  uint16_t* lists = cache_lists ? reinterpret_cast<uint16_t*>(mspace + 2 * mask_pairs) : nullptr;
   __shared__ int64_t s_red[32];
 
   for (int i = tid; i < a.nwords; i += UNION_THREADS) tile_bits[i] = 0;
@@ -952,29 +950,12 @@ __global__ void __launch_bounds__(UNION_THREADS) k_tile_union(TUArgs a, int64_t 
     if (nh > a.nblk) nh = a.nblk;
     const int need = (int)(nh < a.Ks ? nh : a.Ks);
     const int32_t* lst = a.sel + ((int64_t)g * a.nq + (t - a.q_begin)) * a.Ks;
-    uint16_t* my = lists ? lists + (int64_t)i * a.Ks : nullptr;
-    if (my) {  // one coalesced read of the list into shared memory
-      for (int xb = 0; xb < need; xb += 32 * 8) {
-        int32_t jj[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int x = xb + u * 32 + lane;
-          jj[u] = x < need ? lst[x] : 0;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int x = xb + u * 32 + lane;
-          if (x < need) my[x] = (uint16_t)jj[u];
-        }
-      }
-      __syncwarp();
-    }
     // each lane ORs a contiguous piece of the ascending list, one atomic per word run
     const int per = (need + 31) / 32;
     const int xa = lane * per, x1 = min(need, xa + per);
     uint32_t word = 0xffffffffu, bits = 0;
     for (int x = xa; x < x1; ++x) {
-      const int32_t j = my ? (int32_t)my[x] : lst[x];
+      const int32_t j = lst[x];
       if ((uint32_t)(j >> 5) != word) {
         if (bits) atomicOr(&tile_bits[word], bits);
         word = (uint32_t)(j >> 5);
@@ -984,7 +965,7 @@ __global__ void __launch_bounds__(UNION_THREADS) k_tile_union(TUArgs a, int64_t 
     }
     if (bits) atomicOr(&tile_bits[word], bits);
   }
-  finish_tile(a, g, tau, base, len, tile_bits, wprefix, mspace, mask_pairs, lists);
+  finish_tile(a, g, tau, base, len, tile_bits, wprefix, mspace, mask_pairs);
 }
 
 }  // namespace
@@ -1374,13 +1355,11 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
   const size_t budget = 200 * 1024;
   if (fixed + 1024 > budget) return SGQA_ERR_UNSUPPORTED;
   const int64_t u_max = std::min<int64_t>((int64_t)dm.W * dm.Ks, dm.nblk);  // slots of a tile
-  // the tile's lists as 16-bit block indices when they fit, so they are read once
-  const size_t list_bytes = ((size_t)dm.W * dm.Ks * 2 + 15) & ~(size_t)15;
-  const int cache_lists = (dm.nblk <= 65536 && list_bytes + fixed + 8 * 1024 <= budget) ? 1 : 0;
-  const size_t mask_budget = budget - fixed - (cache_lists ? list_bytes : 0);
+  // (the lists are read twice, from L2; a small footprint keeps many CTAs per SM)
+  const size_t mask_budget = budget - fixed;
   const int64_t mask_pairs =
       std::min<int64_t>(std::min<int64_t>(u_max, 4096), (int64_t)(mask_budget / 8));
-  const size_t union_smem = fixed + (size_t)mask_pairs * 8 + (cache_lists ? list_bytes : 0);
+  const size_t union_smem = fixed + (size_t)mask_pairs * 8;
   if (cudaFuncSetAttribute(k_topk_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)row_smem) != cudaSuccess ||
       cudaFuncSetAttribute(k_tile_union, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1392,7 +1371,7 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
   if (cudaGetLastError() != cudaSuccess) return SGQA_ERR_CUDA;
   log_begin(SGQA_K_TILE_UNION, st);
   k_tile_union<<<dim3((unsigned)(tau_end - a.tau_begin), (unsigned)dm.Hkv), UNION_THREADS,
-                 union_smem, st>>>(a, mask_pairs, cache_lists);
+                 union_smem, st>>>(a, mask_pairs);
   log_end(st);
   return cudaGetLastError() == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA;
 }
