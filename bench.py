@@ -51,6 +51,8 @@ def parse_args(argv=None):
                     help="AR(1) correlation of the query noise (0 = i.i.d. stress case)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-quality", action="store_true",
+                    help="skip the union / recall / coverage report (computed after timing)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--seq", type=int, default=None,
                     help="shrink the workload to this many queries (profiling small cases)")
@@ -297,6 +299,72 @@ def run_reference(args, wl, rank):
     return line
 
 
+def quality(wl, inp, Q, K, V, pt, Kbar, lse, dev, nq_max=1024):
+    """Selection quality on the last nq_max queries (a whole number of tiles),
+    through the C ABI and outside the timed region:
+      union inflation |U| / min(k/B, nh) per (tile, group) of the standalone
+      selection; needle recall (planted blocks found in each query's own
+      selection); attention-mass coverage exp(lse_sparse - lse_dense) per
+      (query, head), lse_sparse from the timed prefill and lse_dense from the
+      same prefill with k covering every historical block."""
+    import torch
+
+    from block_sparse_long_sgqa_gb300 import sgqa
+
+    W, B = wl.tile_q, wl.block_size
+    nq = min(nq_max, wl.seq_q) // W * W
+    if nq == 0:
+        return None
+    q0 = wl.seq_q - nq
+    sub = wl.replace(seq_q=nq, q_offset=wl.q_offset + q0)
+    ps = sgqa.params_for(sub)
+    Qs = Q[q0:].contiguous()
+    nblk = wl.seq_kv // B
+    Ks = wl.topk_tokens // B
+    scores = torch.empty(wl.n_kv_heads, nq, nblk, device=dev)
+    sgqa.sgqa_index_scores(ps, Qs, Kbar, 0, nq, scores,
+                           sgqa.alloc_workspace(ps, sgqa.WS_INDEX_SCORES, dev))
+    sel = torch.empty(wl.n_kv_heads, nq, Ks, dtype=torch.int32, device=dev)
+    uo, ul, ub, um = sgqa.alloc_union(ps, dev)
+    st = sgqa.new_status(dev)
+    sgqa.sgqa_topk_union(ps, scores, 0, nq, sel, uo, ul, ub, um, status=st)
+    del scores
+    t = np.arange(q0, wl.seq_q)
+    nh = np.minimum((wl.q_offset + t) // B, nblk)
+    tiles = np.arange(nq // W)
+    kcap = np.minimum(Ks, nh[tiles * W + W - 1])  # the tile's last query has the most blocks
+    infl = (ul.cpu().numpy().reshape(wl.n_kv_heads, -1)[:, :len(tiles)] / np.maximum(kcap, 1))
+    out = {"queries": f"last {nq}", "union_inflation_mean": float(infl.mean()),
+           "union_inflation_p99": float(np.percentile(infl, 99))}
+    if "needles" in inp:
+        seln = sel.cpu().numpy()
+        nd = inp["needles"]
+        found = total = 0
+        for i in range(nq):
+            tau = (q0 + i) // W
+            for g in range(wl.n_kv_heads):
+                js = nd[tau, g][nd[tau, g] >= 0]
+                js = js[js < nh[i]]
+                total += len(js)
+                found += int(np.isin(js, seln[g, i]).sum())
+        out["needle_recall"] = found / total if total else None
+    del sel
+    # dense reference: every historical block selected
+    dense = sub.replace(topk_tokens=nblk * B)
+    pd = sgqa.params_for(dense)
+    Od, lsed = sgqa.alloc_outputs(pd, dev)
+    Kb = sgqa.kbar_empty(pd, dev)
+    sgqa.sgqa_prefill(pd, Qs, K, V, Kb, Od, lsed, sgqa.alloc_workspace(pd, sgqa.WS_PREFILL, dev),
+                      page_table=pt, status=st)
+    code, det = sgqa.read_status(st)
+    if code != 0:
+        raise RuntimeError(f"device status in the quality report: {sgqa.status_string(code)} ({det})")
+    cov = torch.exp(lse[:, q0:].double() - lsed.double()).cpu().numpy()
+    out["coverage_mean"] = float(cov.mean())
+    out["coverage_p1"] = float(np.percentile(cov, 1))
+    return out
+
+
 def config_of(wl, args):
     return {"workload": wl.name, "seq_q": wl.seq_q, "seq_kv": wl.seq_kv, "q_offset": wl.q_offset,
             "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
@@ -480,6 +548,11 @@ def main(argv=None):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms}
 
+    # ---------------- selection quality (rank 0, after timing)
+    qual = None
+    if rank == 0 and not args.no_quality:
+        qual = quality(wl, inp, Q, K, V, pt, Kbar, lse, dev)
+
     # ---------------- CPU baseline (rank 0, single GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -494,7 +567,8 @@ def main(argv=None):
                 "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
                 "data": "synthetic", "config": config_of(wl, args), "clocks": clocks,
                 "e2e": e2e, "gpu_launches": n_launch, "roofline": roofline,
-                "step_roofline": step_roof, "kernels": kernels, "cpu_baseline": cpu,
+                "step_roofline": step_roof, "kernels": kernels, "quality": qual,
+                "cpu_baseline": cpu,
                 "input_gen_s": round(t_gen, 2)}
         print(json.dumps(line), flush=True)
     return 0
