@@ -66,6 +66,7 @@ struct TUArgs {
   int32_t* tflag;       // [Hkv][ceil(nq / 128)]: row tile has a row the candidates left
   int32_t* flist;       // flagged row tiles, (g << 20) | rt
   int32_t* nflist;      // their count
+  int rb;               // row-select warps take blocks of rb consecutive queries
   int32_t* status;
 };
 
@@ -871,11 +872,12 @@ __device__ void finish_tile(const TUArgs& a, int g, int64_t tau, int64_t base, i
   }
 }
 
-// Row kernel: the rows of every group are cut into blocks of 8 consecutive
-// queries; warp w of the grid takes blocks w, w + (warps in the grid), ...
-// (persistent CTAs, so all SMs stay busy however many tiles there are), and
-// carries its threshold predictor from row to row within a block.
-constexpr int ROW_BLOCK = 8;
+// Row kernel: the rows of every group are cut into blocks of rb consecutive
+// queries (8 where the one-pass candidate path applies, else 1); warp w of
+// the grid takes blocks w, w + (warps in the grid), ... (persistent CTAs, so
+// all SMs stay busy however many tiles there are), and carries its threshold
+// predictor from row to row within a block.
+constexpr int ROW_BLOCK = 8;  // when the previous-row threshold can serve (else 1)
 
 // Bulk prefetch into L2 of the scores of local row r of group g (the blocks
 // the select reads, rounded up to 16 bytes; rows start 16-byte aligned when
@@ -909,11 +911,11 @@ __global__ void __launch_bounds__(ROW_WARPS * 32, 4) k_topk_rows(TUArgs a) {
     }
     return;
   }
-  const int64_t bpg = (a.nq + ROW_BLOCK - 1) / ROW_BLOCK;  // row blocks per group
+  const int64_t bpg = (a.nq + a.rb - 1) / a.rb;  // row blocks per group
   for (int64_t b = (int64_t)blockIdx.x * ROW_WARPS + warp; b < bpg * a.Hkv; b += nwt) {
     const int g = (int)(b / bpg);
-    const int64_t r0 = (b % bpg) * ROW_BLOCK;
-    const int64_t r1 = r0 + ROW_BLOCK < a.nq ? r0 + ROW_BLOCK : a.nq;
+    const int64_t r0 = (b % bpg) * a.rb;
+    const int64_t r1 = r0 + a.rb < a.nq ? r0 + a.rb : a.nq;
     Pred pr;
     pr.valid = false;
     if (lane_id() == 0) prefetch_row_l2(a, g, r0);
@@ -1346,7 +1348,14 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
     return SGQA_ERR_CUDA;
-  const int64_t row_blocks = (a.nq + ROW_BLOCK - 1) / ROW_BLOCK * dm.Hkv;
+  // blocks of 8 consecutive rows only where the one-pass candidate path (and
+  // its previous-row threshold) can apply; longer rows go one per warp so
+  // that many rows stream at once
+  {
+    const int64_t nh_lo = nh_of(dm, q_begin), nh_hi = nh_of(dm, q_end - 1);
+    a.rb = (dm.Ks <= CAND_NEED_MAX && nh_hi >= 2048 && nh_lo <= 16384) ? ROW_BLOCK : 1;
+  }
+  const int64_t row_blocks = (a.nq + a.rb - 1) / a.rb * dm.Hkv;
   const int64_t row_ctas =
       std::min<int64_t>((row_blocks + ROW_WARPS - 1) / ROW_WARPS, (int64_t)nsm * 4);
   const size_t row_smem = (size_t)ROW_WARPS * WARP_BYTES;
