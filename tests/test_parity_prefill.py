@@ -191,12 +191,17 @@ def periodic_keys(inp, period):
     return dict(inp, K=np.ascontiguousarray(K[(pos // 8 % period) * 8 + pos % 8]))
 
 
-@pytest.mark.parametrize("case", ["clustered", "period61", "period2", "gqa_32k"])
+@pytest.mark.parametrize("case", ["clustered", "period61", "period2", "gqa_32k", "long"])
 def test_prefill_candidates_equal_full_select(s, case):
     """The fused prefill selects rows of 2048 .. 16384 blocks from threshold
     candidates; those lists must be the ones the full score rows give, so the
-    fused output equals the step-by-step composition bit for bit."""
-    wl = synth.WORKLOADS["gqa_32k"] if case == "gqa_32k" else FILT
+    fused output equals the step-by-step composition bit for bit.  "gqa_32k"
+    has rows on both sides of 2048 blocks in one chunk; "long" is the last
+    4096 queries of the 128K workload (rows of 15872 .. 16383 blocks)."""
+    if case == "long":
+        wl = synth.WORKLOADS["step5_128k"].replace(name="long", seq_q=4096, q_offset=131072 - 4096)
+    else:
+        wl = synth.WORKLOADS["gqa_32k"] if case == "gqa_32k" else FILT
     inp = synth.make_inputs(wl)
     if case.startswith("period"):
         inp = periodic_keys(inp, int(case[6:]))
@@ -206,3 +211,20 @@ def test_prefill_candidates_equal_full_select(s, case):
     O2, lse2 = composition(s, p, d, Kbar)
     assert torch.equal(O, O2)
     assert torch.equal(lse, lse2)
+
+
+@pytest.mark.parametrize("case", ["b8", "filt", "mixed"])
+def test_prefill_plan_counts_launches(s, case):
+    """sgqa_prefill_plan's launch count is the number of kernels the call
+    enqueues: chunks without candidates (b8), with them (filt), and both in
+    one call (the 128K shapes at 32K tokens: two chunks of 16384 queries,
+    the first with rows under 2048 blocks)."""
+    mixed = synth.WORKLOADS["step5_128k"].replace(name="mixed", seq_q=32768, seq_kv=32768)
+    wl = {"b8": SMALL["b8"], "filt": FILT, "mixed": mixed}[case]
+    p = s.params_for(wl)
+    _, planned = s.sgqa_prefill_plan(p)
+    d = dev_inputs(synth.make_inputs(wl))
+    log = s.launch_log(planned + 64)
+    with log:
+        run_prefill(s, p, d)
+    assert log.count == planned
