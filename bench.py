@@ -56,6 +56,10 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--seq", type=int, default=None,
                     help="shrink the workload to this many queries (profiling small cases)")
+    ap.add_argument("--tile-q", type=int, default=None,
+                    help="union tile size (queries) instead of the workload's")
+    ap.add_argument("--union-mode", choices=["masked", "full"], default="masked",
+                    help="masked: each query attends its own selection; full: the tile's union")
     return ap.parse_args(argv)
 
 
@@ -278,6 +282,9 @@ def run_reference(args, wl, rank):
 
     if rank != 0:
         return None
+    if args.union_mode != "masked":
+        return {"impl": "reference",
+                "unavailable": "the oracle sample times the masked union mode only"}
     inp = synth.make_inputs(wl, rho_q=args.rho_q)
     cores = len(os.sched_getaffinity(0))
     vals, desc = [], ""
@@ -369,7 +376,7 @@ def config_of(wl, args):
     return {"workload": wl.name, "seq_q": wl.seq_q, "seq_kv": wl.seq_kv, "q_offset": wl.q_offset,
             "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
             "block_size": wl.block_size, "topk_tokens": wl.topk_tokens, "tile_q": wl.tile_q,
-            "page_size": wl.page_size, "union_mode": "masked",
+            "page_size": wl.page_size, "union_mode": args.union_mode,
             "inputs": f"seeded {wl.dist}" + (f", AR(1) query noise rho={wl.rho_q if args.rho_q is None else args.rho_q}"
                                               if wl.dist == "clustered" else "")
                       + (f", {wl.needles} needle blocks per tile" if wl.needles else ""),
@@ -385,6 +392,8 @@ def main(argv=None):
     wl = synth.WORKLOADS[args.workload]
     if args.seq:
         wl = wl.replace(seq_q=args.seq, seq_kv=wl.q_offset + args.seq)
+    if args.tile_q:
+        wl = wl.replace(tile_q=args.tile_q)
     if args.impl == "reference":
         line = run_reference(args, wl, rank)
         if line is not None:
@@ -398,7 +407,7 @@ def main(argv=None):
     torch.cuda.set_device(local)
     dist_init(world, "nccl")
     dev = torch.device("cuda", local)
-    p = sgqa.params_for(wl)
+    p = sgqa.params_for(wl, union_mode=1 if args.union_mode == "full" else 0)
     chunk, launches = sgqa.sgqa_prefill_plan(p)
 
     t_gen = time.perf_counter()
@@ -555,7 +564,7 @@ def main(argv=None):
 
     # ---------------- CPU baseline (rank 0, single GPU only)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
+    if rank == 0 and world == 1 and not args.no_cpu and args.union_mode == "masked":
         v, desc, _ = oracle_sample(wl, inp, args.cpu_seconds)
         cpu = {"value": v, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
                "sample": desc}
