@@ -12,7 +12,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsgqa.so")
-SOURCES = ["api.cu", "merge.cu", "index_gemm.cu", "topk_union.cu", "attn.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "merge.cu", "index_gemm.cu", "topk_union.cu", "select_long.cu", "attn.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 

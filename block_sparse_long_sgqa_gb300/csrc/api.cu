@@ -525,18 +525,19 @@ SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int
   if (launches) {
     // with an empty block-key cache: merge, operand staging (fp32 rounding,
     // K/V block packing), then per chunk the index query and indexer GEMM
-    // (when there are blocks), top-k rows, tile union and attention
-    // (plus, where some rows select from threshold candidates, the sampled-key
-    // gather once and per such chunk the sampled-block GEMM, the thresholds,
-    // the candidate select and the refill GEMM of the row tiles it left)
-    const int64_t nchunks = (dm.T + chunk - 1) / chunk;
+    // (when there are blocks), the row selects (a CTA-per-row launch too when
+    // the chunk has rows of more than 16384 blocks), tile union and attention;
+    // where some rows select from threshold candidates, the sampled-key gather
+    // once and per such chunk the sampled-block GEMM, the thresholds, the
+    // candidate select and the refill GEMM of the row tiles it left (the rows
+    // it leaves then all go through the warp-per-row select)
+    const bool any_filt = dm.nblk > 0 && chunk_filtered(dm, 0, dm.T);
     int64_t n = (dm.nblk > 0 ? 1 : 0) + (dm.dtype == SGQA_FP32 ? (dm.B >= 8 ? 1 : 3) : 0) +
-                (dm.B >= 8 ? 2 : 0);
-    n += nchunks * ((dm.nblk > 0 ? 2 : 0) + topk_union_launches(dm) + 1);
-    if (dm.nblk > 0 && chunk_filtered(dm, 0, dm.T)) {
-      n += 1;
-      for (int64_t q0 = 0; q0 < dm.T; q0 += chunk)
-        if (chunk_filtered(dm, q0, std::min<int64_t>(dm.T, q0 + chunk))) n += 4;
+                (dm.B >= 8 ? 2 : 0) + (any_filt ? 1 : 0);
+    for (int64_t q0 = 0; q0 < dm.T; q0 += chunk) {
+      const int64_t q1 = std::min<int64_t>(dm.T, q0 + chunk);
+      const bool filt = any_filt && chunk_filtered(dm, q0, q1);
+      n += (dm.nblk > 0 ? 2 : 0) + 1 + (filt ? 4 + 2 : topk_union_launches(dm, q0, q1));
     }
     *launches = (int32_t)n;
   }

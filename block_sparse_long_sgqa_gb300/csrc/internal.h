@@ -128,9 +128,18 @@ int launch_cand_rows(const Dims& dm, int64_t q_begin, int64_t q_end, int32_t* se
 int launch_row_tau(const Dims& dm, const float* sample_scores, int64_t q_begin, int64_t q_end,
                    float* tau, cudaStream_t st);
 
+// Rows of more than kFiltMaxNh blocks (that do not take every block) are
+// selected one CTA per row: local rows [long_rows_first(..), q_end - q_begin)
+// of each group, by launch_select_long (scores and sel laid out as for
+// launch_topk_union).
+int64_t long_rows_first(const Dims& dm, int64_t q_begin, int64_t q_end);
+int launch_select_long(const Dims& dm, const float* scores, int64_t q_begin, int64_t q_end,
+                       int64_t r_first, int32_t* sel, int32_t* status, cudaStream_t st);
+
 size_t topk_union_ws_bytes(const Dims& dm, int64_t nq);
-// Kernel launches of one top-k/union call (aligned score buffers).
-int topk_union_launches(const Dims& dm);
+// Kernel launches of one top-k/union call over [q_begin, q_end) (without the
+// candidate path).
+int topk_union_launches(const Dims& dm, int64_t q_begin, int64_t q_end);
 int launch_topk_union(const Dims& dm, const float* scores, int64_t q_begin, int64_t q_end,
                       int32_t* sel, int64_t* union_off, int32_t* union_len, int32_t* union_blk,
                       uint64_t* union_mask, int64_t union_cap, int32_t* status, cudaStream_t st);

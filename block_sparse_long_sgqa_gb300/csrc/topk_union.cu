@@ -67,6 +67,7 @@ struct TUArgs {
   int32_t* flist;       // flagged row tiles, (g << 20) | rt
   int32_t* nflist;      // their count
   int rb;               // row-select warps take blocks of rb consecutive queries
+  int64_t r_end;        // the warp path selects local rows [0, r_end) (longer rows: one CTA each)
   int32_t* status;
 };
 
@@ -911,11 +912,11 @@ __global__ void __launch_bounds__(ROW_WARPS * 32, 4) k_topk_rows(TUArgs a) {
     }
     return;
   }
-  const int64_t bpg = (a.nq + a.rb - 1) / a.rb;  // row blocks per group
+  const int64_t bpg = (a.r_end + a.rb - 1) / a.rb;  // row blocks per group
   for (int64_t b = (int64_t)blockIdx.x * ROW_WARPS + warp; b < bpg * a.Hkv; b += nwt) {
     const int g = (int)(b / bpg);
     const int64_t r0 = (b % bpg) * a.rb;
-    const int64_t r1 = r0 + a.rb < a.nq ? r0 + a.rb : a.nq;
+    const int64_t r1 = r0 + a.rb < a.r_end ? r0 + a.rb : a.r_end;
     Pred pr;
     pr.valid = false;
     if (lane_id() == 0) prefetch_row_l2(a, g, r0);
@@ -1228,7 +1229,9 @@ __global__ void __launch_bounds__(CR_WARPS * 32, 2) k_cand_rows(TUArgs a) {
 
 }  // namespace
 
-int topk_union_launches(const Dims&) { return 2; }
+int topk_union_launches(const Dims& dm, int64_t q_begin, int64_t q_end) {
+  return 2 + (long_rows_first(dm, q_begin, q_end) < q_end - q_begin ? 1 : 0);
+}
 
 int launch_cand_rows(const Dims& dm, int64_t q_begin, int64_t q_end, int32_t* sel,
                      const uint2* cand, const int32_t* ccnt, int caph, int32_t* rest,
@@ -1355,7 +1358,8 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
     const int64_t nh_lo = nh_of(dm, q_begin), nh_hi = nh_of(dm, q_end - 1);
     a.rb = (dm.Ks <= CAND_NEED_MAX && nh_hi >= 2048 && nh_lo <= 16384) ? ROW_BLOCK : 1;
   }
-  const int64_t row_blocks = (a.nq + a.rb - 1) / a.rb * dm.Hkv;
+  a.r_end = rest == nullptr ? long_rows_first(dm, q_begin, q_end) : a.nq;
+  const int64_t row_blocks = std::max<int64_t>(1, (a.r_end + a.rb - 1) / a.rb * dm.Hkv);
   const int64_t row_ctas =
       std::min<int64_t>((row_blocks + ROW_WARPS - 1) / ROW_WARPS, (int64_t)nsm * 4);
   const size_t row_smem = (size_t)ROW_WARPS * WARP_BYTES;
@@ -1378,6 +1382,10 @@ int launch_topk_union_layout(const Dims& dm, const float* scores, int64_t q_begi
   k_topk_rows<<<(unsigned)row_ctas, ROW_WARPS * 32, row_smem, st>>>(a);
   log_end(st);
   if (cudaGetLastError() != cudaSuccess) return SGQA_ERR_CUDA;
+  if (a.r_end < a.nq) {  // the long rows, one CTA each
+    const int rc = launch_select_long(dm, scores, q_begin, q_end, a.r_end, sel, status, st);
+    if (rc != SGQA_OK) return rc;
+  }
   log_begin(SGQA_K_TILE_UNION, st);
   k_tile_union<<<dim3((unsigned)(tau_end - a.tau_begin), (unsigned)dm.Hkv), UNION_THREADS,
                  union_smem, st>>>(a, mask_pairs);

@@ -218,6 +218,39 @@ def test_topk_union_long_rows(s, case, Ks, kv_extra):
     assert _gpu_union_lists(s, p, uo, ul, ub, um) == _oracle_union_lists(*ref_u)
 
 
+@pytest.mark.parametrize("case", ["clustered", "clustered_ties", "iid", "all_equal"])
+@pytest.mark.parametrize("Ks", [37, 512, 2048])
+def test_topk_union_cta_rows(s, case, Ks):
+    """Rows of more than 16384 blocks (25000-25016 here) take the CTA-per-row
+    select; bit-exact against the oracle.  "all_equal" puts every key in one
+    bucket, too many for shared memory, so each digit level passes over the
+    row again and the lowest indices win the tie."""
+    T, B, off, Hkv, W = 128, 8, 200000, 2, 64
+    wl = synth.Workload("cta", T, off + T, off, 8, Hkv, 128, B, Ks * B, W, "bf16", "normal")
+    p = s.params_for(wl)
+    nb = wl.n_blocks
+    rng = np.random.default_rng(12)
+    level = np.repeat(rng.normal(0.0, 1.0, (Hkv, 1, nb // 64 + 1)), 64, axis=2)[:, :, :nb]
+    S = level + 0.3 * rng.normal(0.0, 1.0, (Hkv, T, nb))
+    if case == "clustered_ties":
+        S = np.round(S * 8.0) / 8.0
+    elif case == "iid":
+        S = rng.normal(0.0, 1.0, (Hkv, T, nb))
+    elif case == "all_equal":
+        S = np.full((Hkv, T, nb), 0.5)
+    S32 = np.ascontiguousarray(S, np.float32)
+    rows = np.arange(T)
+    ref_sel = oracle.select(S32, B, off, rows, Ks)
+    ref_u = oracle.union(ref_sel, W, nb)
+    sel = torch.empty(Hkv, T, Ks, dtype=torch.int32, device="cuda")
+    uo, ul, ub, um = s.alloc_union(p)
+    st = s.new_status()
+    s.sgqa_topk_union(p, torch.from_numpy(S32).cuda(), 0, T, sel, uo, ul, ub, um, status=st)
+    assert s.read_status(st)[0] == 0
+    assert np.array_equal(sel.cpu().numpy(), ref_sel)
+    assert _gpu_union_lists(s, p, uo, ul, ub, um) == _oracle_union_lists(*ref_u)
+
+
 @pytest.mark.parametrize("name", list(SMALL))
 @pytest.mark.parametrize("mode", [0, 1])
 def test_sparse_attn_given_lists(s, name, mode):
