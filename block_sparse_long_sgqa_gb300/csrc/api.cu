@@ -61,9 +61,7 @@ int derive(const sgqa_params* p, Dims* dm) {
   if (p->head_dim != 64 && p->head_dim != 128) return SGQA_ERR_UNSUPPORTED;
   if (p->tile_q > 64) return SGQA_ERR_UNSUPPORTED;
   if (p->n_q_heads / p->n_kv_heads > 128) return SGQA_ERR_UNSUPPORTED;
-  if (p->page_size > 0 &&
-      (p->page_size % B || p->page_size % 8 || p->seq_kv % p->page_size))
-    return SGQA_ERR_UNSUPPORTED;
+  if (p->page_size > 0 && (p->page_size % B || p->page_size % 8)) return SGQA_ERR_UNSUPPORTED;
   dm->T = p->seq_q;
   dm->Tkv = p->seq_kv;
   dm->off = p->q_offset;

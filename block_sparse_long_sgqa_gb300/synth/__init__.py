@@ -231,7 +231,7 @@ def make_inputs(wl: Workload, rho_q: Optional[float] = None) -> dict:
     out.update(Q=Q, K=K, V=V)
 
     if wl.page_size:
-        npages = Tkv // wl.page_size
+        npages = -(-Tkv // wl.page_size)  # a partial last page counts
         u = uniform(seed, STREAM_PAGES, npages)
         out["page_table"] = np.argsort(u, kind="stable").astype(np.int32)
     return out
@@ -240,9 +240,11 @@ def make_inputs(wl: Workload, rho_q: Optional[float] = None) -> dict:
 def to_paged(x: np.ndarray, page_table: np.ndarray, page_size: int) -> np.ndarray:
     """Lay a logical [Tkv][Hkv][d] tensor out as physical pages
     [npages][Hkv][page_size][d]: logical page i lives at physical page
-    page_table[i]."""
+    page_table[i]; a partial last page is padded with zeros."""
     Tkv, Hkv, d = x.shape
-    npages = Tkv // page_size
+    npages = -(-Tkv // page_size)
+    if npages * page_size != Tkv:
+        x = np.concatenate([x, np.zeros((npages * page_size - Tkv, Hkv, d), x.dtype)])
     logical = x.reshape(npages, page_size, Hkv, d).transpose(0, 2, 1, 3)
     phys = np.empty_like(logical)
     phys[page_table] = logical

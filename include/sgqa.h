@@ -41,8 +41,9 @@
  *     historical blocks and keeps Ks(t) = min(topk_tokens / B, nh(t)).
  *   - Layouts (row-major, innermost last): Q and O [seq_q][n_q_heads][head_dim];
  *     contiguous K and V [seq_kv][n_kv_heads][head_dim]; paged K and V
- *     [n_pages][n_kv_heads][page_size][head_dim] with page_table[seq_kv /
- *     page_size] mapping logical page i to its physical page; block keys
+ *     [n_pages][n_kv_heads][page_size][head_dim] with page_table[ceil(seq_kv /
+ *     page_size)] mapping logical page i to its physical page (the last page
+ *     may be partly filled: positions from seq_kv on are never read); block keys
  *     Kbar [n_kv_heads][nblk][head_dim] fp32; scores
  *     [n_kv_heads][q_end - q_begin][nblk] fp32; lse [n_q_heads][seq_q] fp32
  *     (natural log).

@@ -228,3 +228,22 @@ def test_prefill_plan_counts_launches(s, case):
     with log:
         run_prefill(s, p, d)
     assert log.count == planned
+
+
+@pytest.mark.parametrize("pos", [20000, 150001])
+def test_decode_step_paged(s, pos):
+    """A decode step: one query at a position that ends mid-page, over a paged
+    cache (64-token pages, the 1M workload's heads) whose earlier blocks' keys
+    are cached; against the oracle.  At 20000 the row selects from threshold
+    candidates, at 150001 (18750 blocks) it takes the CTA-per-row select."""
+    wl = synth.WORKLOADS["chunk_1m"].replace(name="decode", seq_q=1, q_offset=pos, seq_kv=pos + 1)
+    inp = synth.make_inputs(wl)
+    p = s.params_for(wl)
+    d = dev_inputs(inp)
+    kvalid = pos // wl.block_size  # blocks complete before this token
+    Kbar = s.kbar_empty(p)
+    s.sgqa_block_merge(p, d["K"], Kbar, 0, kvalid, page_table=d["page_table"])
+    O, lse, Kbar = run_prefill(s, p, d, kbar=Kbar, kvalid=kvalid)
+    rows = np.arange(1, dtype=np.int32)
+    _, frac = check_end_to_end(s, wl, inp, O, lse, rows, Kbar, d)
+    assert frac == 1.0
