@@ -9,13 +9,17 @@
 // Rows of more than 16384 blocks (1M-token caches, small block sizes) are
 // too long for one warp to stream quickly, so here a 512-thread CTA takes a
 // row: an 11-bit histogram of the top key bits finds the bucket holding the
-// k-th largest key; the bucket's members are compacted into shared memory
-// (a bucket too large for that is histogrammed again, one digit lower, over
-// the row), and 11-bit radix levels among them resolve the k-th key exactly.
-// A last pass over the row in block order writes every block above that key
-// and, of the blocks equal to it, the lowest-indexed ones: each thread takes
-// four consecutive blocks per step and one CTA-wide prefix sum per step
-// (blocks above, blocks equal) gives every taken block its list position.
+// k-th largest key.  When the keys at or above that bucket fit in shared
+// memory (k/B plus the bucket, up to 6144) the second pass keeps them with
+// their blocks, 11-bit radix levels among the bucket's resolve the k-th key
+// exactly, and the taken blocks (above it, and of those equal to it the
+// lowest-indexed) are marked in a bitmap over the row read out in block order
+// by a CTA prefix sum: two passes over the row.  Otherwise the bucket's keys
+// alone are compacted (or, for a bucket too large, the row is histogrammed
+// again one digit lower), and a third pass over the row in block order writes
+// every block above the k-th key and the lowest-indexed ones equal to it:
+// each thread takes four consecutive blocks per step and one CTA-wide prefix
+// sum per step (blocks above, blocks equal) gives every block its place.
 #include "common.cuh"
 #include "internal.h"
 
@@ -26,6 +30,8 @@ constexpr int SL_THREADS = 512;
 constexpr int SL_WARPS = SL_THREADS / 32;
 constexpr int SL_BINS = 2048;  // 11-bit digits
 constexpr int SL_CAP = 4096;   // bucket members resolved in shared memory
+constexpr int SL_CAP2 = 6144;  // keys at or above the bucket kept with their blocks
+constexpr int SL_BMAX = 131072;  // longest row the bitmap emission covers
 
 struct SLArgs {
   const float* scores;  // [Hkv][nq][nblk]
@@ -38,11 +44,36 @@ struct SLArgs {
 
 struct SLShared {
   uint32_t hist[SL_BINS];
-  uint32_t ckey[SL_CAP];  // the bucket's keys (the final pass reads the row again)
+  uint32_t ckey[SL_CAP2];  // compacted keys (the bucket's, or all at or above it)
+  uint32_t cidx[SL_CAP2];  // their blocks (two-pass form)
+  uint32_t bmA[SL_BMAX / 32];  // taken blocks (two-pass form)
+  uint32_t bmE[SL_BMAX / 32];  // blocks tied at the k-th key
   uint32_t wsum[SL_WARPS];
   uint32_t ccount;
   uint32_t b_bin, b_above, b_cnt;
 };
+
+// CTA-wide exclusive prefix sum of v (thread order); *total gets the sum.
+__device__ uint32_t cta_excl_scan(SLShared& sm, uint32_t v, uint32_t* total) {
+  const int lane = lane_id(), warp = warp_id();
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sm.wsum[warp] = incl;
+  __syncthreads();
+  uint32_t base = 0, tot = 0;
+  for (int w = 0; w < SL_WARPS; ++w) {
+    const uint32_t x = sm.wsum[w];
+    if (w < warp) base += x;
+    tot += x;
+  }
+  __syncthreads();  // wsum is reused by the next scan
+  *total = tot;
+  return base + incl - v;
+}
 
 // Bucket search over hist (SL_BINS bins) for the rem-th largest: the bin b,
 // the count in bins above it and its own count (broadcast through sh).
@@ -139,6 +170,94 @@ __global__ void __launch_bounds__(SL_THREADS) k_select_long(SLArgs a) {
     rem -= sm.b_above;
     cnt = sm.b_cnt;
     sh = nsh;
+    if (!in_smem && sh == 21 && nh <= SL_BMAX && (need - rem) + cnt <= (uint32_t)SL_CAP2) {
+      // ---- two-pass form: keep every key at or above the bucket with its
+      // block, resolve the bucket among them, and emit from bitmaps over the
+      // row's blocks (no third pass over the row)
+      if (tid == 0) sm.ccount = 0u;
+      __syncthreads();
+      for (int64_t j = tid; j < nh; j += SL_THREADS) {
+        const uint32_t key = order_key(__ldg(row + j));
+        if ((key >> sh) >= T) {
+          const uint32_t p = atomicAdd(&sm.ccount, 1u);
+          if (p < (uint32_t)SL_CAP2) {
+            sm.ckey[p] = key;
+            sm.cidx[p] = (uint32_t)j;
+          }
+        }
+      }
+      __syncthreads();
+      const uint32_t n2 = sm.ccount < (uint32_t)SL_CAP2 ? sm.ccount : (uint32_t)SL_CAP2;
+      if (sm.ccount != (need - rem) + cnt && tid == 0) report(a.status, SGQA_ERR_BOUNDS, (int)t);
+      while (cnt != rem && sh > 0) {  // the bucket's remaining digits
+        const int w2 = sh < 11 ? sh : 11;
+        const int nsh2 = sh - w2;
+        const uint32_t m2 = (1u << w2) - 1u;
+        for (int i = tid; i < SL_BINS; i += SL_THREADS) sm.hist[i] = 0u;
+        __syncthreads();
+        for (uint32_t i = tid; i < n2; i += SL_THREADS) {
+          const uint32_t key = sm.ckey[i];
+          if ((key >> sh) == T) atomicAdd(&sm.hist[(key >> nsh2) & m2], 1u);
+        }
+        __syncthreads();
+        cta_find_bin(sm, rem);
+        T = (T << w2) | sm.b_bin;
+        rem -= sm.b_above;
+        cnt = sm.b_cnt;
+        sh = nsh2;
+        __syncthreads();
+      }
+      const int nwords = (int)((nh + 31) >> 5);
+      for (int i = tid; i < nwords; i += SL_THREADS) {
+        sm.bmA[i] = 0u;
+        sm.bmE[i] = 0u;
+      }
+      __syncthreads();
+      const bool tie2 = cnt != rem;
+      for (uint32_t i = tid; i < n2; i += SL_THREADS) {
+        const uint32_t key = sm.ckey[i], j = sm.cidx[i];
+        const uint32_t p = key >> sh;  // sh < 32 here
+        const uint32_t bit = 1u << (j & 31);
+        if (p > T || (p == T && !tie2)) atomicOr(&sm.bmA[j >> 5], bit);
+        else if (p == T) atomicOr(&sm.bmE[j >> 5], bit);
+      }
+      __syncthreads();
+      // each thread owns a contiguous run of bitmap words
+      const int per = (nwords + SL_THREADS - 1) / SL_THREADS;
+      const int w0 = tid * per, w1 = min(nwords, w0 + per);
+      uint32_t tot = 0;
+      if (tie2) {  // the first `rem` tied blocks in block order join the taken ones
+        uint32_t c = 0;
+        for (int w = w0; w < w1; ++w) c += __popc(sm.bmE[w]);
+        int left = (int)rem - (int)cta_excl_scan(sm, c, &tot);
+        for (int w = w0; w < w1 && left > 0; ++w) {
+          const uint32_t e = sm.bmE[w];
+          const int n = __popc(e);
+          if (n <= left) {
+            sm.bmA[w] |= e;
+            left -= n;
+          } else {
+            sm.bmA[w] |= e & ((2u << __fns(e, 0, left)) - 1u);  // its lowest `left` bits
+            left = 0;
+          }
+        }
+        __syncthreads();
+      }
+      uint32_t c = 0;
+      for (int w = w0; w < w1; ++w) c += __popc(sm.bmA[w]);
+      uint32_t pos = cta_excl_scan(sm, c, &tot);
+      for (int w = w0; w < w1; ++w) {
+        uint32_t m = sm.bmA[w];
+        while (m) {
+          if (pos < need) out[pos] = w * 32 + (__ffs(m) - 1);
+          ++pos;
+          m &= m - 1u;
+        }
+      }
+      for (int64_t x = need + tid; x < a.Ks; x += SL_THREADS) out[x] = -1;
+      if (tid == 0 && tot != need) report(a.status, SGQA_ERR_BOUNDS, (int)t);
+      return;
+    }
     if (!in_smem && cnt != rem && sh > 0 && cnt <= (uint32_t)SL_CAP) {
       // compact the bucket's members (any order) for the remaining levels
       if (tid == 0) sm.ccount = 0u;
