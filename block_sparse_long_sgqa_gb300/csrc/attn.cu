@@ -19,8 +19,9 @@
 //  warp 0   builds each stage's block list from the union entries (an
 //           8-deep ring, so the lists run ahead of the loads);
 //  warp 11  issues the K loads: for B >= 8 one contiguous bulk copy per block
-//           from the block-packed, pre-swizzled K (see k_kv_pack), for B < 8 a
-//           cp.async row gather from the original layout;
+//           from the block-packed, pre-swizzled K (see k_kv_pack), for B < 8
+//           four-row TMA gathers (tile::gather4) from the original layout,
+//           contiguous or paged;
 //  warp 1   issues the V loads the same way;
 //  warp 2   one thread issues S = Q K^T into a double-buffered TMEM tile
 //           (K slots, three of them, are released as soon as their QK product
@@ -50,10 +51,15 @@ struct MetaT {         // one stage's block list
   int32_t pad;
   int32_t blk[NBPS];
   uint64_t mask[NBPS]; // bit qi: query qi of the sub-tile may attend the block
+  // B = 2, 4: qb[qi][w] bit j: query qi selected the historical block in slot
+  // 32 w + j (slots before diag), the transpose of mask written once per stage
+  static constexpr int N = NBPS;
+  static constexpr int QW = NBPS == 32 || NBPS == 64 ? NBPS / 32 : 0;
+  uint32_t qb[64][QW > 0 ? QW : 1];
 };
 
 // Bit bs (bs < diag): query qi of the sub-tile selected the historical block
-// in slot bs of this stage.
+// in slot bs of this stage (B >= 8: at most 16 slots, read per thread).
 template <typename Meta>
 __device__ __forceinline__ uint32_t qbits_of(const Meta& m, int qi) {
   constexpr int N = (int)(sizeof(m.blk) / sizeof(m.blk[0]));
@@ -65,12 +71,41 @@ __device__ __forceinline__ uint32_t qbits_of(const Meta& m, int qi) {
   return diag >= 32 ? hb : (hb & ((1u << diag) - 1u));
 }
 
+// Keys 32 w .. 32 w + 31 of a stage that query qi may attend among its
+// historical blocks, from the query's slot bits hb (slots 32 w / B ..), each
+// widened to the B keys of its block (a block never straddles a 32-key word).
+template <int B>
+__device__ __forceinline__ uint32_t hist_keys(uint32_t hb, int w) {
+  if constexpr (B == 2) {
+    uint32_t x = (hb >> ((w & 1) * 16)) & 0xFFFFu;  // hb: the slot word of keys 64 (w / 2) ..
+    x = (x | (x << 8)) & 0x00FF00FFu;
+    x = (x | (x << 4)) & 0x0F0F0F0Fu;
+    x = (x | (x << 2)) & 0x33333333u;
+    x = (x | (x << 1)) & 0x55555555u;  // bit i at 2 i
+    return x * 3u;
+  } else if constexpr (B == 4) {
+    uint32_t x = (hb >> (w * 8)) & 0xFFu;
+    x = (x | (x << 12)) & 0x000F000Fu;
+    x = (x | (x << 6)) & 0x03030303u;
+    x = (x | (x << 3)) & 0x11111111u;  // bit i at 4 i
+    return x * 0xFu;
+  } else if constexpr (B == 8) {
+    return ((((hb >> (w * 4)) & 0xFu) * 0x00204081u) & 0x01010101u) * 0xFFu;
+  } else {
+    static_assert(B == 16, "block sizes 2, 4, 8, 16");
+    const uint32_t x = hb >> (w * 2);
+    return ((x & 1u) ? 0x0000FFFFu : 0u) | ((x & 2u) ? 0xFFFF0000u : 0u);
+  }
+}
+
 template <int D, int B>
 struct AttnCfg {
   static constexpr int BM = 128;  // rows per MMA
   static constexpr int KB = 128;  // keys per stage
   static constexpr int NBPS = KB / B;
-  static constexpr bool TMA = B >= 8;  // blocks are whole 8-row swizzle atoms
+  // B >= 8: blocks are whole 8-row swizzle atoms, one bulk copy each from the
+  // packed copy; smaller blocks are gathered key by key (four-row TMA gathers)
+  static constexpr bool TMA = B >= 8;
   static constexpr int SK = 3;            // K slots
   static constexpr int SV = 2;            // V slots
   static constexpr int NM = 8;            // stage block-list slots
@@ -110,17 +145,6 @@ struct AttnArgs {
   int32_t* status;
 };
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -130,12 +154,6 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
   return m;
-}
-
-// Byte offset of 16-byte unit u (0..7) of row r inside a [rows][128 B] tile
-// with the 128-byte swizzle that TMA and UMMA use.
-__device__ __forceinline__ uint32_t sw128(int r, int u) {
-  return (uint32_t)(r * 128 + ((u ^ (r & 7)) << 4));
 }
 
 // State of the block-list generator of one work item (kept by warp 0).
@@ -157,7 +175,7 @@ __device__ __forceinline__ void union_entry(const AttnArgs& a, int64_t idx, int6
 }
 
 // Fill `m` with up to nbps blocks.  Warp-cooperative (warp 0).
-template <typename Meta>
+template <bool QB, typename Meta>
 __device__ void gen_stage(const AttnArgs& a, Gen& gs, Meta& m, int nbps, int sh, uint64_t qmask,
                           int nq) {
   const int lane = lane_id();
@@ -199,10 +217,10 @@ __device__ void gen_stage(const AttnArgs& a, Gen& gs, Meta& m, int nbps, int sh,
         gs.cur += 32;
       }
     } else {
-      // take the first `room` entries of this chunk only
-      uint32_t mm = pm;
-      for (int k = 1; k < room; ++k) mm &= mm - 1;
-      const int last_lane = __ffs(mm) - 1;
+      // take the first `room` entries of this chunk only (cnt > room >= 1, so
+      // exactly one lane holds the entry of rank room - 1)
+      const int last_lane =
+          __ffs(__ballot_sync(FULL, ((pm >> lane) & 1u) && rank == room - 1)) - 1;
       if (((pm >> lane) & 1u) && rank < room) {
         m.blk[n + rank] = b;
         m.mask[n + rank] = sub;
@@ -240,15 +258,34 @@ __device__ void gen_stage(const AttnArgs& a, Gen& gs, Meta& m, int nbps, int sh,
     m.last = gs.phase == 2 ? 1 : 0;
   }
   __syncwarp();
-  if (nbps <= 32) {
-    // first slot holding a current block of the sub-tile (the slots before it
-    // are historical; the softmax threads read their queries' bits from them)
-    const bool inb = lane < n;
-    const int32_t blk = inb ? m.blk[lane] : 0;
-    const uint32_t cur_m = __ballot_sync(FULL, inb && blk >= gs.c0);
-    if (lane == 0) m.diag = cur_m ? __ffs(cur_m) - 1 : n;
-    __syncwarp();
+  // first slot holding a current block of the sub-tile: the slots before it
+  // are historical; with QB each query's bits over them are transposed into
+  // qb (one ballot per query and 32 slots) for the softmax threads
+  // (B = 1 takes every slot block by block and needs neither)
+  if constexpr (Meta::N > 64) return;
+  int diag = n;
+  for (int w0 = 0; w0 < n; w0 += 32) {
+    const int bs = w0 + lane;
+    const uint32_t cm = __ballot_sync(FULL, bs < n && m.blk[bs] >= gs.c0);
+    if (cm) {
+      diag = w0 + __ffs(cm) - 1;
+      break;
+    }
   }
+  if (lane == 0) m.diag = diag;
+  if constexpr (QB) {
+#pragma unroll
+    for (int w = 0; w < Meta::QW; ++w) {
+      const int bs = w * 32 + lane;
+      const uint64_t mk = bs < diag ? m.mask[bs] : 0ull;
+#pragma unroll 1
+      for (int qi = 0; qi < nq; ++qi) {
+        const uint32_t bits = __ballot_sync(FULL, (mk >> qi) & 1ull);
+        if (lane == (qi & 31)) m.qb[qi][w] = bits;
+      }
+    }
+  }
+  __syncwarp();
 }
 
 // Bulk-copy a stage's packed blocks into shared slots 0..NBPS-1 (warp-wide):
@@ -268,19 +305,42 @@ __device__ __forceinline__ void copy_blocks(uint8_t* dst, const __nv_bfloat16* b
   }
 }
 
-template <int D>
-__device__ __forceinline__ const __nv_bfloat16* kv_row(const AttnArgs& a, const __nv_bfloat16* base,
-                                                       int g, int64_t p) {
-  if (a.ps > 0) {
-    const int64_t phys = a.page_table[p / a.ps];
-    return base + ((phys * a.Hkv + g) * a.ps + (p % a.ps)) * (int64_t)D;
+// Gathers one stage's 128 key rows (bf16) of K or V for KV head g into the
+// [head-dim half][key][128 B] swizzled layout the MMA reads: lane j brings keys
+// 4j .. 4j + 3, one four-row TMA gather per 64-column half.  The map's rows
+// are p * Hkv + g (contiguous cache) or (page * Hkv + g) * page_size + p %
+// page_size (paged).  Keys past the stage's blocks read position 0 instead;
+// the softmax gives them no weight.
+template <int D, int B, int NBPS>
+__device__ __forceinline__ void gather_stage(uint8_t* dst, const CUtensorMap* map,
+                                             const AttnArgs& a, const MetaT<NBPS>& m, int g,
+                                             int lane, uint64_t* bar) {
+  constexpr int KB = 128;
+  static_assert(KB == 4 * 32, "one four-row gather per lane and half");
+  const int nkeys = m.nb * B;
+  int32_t r[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int k = lane * 4 + e;
+    int64_t p = k < nkeys ? (int64_t)m.blk[k / B] * B + (k % B) : 0;
+    if (p >= a.Tkv) p = 0;
+    int64_t row = a.ps > 0 ? ((int64_t)a.page_table[p / a.ps] * a.Hkv + g) * a.ps + p % a.ps
+                           : p * a.Hkv + g;
+    if (row > 0x7fffffffll) {  // beyond the map's 32-bit row coordinate
+      report(a.status, SGQA_ERR_BOUNDS, 230);
+      row = 0;
+    }
+    r[e] = (int32_t)row;
   }
-  return base + (p * a.Hkv + g) * (int64_t)D;
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c)
+    tma_gather4(dst + c * (KB * 128) + lane * 512, map, bar, c * 64, r[0], r[1], r[2], r[3]);
 }
 
 template <int D, int B>
 __global__ void __launch_bounds__(384, 1)
-    k_sparse_attn(const __grid_constant__ CUtensorMap mq, AttnArgs a) {
+    k_sparse_attn(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                  const __grid_constant__ CUtensorMap mv, AttnArgs a) {
   using C = AttnCfg<D, B>;
   using Meta = MetaT<C::NBPS>;
   constexpr int NBPS = C::NBPS;  // blocks per stage
@@ -329,11 +389,11 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < C::SK; ++i) {
-      mbar_init(&k_full[i], kTma ? 1 : 64);
+      mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
     }
     for (int i = 0; i < C::SV; ++i) {
-      mbar_init(&v_full[i], kTma ? 1 : 64);
+      mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
     for (int i = 0; i < C::NM; ++i) {
@@ -363,6 +423,10 @@ __global__ void __launch_bounds__(384, 1)
     // ================================================ block lists + K loads
     if (lane == 0) {
       tma_prefetch_desc(&mq);
+      if constexpr (!kTma) {
+        tma_prefetch_desc(&mk);
+        tma_prefetch_desc(&mv);
+      }
       // the Q box is G x QS rows (fewer than 128 when a sub-tile cannot fill M)
       mbar_expect_tx(q_full, (uint32_t)(C::KC * 128 * a.G * a.QS));
       for (int c = 0; c < C::KC; ++c)  // box (64, G, QS) lands as rows qi * G + h
@@ -385,7 +449,7 @@ __global__ void __launch_bounds__(384, 1)
       const bool w = mbar_wait(&m_empty[ms], (uint32_t)(((i / C::NM) & 1) ^ 1), ab, a.status, 201);
       if (!__all_sync(FULL, w)) break;
       Meta& m = meta_at(ms);
-      gen_stage(a, gs, m, NBPS, sh, qmask, nq_sub);
+      gen_stage<B == 2 || B == 4>(a, gs, m, NBPS, sh, qmask, nq_sub);
       if (lane == 0 && m.last) {
         *n_stages = i + 1;  // lets the softmax group without a further stage stop
         __threadfence_block();
@@ -405,39 +469,21 @@ __global__ void __launch_bounds__(384, 1)
       const Meta& m = meta_at(ms);
       const bool last = m.last != 0;
       uint8_t* sK = smem + C::OFF_K + ks * C::KV_TILE;
-      if constexpr (kTma) {
-        // lane bs copies block slot bs (one contiguous packed block each)
-        constexpr uint32_t BLK = B * D * 2;
-        if (lane == 0) mbar_expect_tx(&k_full[ks], C::KV_TILE);
-        __syncwarp();
+      if (lane == 0) mbar_expect_tx(&k_full[ks], C::KV_TILE);
+      __syncwarp();
+      if constexpr (kTma)  // lane bs copies block slot bs (one contiguous packed block each)
         copy_blocks<NBPS>(sK, a.Kp + (int64_t)g * (a.nblkp + 1) * (B * D), m.blk, m.nb,
-                              a.nblkp, B * D, &k_full[ks]);
-        ++issued_k[ks];
-      } else {
-        const int nkeys = m.nb * B;
-        for (int idx = lane; idx < C::KB * (D / 8); idx += 32) {
-          const int k = idx / (D / 8), c = idx % (D / 8);
-          const uint32_t o = (c >> 3) * (C::KB * 128) + sw128(k, c & 7);
-          const int64_t p = k < nkeys ? (int64_t)m.blk[k / B] * B + (k % B) : a.Tkv;
-          if (p < a.Tkv)
-            cp_async16(sK + o, kv_row<D>(a, a.K, g, p) + c * 8);
-          else
-            *reinterpret_cast<uint4*>(sK + o) = make_uint4(0, 0, 0, 0);
-        }
-        mbar_arrive(&k_full[ks]);
-        cp_async_arrive(&k_full[ks]);
-      }
+                          a.nblkp, B * D, &k_full[ks]);
+      else
+        gather_stage<D, B, NBPS>(sK, &mk, a, m, g, lane, &k_full[ks]);
+      ++issued_k[ks];
       __syncwarp();
       if (lane == 0) mbar_arrive(&m_empty[ms]);
       if (last) break;
     }
-    if constexpr (kTma) {
-      if (lane == 0 && ab.set())  // let in-flight copies land before the CTA exits
-        for (int k = 0; k < C::SK; ++k)
-          if (issued_k[k] > 0) mbar_wait_drain(&k_full[k], (issued_k[k] - 1) & 1, a.status, 292);
-    } else {
-      cp_async_wait_all();
-    }
+    if (lane == 0 && ab.set())  // let in-flight copies land before the CTA exits
+      for (int k = 0; k < C::SK; ++k)
+        if (issued_k[k] > 0) mbar_wait_drain(&k_full[k], (issued_k[k] - 1) & 1, a.status, 292);
   } else if (warp == 1) {
     // ============================================================= V loads
     int issued_v[C::SV] = {};
@@ -449,38 +495,21 @@ __global__ void __launch_bounds__(384, 1)
       const Meta& m = meta_at(ms);
       const bool last = m.last != 0;
       uint8_t* sV = smem + C::OFF_V + vs * C::KV_TILE;
-      if constexpr (kTma) {
-        constexpr uint32_t BLK = B * D * 2;
-        if (lane == 0) mbar_expect_tx(&v_full[vs], C::KV_TILE);
-        __syncwarp();
+      if (lane == 0) mbar_expect_tx(&v_full[vs], C::KV_TILE);
+      __syncwarp();
+      if constexpr (kTma)
         copy_blocks<NBPS>(sV, a.Vp + (int64_t)g * (a.nblkp + 1) * (B * D), m.blk, m.nb,
-                              a.nblkp, B * D, &v_full[vs]);
-        ++issued_v[vs];
-      } else {
-        const int nkeys = m.nb * B;
-        for (int idx = lane; idx < C::KB * (D / 8); idx += 32) {
-          const int k = idx / (D / 8), c = idx % (D / 8);
-          const uint32_t o = (c >> 3) * (C::KB * 128) + sw128(k, c & 7);
-          const int64_t p = k < nkeys ? (int64_t)m.blk[k / B] * B + (k % B) : a.Tkv;
-          if (p < a.Tkv)
-            cp_async16(sV + o, kv_row<D>(a, a.V, g, p) + c * 8);
-          else
-            *reinterpret_cast<uint4*>(sV + o) = make_uint4(0, 0, 0, 0);
-        }
-        mbar_arrive(&v_full[vs]);
-        cp_async_arrive(&v_full[vs]);
-      }
+                          a.nblkp, B * D, &v_full[vs]);
+      else
+        gather_stage<D, B, NBPS>(sV, &mv, a, m, g, lane, &v_full[vs]);
+      ++issued_v[vs];
       __syncwarp();
       if (lane == 0) mbar_arrive(&m_empty[ms]);
       if (last) break;
     }
-    if constexpr (kTma) {
-      if (lane == 0 && ab.set())
-        for (int k = 0; k < C::SV; ++k)
-          if (issued_v[k] > 0) mbar_wait_drain(&v_full[k], (issued_v[k] - 1) & 1, a.status, 293);
-    } else {
-      cp_async_wait_all();
-    }
+    if (lane == 0 && ab.set())
+      for (int k = 0; k < C::SV; ++k)
+        if (issued_v[k] > 0) mbar_wait_drain(&v_full[k], (issued_v[k] - 1) & 1, a.status, 293);
   } else if (warp == 2) {
     // ============================================================ MMA issuer
     if (lane == 0) {
@@ -491,7 +520,6 @@ __global__ void __launch_bounds__(384, 1)
       // S_j = Q K_j^T into TMEM buffer j % 2 (operands ready)
       auto do_qk = [&](int j) {
         const int ks = j % C::SK;
-        if (!kTma) fence_proxy_async_smem();  // cp.async writes -> tensor-core reads
         tc_fence_after();
         const uint32_t sK = smem_u32(smem + C::OFF_K + ks * C::KV_TILE);
 #pragma unroll
@@ -511,7 +539,6 @@ __global__ void __launch_bounds__(384, 1)
       // O[i % 2] += P_i V_i, P read from TMEM (operands ready)
       auto do_pv = [&](int i) {
         const int vs = i % C::SV;
-        if (!kTma) fence_proxy_async_smem();
         tc_fence_after();
         const uint32_t sV = smem_u32(smem + C::OFF_V + vs * C::KV_TILE);
 #pragma unroll
@@ -639,24 +666,25 @@ __global__ void __launch_bounds__(384, 1)
       // prefix of the query's own block.
       uint32_t al0 = 0u, al1 = 0u, al2 = 0u, al3 = 0u;
       if (row_ok) {
-        int bsd = 0;  // first slot handled block by block
-        if constexpr (kTma) {
-          // historical blocks: the query's bitmask, one bit per block -> B keys
+        // historical blocks from the query's slot bits, widened to keys; then
+        // the current blocks of the sub-tile block by block (the causal cut).
+        // B = 1 takes every slot block by block.
+        int bsd = 0;
+        if constexpr (B >= 8) {
           const uint32_t hb = qbits_of(m, qi);
-          if constexpr (B == 8) {
-            al0 = ((((hb >> 0) & 0xFu) * 0x00204081u) & 0x01010101u) * 0xFFu;
-            al1 = ((((hb >> 4) & 0xFu) * 0x00204081u) & 0x01010101u) * 0xFFu;
-            al2 = ((((hb >> 8) & 0xFu) * 0x00204081u) & 0x01010101u) * 0xFFu;
-            al3 = ((((hb >> 12) & 0xFu) * 0x00204081u) & 0x01010101u) * 0xFFu;
-          } else {  // B == 16: two blocks of 16 keys per word
-            al0 = ((hb & 1u) ? 0x0000FFFFu : 0u) | ((hb & 2u) ? 0xFFFF0000u : 0u);
-            al1 = ((hb & 4u) ? 0x0000FFFFu : 0u) | ((hb & 8u) ? 0xFFFF0000u : 0u);
-            al2 = ((hb & 16u) ? 0x0000FFFFu : 0u) | ((hb & 32u) ? 0xFFFF0000u : 0u);
-            al3 = ((hb & 64u) ? 0x0000FFFFu : 0u) | ((hb & 128u) ? 0xFFFF0000u : 0u);
-          }
+          al0 = hist_keys<B>(hb, 0);
+          al1 = hist_keys<B>(hb, 1);
+          al2 = hist_keys<B>(hb, 2);
+          al3 = hist_keys<B>(hb, 3);
+          bsd = m.diag;
+        } else if constexpr (B >= 2) {
+          constexpr int hw = B == 2 ? 1 : 0;  // slot word of keys 64 .. 127
+          al0 = hist_keys<B>(m.qb[qi][0], 0);
+          al1 = hist_keys<B>(m.qb[qi][0], 1);
+          al2 = hist_keys<B>(m.qb[qi][hw], 2);
+          al3 = hist_keys<B>(m.qb[qi][hw], 3);
           bsd = m.diag;
         }
-        // current blocks of the sub-tile (and, without the bitmask, every block)
 #pragma unroll 1
         for (int bs = bsd; bs < nb; ++bs) {
           const int64_t b = m.blk[bs];
@@ -683,10 +711,10 @@ __global__ void __launch_bounds__(384, 1)
       // exponentials); otherwise the stage is redone in two passes below.
       float rs0 = 0.0f, rs1 = 0.0f;
       bool fast = __all_sync(FULL, m_used != ninf || (al0 | al1 | al2 | al3) == 0u);
-      // Stages whose blocks are all historical (B >= 8) take the mask per
+      // Stages whose blocks are all historical (B >= 4) take the mask per
       // block: block maxima, and -m or -inf as the exponent's additive term.
       bool by_block = false;
-      if constexpr (kTma) by_block = m.diag >= nb;
+      if constexpr (B >= 8) by_block = m.diag >= nb;
       if (fast && by_block) {
         constexpr int BPHh = 64 / B;  // blocks per 64 keys
         const uint32_t hb = row_ok ? qbits_of(m, qi) : 0u;
@@ -926,16 +954,43 @@ bool make_qmap(const Dims& dm, int QS, const void* Q, CUtensorMap* mq) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map for gathering single key rows of K or V (bf16): a 2-d view
+// [rows][d] with box 64 x 1 and the 128-byte swizzle.  Rows are p * Hkv + g
+// for a contiguous cache; a paged cache's pool size is not passed, so its view
+// spans every row a 32-bit coordinate can name and the page table bounds the
+// rows actually read.
+bool make_kvmap(const Dims& dm, const void* X, CUtensorMap* mx) {
+  auto fn = tmap_encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t e = 2;
+  const cuuint32_t estr[2] = {1, 1};
+  const cuuint64_t rows =
+      dm.ps > 0 ? (cuuint64_t)0x7fffffff : (cuuint64_t)dm.Tkv * (cuuint64_t)dm.Hkv;
+  cuuint64_t dims[2] = {(cuuint64_t)dm.d, rows};
+  cuuint64_t str[1] = {dm.d * e};
+  cuuint32_t box[2] = {64, 1};
+  return fn(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, str, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, int B>
 int launch_db(const Dims& dm, const AttnArgs& a, const void* Q, int64_t items, cudaStream_t st) {
   using C = AttnCfg<D, B>;
-  CUtensorMap mq;
+  CUtensorMap mq, mk, mv;
   if (!make_qmap(dm, a.QS, Q, &mq)) return SGQA_ERR_CUDA;
+  if constexpr (C::TMA) {  // packed blocks: bulk copies, no gather maps
+    memset(&mk, 0, sizeof(mk));
+    memset(&mv, 0, sizeof(mv));
+  } else {
+    if (dm.ps == 0 && (int64_t)dm.Tkv * dm.Hkv > 0x7fffffffll) return SGQA_ERR_UNSUPPORTED;
+    if (!make_kvmap(dm, a.K, &mk) || !make_kvmap(dm, a.V, &mv)) return SGQA_ERR_CUDA;
+  }
   if (cudaFuncSetAttribute(k_sparse_attn<D, B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM) != cudaSuccess)
     return SGQA_ERR_CUDA;
   log_begin(SGQA_K_ATTN, st);
-  k_sparse_attn<D, B><<<(unsigned)items, C::NTHREADS, C::SMEM, st>>>(mq, a);
+  k_sparse_attn<D, B><<<(unsigned)items, C::NTHREADS, C::SMEM, st>>>(mq, mk, mv, a);
   log_end(st);
   return cudaGetLastError() == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA;
 }

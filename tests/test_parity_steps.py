@@ -28,6 +28,12 @@ SMALL = {
                           topk_tokens=256),
     "d64_g2": BASE.replace(name="d64_g2", seq_q=400, seq_kv=450, q_offset=50, n_q_heads=8,
                            n_kv_heads=4, head_dim=64, topk_tokens=96, tile_q=32),
+    # key-by-key gathers (B < 8) from a paged cache with a partly filled last
+    # page, and at head_dim 64
+    "paged_b4": BASE.replace(name="paged_b4", seq_q=600, seq_kv=1000, q_offset=400, block_size=4,
+                             page_size=64, topk_tokens=128),
+    "d64_b2": BASE.replace(name="d64_b2", seq_q=300, seq_kv=380, q_offset=80, n_q_heads=8,
+                           n_kv_heads=4, head_dim=64, block_size=2, topk_tokens=64, tile_q=32),
     # Step-5-shaped heads with planted needles: large logit jumps between stages
     # exercise the online-softmax rescale of O in TMEM
     "needles": synth.WORKLOADS["step5_128k"].replace(name="needles", seq_q=1200, seq_kv=1200,
