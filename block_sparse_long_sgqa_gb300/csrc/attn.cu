@@ -360,7 +360,6 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* m_full = bars + 11;    // [NM]
   uint64_t* m_empty = bars + 19;   // [NM]
   uint64_t* s_full = bars + 27;    // [2]
-  uint64_t* s_empty = bars + 29;   // [2]
   uint64_t* p_full = bars + 31;    // [2] P of a stage of softmax group g written
   uint64_t* mma_done = bars + 33;
   uint64_t* p_empty = bars + 34;   // [2] PV product into O[g] done
@@ -402,7 +401,6 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 1);  // committed after the PV product that reads P
       mbar_init(&p_full[i], 4);
       mbar_init(&p_empty[i], 1);
     }
@@ -556,12 +554,15 @@ __global__ void __launch_bounds__(384, 1)
         }
         umma_commit(&p_empty[i & 1]);
         umma_commit(&v_empty[vs]);
-        umma_commit(&s_empty[i & 1]);  // S/P buffer free for QK_{i+2}
       };
       // Issue each product as soon as its operands are ready (the two softmax
-      // groups' chains are independent), PV first since it frees an S buffer.
-      // QK_j is tested only once PV_{j-2} has been issued, so every phase
-      // tested is at most one ahead of the last one completed.
+      // groups' chains are independent), PV first.  QK_j overwrites the S/P
+      // buffer that PV_{j-2} reads P from; it is issued once PV_{j-2} has been
+      // issued, not once it has completed: tcgen05.mma operations of one
+      // thread execute in issue order, so PV_{j-2} has read P before QK_j
+      // writes S.  Every phase tested is at most one ahead of the last one
+      // completed.  (Polling measured faster than sleeping in each barrier in
+      // turn: the wake-up from a suspended wait lengthens every hand-off.)
       int qn = 0, pn = 0;  // next QK and PV to issue
       int n_st = -1;       // stages of the item, once the last list has been seen
       uint64_t t_prog = globaltimer();
@@ -576,8 +577,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         if ((n_st < 0 || qn < n_st) && qn <= pn + 1 &&
             mbar_test(&m_full[qn % C::NM], (uint32_t)((qn / C::NM) & 1)) &&
-            mbar_test(&k_full[qn % C::SK], (uint32_t)((qn / C::SK) & 1)) &&
-            mbar_test(&s_empty[qn & 1], (uint32_t)(((qn >> 1) & 1) ^ 1))) {
+            mbar_test(&k_full[qn % C::SK], (uint32_t)((qn / C::SK) & 1))) {
           if (meta_at(qn % C::NM).last) n_st = qn + 1;
           do_qk(qn);
           ++qn;
