@@ -175,14 +175,23 @@ IndexWs carve_index(Carve& c, const Dims& dm, int64_t nq) {
   return w;
 }
 
+// Whether the attention reads K/V from block-packed copies made by the call
+// (B >= 8): worth it when the call gathers at least as many blocks as the
+// cache holds, and always for fp32 inputs (the copy converts them on the
+// way).  Otherwise (a few queries over a long cache, as in a decode step) the
+// keys are gathered from the cache itself.
+bool use_pack(const Dims& dm) {
+  return dm.B >= 8 && (dm.dtype == SGQA_FP32 || dm.T * dm.Ks >= dm.nblk);
+}
+
 struct AttnWs {
   __nv_bfloat16 *Q, *K, *V;  // bf16 copies of fp32 inputs (null when not needed)
-  __nv_bfloat16 *Kp, *Vp;    // block-packed K/V for B >= 8 (k_kv_pack)
+  __nv_bfloat16 *Kp, *Vp;    // block-packed K/V (use_pack)
 };
 AttnWs carve_attn(Carve& c, const Dims& dm) {
   AttnWs w{nullptr, nullptr, nullptr, nullptr, nullptr};
   if (dm.dtype == SGQA_FP32) w.Q = c.take<__nv_bfloat16>((size_t)dm.T * dm.H * dm.d);
-  if (dm.B >= 8) {  // packed copies (converted to bf16 on the way)
+  if (use_pack(dm)) {  // packed copies (converted to bf16 on the way)
     w.Kp = c.take<__nv_bfloat16>((size_t)kv_pack_elems(dm));
     w.Vp = c.take<__nv_bfloat16>((size_t)kv_pack_elems(dm));
   } else if (dm.dtype == SGQA_FP32) {
@@ -262,28 +271,32 @@ PrefillWs carve_prefill(Carve& c, const Dims& dm) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA; }
 
-// Attention operands: fp32 inputs rounded to bf16, and for B >= 8 the
-// block-packed K/V.  Sets q/k/v to the buffers the attention kernel reads.
+// Attention operands: fp32 inputs rounded to bf16, and with use_pack the
+// block-packed K/V.  Sets q/k/v to the buffers the attention kernel reads and
+// `ad` to the dims it reads them with: fp32 K/V that are gathered key by key
+// are converted into a contiguous bf16 copy (page_size 0 in `ad`).
 cudaError_t stage_attn(const Dims& dm, const void* Q, const void* K, const void* V,
                        const int32_t* page_table, const AttnWs& w, const __nv_bfloat16** q,
-                       const __nv_bfloat16** k, const __nv_bfloat16** v, cudaStream_t st) {
+                       const __nv_bfloat16** k, const __nv_bfloat16** v, Dims* ad,
+                       cudaStream_t st) {
   *q = static_cast<const __nv_bfloat16*>(Q);
   *k = static_cast<const __nv_bfloat16*>(K);
   *v = static_cast<const __nv_bfloat16*>(V);
+  *ad = dm;
   cudaError_t e = cudaSuccess;
+  const bool pack = use_pack(dm);
   if (dm.dtype == SGQA_FP32) {
     e = launch_to_bf16(static_cast<const float*>(Q), w.Q, dm.T * dm.H * dm.d, st);
     *q = w.Q;
-    if (dm.B < 8) {
-      if (e == cudaSuccess)
-        e = launch_to_bf16(static_cast<const float*>(K), w.K, dm.Tkv * dm.Hkv * dm.d, st);
-      if (e == cudaSuccess)
-        e = launch_to_bf16(static_cast<const float*>(V), w.V, dm.Tkv * dm.Hkv * dm.d, st);
+    if (!pack) {
+      if (e == cudaSuccess) e = launch_kv_to_bf16(dm, static_cast<const float*>(K), page_table, w.K, st);
+      if (e == cudaSuccess) e = launch_kv_to_bf16(dm, static_cast<const float*>(V), page_table, w.V, st);
       *k = w.K;
       *v = w.V;
+      ad->ps = 0;
     }
   }
-  if (dm.B >= 8) {
+  if (pack) {
     if (e == cudaSuccess) e = launch_kv_pack(dm, K, page_table, w.Kp, st);
     if (e == cudaSuccess) e = launch_kv_pack(dm, V, page_table, w.Vp, st);
   }
@@ -419,15 +432,17 @@ SGQA_API int sgqa_sparse_attn_fwd(const sgqa_params* p, const void* Q, const voi
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
     return SGQA_ERR_ALIGNMENT;
   const size_t need = sgqa_workspace_bytes(p, SGQA_WS_SPARSE_ATTN);
-  if ((dm.dtype == SGQA_FP32 || dm.B >= 8) && (ws == nullptr || ws_bytes < need))
+  if ((dm.dtype == SGQA_FP32 || use_pack(dm)) && (ws == nullptr || ws_bytes < need))
     return SGQA_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   Carve c(align_ws(ws));
   AttnWs w = carve_attn(c, dm);
   const __nv_bfloat16 *q, *k, *v;
-  if (stage_attn(dm, Q, K, V, page_table, w, &q, &k, &v, st) != cudaSuccess) return SGQA_ERR_CUDA;
-  return launch_sparse_attn(dm, q, k, v, w.Kp, w.Vp, page_table, union_off, union_len, union_blk,
-                            union_mask, O, lse, 0, dm.ntiles, status, st);
+  Dims ad;
+  if (stage_attn(dm, Q, K, V, page_table, w, &q, &k, &v, &ad, st) != cudaSuccess)
+    return SGQA_ERR_CUDA;
+  return launch_sparse_attn(ad, q, k, v, w.Kp, w.Vp, ad.ps > 0 ? page_table : nullptr, union_off,
+                            union_len, union_blk, union_mask, O, lse, 0, dm.ntiles, status, st);
 }
 
 SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, const void* V,
@@ -463,7 +478,8 @@ SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, co
   }
   if (e == cudaSuccess && w.filt) e = launch_sample_keys(dm, w.ix.khi, w.ix.klo, w.shi, nullptr, st);
   const __nv_bfloat16 *q, *k, *v;
-  if (e == cudaSuccess) e = stage_attn(dm, Q, K, V, page_table, w.at, &q, &k, &v, st);
+  Dims ad;  // the dims the attention reads its K/V with
+  if (e == cudaSuccess) e = stage_attn(dm, Q, K, V, page_table, w.at, &q, &k, &v, &ad, st);
   if (e != cudaSuccess) return SGQA_ERR_CUDA;
 
   for (int64_t q0 = 0; q0 < dm.T; q0 += w.chunk) {
@@ -506,7 +522,8 @@ SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, co
                                   w.ucap, tau0, w.chunk_tiles, w.capG, status, st,
                                   filt ? w.rest : nullptr, filt ? w.counters : nullptr);
     if (rc != SGQA_OK) return rc;
-    rc = launch_sparse_attn_layout(dm, q, k, v, w.at.Kp, w.at.Vp, page_table, w.uoff, w.ulen,
+    rc = launch_sparse_attn_layout(ad, q, k, v, w.at.Kp, w.at.Vp,
+                                   ad.ps > 0 ? page_table : nullptr, w.uoff, w.ulen,
                                    w.ublk, w.umask, O, lse, tau0, tau1, tau0, w.chunk_tiles,
                                    status, st);
     if (rc != SGQA_OK) return rc;
@@ -522,7 +539,7 @@ SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int
   if (chunk_queries) *chunk_queries = chunk;
   if (launches) {
     // with an empty block-key cache: merge, operand staging (fp32 rounding,
-    // K/V block packing), then per chunk the index query and indexer GEMM
+    // K/V block packing when use_pack), then per chunk the index query and indexer GEMM
     // (when there are blocks), the row selects (a CTA-per-row launch too when
     // the chunk has rows of more than 16384 blocks), tile union and attention;
     // where some rows select from threshold candidates, the sampled-key gather
@@ -530,8 +547,9 @@ SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int
     // candidate select and the refill GEMM of the row tiles it left (the rows
     // it leaves then all go through the warp-per-row select)
     const bool any_filt = dm.nblk > 0 && chunk_filtered(dm, 0, dm.T);
-    int64_t n = (dm.nblk > 0 ? 1 : 0) + (dm.dtype == SGQA_FP32 ? (dm.B >= 8 ? 1 : 3) : 0) +
-                (dm.B >= 8 ? 2 : 0) + (any_filt ? 1 : 0);
+    const bool pack = use_pack(dm);
+    int64_t n = (dm.nblk > 0 ? 1 : 0) + (dm.dtype == SGQA_FP32 ? (pack ? 1 : 3) : 0) +
+                (pack ? 2 : 0) + (any_filt ? 1 : 0);
     for (int64_t q0 = 0; q0 < dm.T; q0 += chunk) {
       const int64_t q1 = std::min<int64_t>(dm.T, q0 + chunk);
       const bool filt = any_filt && chunk_filtered(dm, q0, q1);

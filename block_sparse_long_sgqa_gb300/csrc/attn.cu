@@ -103,9 +103,6 @@ struct AttnCfg {
   static constexpr int BM = 128;  // rows per MMA
   static constexpr int KB = 128;  // keys per stage
   static constexpr int NBPS = KB / B;
-  // B >= 8: blocks are whole 8-row swizzle atoms, one bulk copy each from the
-  // packed copy; smaller blocks are gathered key by key (four-row TMA gathers)
-  static constexpr bool TMA = B >= 8;
   static constexpr int SK = 3;            // K slots
   static constexpr int SV = 2;            // V slots
   static constexpr int NM = 8;            // stage block-list slots
@@ -337,14 +334,18 @@ __device__ __forceinline__ void gather_stage(uint8_t* dst, const CUtensorMap* ma
     tma_gather4(dst + c * (KB * 128) + lane * 512, map, bar, c * 64, r[0], r[1], r[2], r[3]);
 }
 
-template <int D, int B>
+// PK: the K/V blocks come from the block-packed copy (B >= 8: whole 8-row
+// swizzle atoms, one bulk copy each); otherwise keys are gathered four rows
+// at a time (TMA tile::gather4) from the original contiguous or paged cache.
+template <int D, int B, bool PK>
 __global__ void __launch_bounds__(384, 1)
     k_sparse_attn(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                   const __grid_constant__ CUtensorMap mv, AttnArgs a) {
   using C = AttnCfg<D, B>;
   using Meta = MetaT<C::NBPS>;
   constexpr int NBPS = C::NBPS;  // blocks per stage
-  constexpr bool kTma = C::TMA;
+  constexpr bool kTma = PK;
+  static_assert(!PK || B >= 8, "packed blocks are whole swizzle atoms");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -974,35 +975,40 @@ bool make_kvmap(const Dims& dm, const void* X, CUtensorMap* mx) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int B>
+template <int D, int B, bool PK>
 int launch_db(const Dims& dm, const AttnArgs& a, const void* Q, int64_t items, cudaStream_t st) {
   using C = AttnCfg<D, B>;
   CUtensorMap mq, mk, mv;
   if (!make_qmap(dm, a.QS, Q, &mq)) return SGQA_ERR_CUDA;
-  if constexpr (C::TMA) {  // packed blocks: bulk copies, no gather maps
+  if constexpr (PK) {  // packed blocks: bulk copies, no gather maps
     memset(&mk, 0, sizeof(mk));
     memset(&mv, 0, sizeof(mv));
   } else {
     if (dm.ps == 0 && (int64_t)dm.Tkv * dm.Hkv > 0x7fffffffll) return SGQA_ERR_UNSUPPORTED;
     if (!make_kvmap(dm, a.K, &mk) || !make_kvmap(dm, a.V, &mv)) return SGQA_ERR_CUDA;
   }
-  if (cudaFuncSetAttribute(k_sparse_attn<D, B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(k_sparse_attn<D, B, PK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM) != cudaSuccess)
     return SGQA_ERR_CUDA;
   log_begin(SGQA_K_ATTN, st);
-  k_sparse_attn<D, B><<<(unsigned)items, C::NTHREADS, C::SMEM, st>>>(mq, mk, mv, a);
+  k_sparse_attn<D, B, PK><<<(unsigned)items, C::NTHREADS, C::SMEM, st>>>(mq, mk, mv, a);
   log_end(st);
   return cudaGetLastError() == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA;
 }
 
 template <int D>
-int launch_d(const Dims& dm, const AttnArgs& a, const void* Q, int64_t items, cudaStream_t st) {
+int launch_d(const Dims& dm, const AttnArgs& a, const void* Q, bool packed, int64_t items,
+             cudaStream_t st) {
   switch (dm.B) {
-    case 1: return launch_db<D, 1>(dm, a, Q, items, st);
-    case 2: return launch_db<D, 2>(dm, a, Q, items, st);
-    case 4: return launch_db<D, 4>(dm, a, Q, items, st);
-    case 8: return launch_db<D, 8>(dm, a, Q, items, st);
-    case 16: return launch_db<D, 16>(dm, a, Q, items, st);
+    case 1: return launch_db<D, 1, false>(dm, a, Q, items, st);
+    case 2: return launch_db<D, 2, false>(dm, a, Q, items, st);
+    case 4: return launch_db<D, 4, false>(dm, a, Q, items, st);
+    case 8:
+      return packed ? launch_db<D, 8, true>(dm, a, Q, items, st)
+                    : launch_db<D, 8, false>(dm, a, Q, items, st);
+    case 16:
+      return packed ? launch_db<D, 16, true>(dm, a, Q, items, st)
+                    : launch_db<D, 16, false>(dm, a, Q, items, st);
     default: return SGQA_ERR_UNSUPPORTED;
   }
 }
@@ -1054,9 +1060,11 @@ int launch_sparse_attn_layout(const Dims& dm, const __nv_bfloat16* Q, const __nv
   a.scale_log2 = dm.scale * 1.4426950408889634f;
   a.status = status;
   const int64_t items = (tau_end - tau_begin) * dm.Hkv * a.nsub;
-  if (dm.B >= 8 && (Kp == nullptr || Vp == nullptr)) return SGQA_ERR_INVALID_ARG;
-  if (dm.d == 128) return launch_d<128>(dm, a, Q, items, st);
-  if (dm.d == 64) return launch_d<64>(dm, a, Q, items, st);
+  // packed copies given: B >= 8 bulk copies; else key gathers from K and V
+  const bool packed = Kp != nullptr && Vp != nullptr;
+  if (packed && dm.B < 8) return SGQA_ERR_INVALID_ARG;
+  if (dm.d == 128) return launch_d<128>(dm, a, Q, packed, items, st);
+  if (dm.d == 64) return launch_d<64>(dm, a, Q, packed, items, st);
   return SGQA_ERR_UNSUPPORTED;
 }
 

@@ -59,6 +59,9 @@ cudaError_t launch_split_kbar(const Dims& dm, const float* Kbar, __nv_bfloat16* 
 cudaError_t launch_index_query(const Dims& dm, const void* Q, int64_t q_begin, int64_t q_end,
                                __nv_bfloat16* qhi, __nv_bfloat16* qlo, cudaStream_t st);
 cudaError_t launch_to_bf16(const float* in, __nv_bfloat16* out, int64_t n, cudaStream_t st);
+// fp32 K or V (contiguous or paged) -> bf16 contiguous [Tkv][Hkv][d].
+cudaError_t launch_kv_to_bf16(const Dims& dm, const float* in, const int32_t* page_table,
+                              __nv_bfloat16* out, cudaStream_t st);
 
 // Block-packed, pre-swizzled copy of K or V for the attention gathers (B >= 8):
 // [Hkv][ceil(Tkv/B) + 1][B * d] bf16, the last block of each head all zeros.

@@ -153,6 +153,31 @@ __global__ void __launch_bounds__(256) k_to_bf16(const float* __restrict__ in, i
   }
 }
 
+// fp32 K or V of a paged cache -> bf16 in the contiguous [Tkv][Hkv][d]
+// layout: eight head-dim lanes of one (position, group) row per thread, the
+// row found through the page table.
+__global__ void __launch_bounds__(256) k_to_bf16_paged(const float* __restrict__ in,
+                                                       const int32_t* __restrict__ page_table,
+                                                       int ps, int64_t Tkv, int Hkv, int d,
+                                                       __nv_bfloat16* __restrict__ out) {
+  const int d8 = d / 8;
+  const int64_t n8 = Tkv * Hkv * d8;
+  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < n8;
+       x += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = x / d8;
+    const int c = (int)(x % d8);
+    const int64_t p = row / Hkv;
+    const int g = (int)(row % Hkv);
+    const float* src =
+        in + (((int64_t)page_table[p / ps] * Hkv + g) * ps + p % ps) * d + (int64_t)c * 8;
+    float v[8];
+    Vec8<float>::load(src, v);
+    uint4 u = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                         pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+    *reinterpret_cast<uint4*>(out + x * 8) = u;
+  }
+}
+
 // Block-packed K/V for the attention gathers: block j of KV head g becomes
 // B/8 groups of 8 positions; each group holds its d/64 head-dim halves as
 // 1 KB atoms of 8 rows x 128 B with the 128-byte swizzle (16-byte unit u of
@@ -325,6 +350,18 @@ cudaError_t launch_to_bf16(const float* in, __nv_bfloat16* out, int64_t n, cudaS
   if (n <= 0) return cudaSuccess;
   log_begin(SGQA_K_STAGE, st);
   k_to_bf16<<<grid_for(n / 8), 256, 0, st>>>(in, n / 8, out);
+  log_end(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_to_bf16(const Dims& dm, const float* in, const int32_t* page_table,
+                              __nv_bfloat16* out, cudaStream_t st) {
+  if (dm.ps == 0) return launch_to_bf16(in, out, dm.Tkv * dm.Hkv * dm.d, st);
+  const int64_t n8 = dm.Tkv * dm.Hkv * (dm.d / 8);
+  if (n8 <= 0) return cudaSuccess;
+  log_begin(SGQA_K_STAGE, st);
+  k_to_bf16_paged<<<grid_for(n8), 256, 0, st>>>(in, page_table, dm.ps, dm.Tkv, dm.Hkv, dm.d,
+                                                 out);
   log_end(st);
   return cudaGetLastError();
 }

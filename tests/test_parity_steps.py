@@ -34,6 +34,15 @@ SMALL = {
                              page_size=64, topk_tokens=128),
     "d64_b2": BASE.replace(name="d64_b2", seq_q=300, seq_kv=380, q_offset=80, n_q_heads=8,
                            n_kv_heads=4, head_dim=64, block_size=2, topk_tokens=64, tile_q=32),
+    # few queries over a longer cache: B >= 8 blocks gathered key by key
+    # instead of copied from a packed cache (fewer selected blocks than cached)
+    "few_b8": BASE.replace(name="few_b8", seq_q=8, seq_kv=3000, q_offset=2992, topk_tokens=256),
+    "few_b16_paged": BASE.replace(name="few_b16_paged", seq_q=4, seq_kv=2000, q_offset=1996,
+                                  head_dim=64, block_size=16, topk_tokens=256, page_size=64),
+    # fp32 inputs over a paged cache, keys gathered: converted through the page table
+    "f32_paged_b4": synth.WORKLOADS["tiny_2k"].replace(name="f32_paged_b4", seq_q=300, seq_kv=700,
+                                                      q_offset=400, block_size=4, topk_tokens=64,
+                                                      page_size=64),
     # Step-5-shaped heads with planted needles: large logit jumps between stages
     # exercise the online-softmax rescale of O in TMEM
     "needles": synth.WORKLOADS["step5_128k"].replace(name="needles", seq_q=1200, seq_kv=1200,
