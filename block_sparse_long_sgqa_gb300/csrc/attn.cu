@@ -32,7 +32,7 @@
 //           per-query block masks (the causal cut only on current blocks),
 //           exchange partial maxima through shared memory, run the fp32 online
 //           softmax in base 2 (O is rescaled in TMEM only when the running
-//           maximum grows by more than 2^8), write P (bf16) into TMEM over the
+//           maximum grows by more than 2^16), write P (bf16) into TMEM over the
 //           S values already read (the S buffer is released by the PV product),
 //           and finally normalise O and write O and the log-sum-exp.
 #include "common.cuh"
@@ -42,6 +42,13 @@ namespace sgqa {
 namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
+
+// Lazy rescaling: the softmax keeps a row's reference maximum until a key
+// exceeds it by more than 2^kLazy (log2 units), so P (bf16) stays below
+// 2^kLazy and O (fp32) is rescaled only on such a jump.  bf16 and fp32 keep
+// the same relative precision at any of these magnitudes; 2^16 leaves ample
+// range for sums of a stage's products into fp32.
+constexpr float kLazy = 16.0f;
 
 template <int NBPS>
 struct MetaT {         // one stage's block list
@@ -332,6 +339,94 @@ __device__ __forceinline__ void gather_stage(uint8_t* dst, const CUtensorMap* ma
 #pragma unroll
   for (int c = 0; c < D / 64; ++c)
     tma_gather4(dst + c * (KB * 128) + lane * 512, map, bar, c * 64, r[0], r[1], r[2], r[3]);
+}
+
+// A stage whose keys 64..127 exceed the softmax row's reference maximum by
+// more than 2^kLazy after keys 0..63 passed and were written as P (TMEM columns
+// 0..31 of the S buffer at tS) under it.  The S values of keys 64..127
+// (columns 64..127) are still in place: their masked maximum mx is taken,
+// the maximum raised to it (rows that need it) with O (at tOg, once the
+// group's previous PV product is done: phase `parity` of p_empty), l, the
+// stage's partial sums rs0/rs1 and the 32 P columns scaled by
+// 2^(m_used - mx), and P of keys 64..127 written into columns 32..63.  Kept
+// out of line: the path is rare, and inlined it slowed the common one.
+// Warp-collective.
+struct MidState {
+  float m_used, l, rs0, rs1;
+  bool ok;
+};
+template <int D>
+__device__ __noinline__ MidState stage_second_half(uint32_t tS, uint32_t tOg, uint32_t al2,
+                                                    uint32_t al3, float sl2, float m_used,
+                                                    float l, float rs0, float rs1,
+                                                    uint64_t* p_empty, uint32_t parity, Abort ab,
+                                                    int32_t* status) {
+  const float ninf = -__int_as_float(0x7f800000);
+  float mx0 = ninf, mx1 = ninf;
+#pragma unroll 1
+  for (int cc = 2; cc < 4; ++cc) {
+    uint32_t v[32];
+    tmem_ld32(tS + cc * 32, v);
+    tmem_wait_ld();
+    const uint32_t am = cc == 2 ? al2 : al3;
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      mx0 = fmaxf(mx0, ((am >> e) & 1u) ? __uint_as_float(v[e]) : ninf);
+      mx1 = fmaxf(mx1, ((am >> (e + 1)) & 1u) ? __uint_as_float(v[e + 1]) : ninf);
+    }
+  }
+  const float mx = fmaxf(mx0, mx1) * sl2;
+  const bool raise = mx > m_used + kLazy;
+  const float f = raise ? ex2(m_used - mx) : 1.0f;
+  MidState r{m_used, l, rs0, rs1, false};
+  if (!__all_sync(FULL, mbar_wait(p_empty, parity, ab, status, 214))) return r;
+  tc_fence_after();
+#pragma unroll 1
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t ov[32];
+    tmem_ld32(tOg + cc * 32, ov);
+    tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+    tmem_st32(tOg + cc * 32, ov);
+  }
+  {
+    uint32_t pw[32];
+    tmem_ld32(tS, pw);
+    tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const float lo = __uint_as_float(pw[e] << 16);
+      const float hi = __uint_as_float(pw[e] & 0xffff0000u);
+      pw[e] = pack_bf16x2(lo * f, hi * f);
+    }
+    tmem_st32(tS, pw);
+  }
+  r.l = l * f;
+  r.rs0 = rs0 * f;
+  r.rs1 = rs1 * f;
+  if (raise) r.m_used = mx;
+  const float msub = r.m_used;
+  uint32_t v0[32], v1[32];
+  tmem_ld32(tS + 64, v0);
+  tmem_ld32(tS + 96, v1);
+  tmem_wait_ld();
+  uint32_t pk[32];
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const float p0 = ((al2 >> e) & 1u) ? ex2(fmaf(__uint_as_float(v0[e]), sl2, -msub)) : 0.0f;
+    const float p1 = ((al2 >> (e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v0[e + 1]), sl2, -msub)) : 0.0f;
+    const float p2 = ((al3 >> e) & 1u) ? ex2(fmaf(__uint_as_float(v1[e]), sl2, -msub)) : 0.0f;
+    const float p3 = ((al3 >> (e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v1[e + 1]), sl2, -msub)) : 0.0f;
+    r.rs0 += p0 + p2;
+    r.rs1 += p1 + p3;
+    pk[e >> 1] = pack_bf16x2(p0, p1);
+    pk[16 + (e >> 1)] = pack_bf16x2(p2, p3);
+  }
+  tmem_st32(tS + 32, pk);
+  tmem_wait_st();
+  r.ok = true;
+  return r;
 }
 
 // PK: the K/V blocks come from the block-packed copy (B >= 8: whole 8-row
@@ -708,11 +803,15 @@ __global__ void __launch_bounds__(384, 1)
       }
       // One pass when possible: p = 2^(s * scale * log2(e) - m_used) with the
       // running reference maximum, as long as no allowed key of the stage
-      // exceeds it by more than 2^8 (checked per 64 keys before their
-      // exponentials); otherwise the stage is redone in two passes below.
+      // exceeds it by more than 2^kLazy (checked per 64 keys before their
+      // exponentials).  When keys 0..63 exceed it the stage is done in two
+      // passes below; when only keys 64..127 do, the maximum is raised in place
+      // (stage_second_half), since P of keys 0..63 already lies over their S
+      // values.
       float rs0 = 0.0f, rs1 = 0.0f;
       bool fast = __all_sync(FULL, m_used != ninf || (al0 | al1 | al2 | al3) == 0u);
-      // Stages whose blocks are all historical (B >= 4) take the mask per
+      bool mid = false;  // keys 64..127 need a higher maximum: the path below
+      // Stages whose blocks are all historical (B >= 8) take the mask per
       // block: block maxima, and -m or -inf as the exponent's additive term.
       bool by_block = false;
       if constexpr (B >= 8) by_block = m.diag >= nb;
@@ -737,8 +836,12 @@ __global__ void __launch_bounds__(384, 1)
             cm = fmaxf(cm, al ? bm : ninf);
             cb[jj] = al ? -m_used : ninf;
           }
-          if (__any_sync(FULL, cm * sl2 > m_used + 8.0f)) {
-            fast = false;
+          if (__any_sync(FULL, cm * sl2 > m_used + kLazy)) {
+            if (hh == 0) {  // nothing written yet: the two passes below
+              fast = false;
+              break;
+            }
+            mid = true;
             break;
           }
           uint32_t pk[32];
@@ -766,8 +869,12 @@ __global__ void __launch_bounds__(384, 1)
             cm0 = fmaxf(cm0, ((a0 >> e) & 1u) ? __uint_as_float(v0[e]) : ninf);
             cm1 = fmaxf(cm1, ((a1 >> e) & 1u) ? __uint_as_float(v1[e]) : ninf);
           }
-          if (__any_sync(FULL, fmaxf(cm0, cm1) * sl2 > m_used + 8.0f)) {
-            fast = false;
+          if (__any_sync(FULL, fmaxf(cm0, cm1) * sl2 > m_used + kLazy)) {
+            if (hh == 0) {  // nothing written yet: the two passes below
+              fast = false;
+              break;
+            }
+            mid = true;
             break;
           }
           uint32_t pk[32];
@@ -785,6 +892,19 @@ __global__ void __launch_bounds__(384, 1)
             pk[16 + (e >> 1)] = pack_bf16x2(p2, p3);
           }
           tmem_st32(tS + hh * 32, pk);  // S columns 0..63 have been read by now
+        }
+      }
+      if (mid) {
+        const MidState ms2 = stage_second_half<D>(tS, tOg, al2, al3, sl2, m_used, l, rs0, rs1,
+                                                  &p_empty[grp], (uint32_t)(((i >> 1) - 1) & 1),
+                                                  ab, a.status);
+        m_used = ms2.m_used;
+        l = ms2.l;
+        rs0 = ms2.rs0;
+        rs1 = ms2.rs1;
+        if (!__all_sync(FULL, ms2.ok)) {
+          ok = false;
+          break;
         }
       }
       if (!fast) {
@@ -809,11 +929,11 @@ __global__ void __launch_bounds__(384, 1)
         }
         const float smax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
         // Raise the reference maximum when this stage exceeds it by more than
-        // 2^8.  O[grp] holds the group's earlier stages under the old maximum:
+        // 2^kLazy.  O[grp] holds the group's earlier stages under the old maximum:
         // it is rescaled once the group's previous PV product (stage i - 2) is
         // done; each warp takes that path together (rows that do not need it
         // scale by 1).
-        const bool raise = smax > m_used + 8.0f;
+        const bool raise = smax > m_used + kLazy;
         const bool rescale = raise && m_used != ninf;
         if (__any_sync(FULL, rescale)) {
           const bool w2 =

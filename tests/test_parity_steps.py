@@ -290,3 +290,48 @@ def test_sparse_attn_given_lists(s, name, mode):
     assert s.read_status(st)[0] == 0
     r3_check(O.float().cpu().numpy(), lse.cpu().numpy(), O64, lse64,
              lse_tol=lse_tol_for(wl, inp, rows))
+
+
+def test_sparse_attn_jump_in_second_half(s):
+    """A stage whose first 64 keys pass the one-pass check against the row's
+    reference maximum (15.5 above it in log2 units, within the 2^16 lazy
+    margin) while one of its last 64 keys exceeds it by 16.5: the maximum is
+    raised in place, O and the P already written for the first 64 keys are
+    rescaled, and those keys keep their weight (half the needle's each).  Keys
+    are exact multiples of one direction: every other selected key has the
+    logit L0 of the row's first stage (about 5).  The needle sits in the second
+    half of softmax group 0's second stage (union blocks 40-47 of stage 32-47),
+    the raised keys in its first half (blocks 32-39)."""
+    T, off, H, d, B = 16, 4096, 8, 128, 8
+    wl = BASE.replace(name="jump", seq_q=T, seq_kv=off + T, q_offset=off, n_q_heads=H,
+                      n_kv_heads=1, head_dim=d, block_size=B, topk_tokens=64 * B, tile_q=16)
+    a = b = 6.25  # logit of a selected key: a * b / sqrt(d) * log2(e) = 4.98
+    b_hi = 25.75  # blocks 32-39: 20.52, above L0 by 15.54
+    c = 27.0      # the needle: 21.52, above L0 by 16.54
+    Tkv = off + T
+    Qf = np.zeros((T, H, d), np.float32)
+    Qf[:, :, 0] = a
+    Kf = np.zeros((Tkv, 1, d), np.float32)
+    Kf[:, 0, 0] = -b                     # blocks 64 .. : never selected
+    Kf[: 64 * B, 0, 0] = b               # blocks 0 .. 63: the selection of every query
+    Kf[32 * B: 40 * B, 0, 0] = b_hi
+    Kf[44 * B + 3, 0, 0] = c
+    Vf = np.random.default_rng(7).normal(0.0, 1.0, (Tkv, 1, d)).astype(np.float32)
+    inp = {"workload": wl, "Q": synth.to_bf16_bits(Qf), "K": synth.to_bf16_bits(Kf),
+           "V": synth.to_bf16_bits(Vf)}
+    p = s.params_for(wl)
+    rows = np.arange(T)
+    Q, K, V = widened(inp)
+    S = oracle.scores(oracle.index_query(Q, 1, rows), oracle.merge_f64(K, B), B, off, rows)
+    sel = oracle.select(S, B, off, rows, 64)
+    assert (sel[0][:, :64] == np.arange(64)).all()  # the construction holds
+    uoff, ublk, umask = oracle.union(sel, wl.tile_q, wl.n_blocks)
+    O64, lse64 = oracle.sparse_attn(Q, K, V, off, B, sel, 0, (uoff, ublk, umask), wl.tile_q)
+    d_ = dev_inputs(inp)
+    O, lse = s.alloc_outputs(p)
+    ws = s.alloc_workspace(p, s.WS_SPARSE_ATTN)
+    st = s.new_status()
+    s.sgqa_sparse_attn_fwd(p, d_["Q"], d_["K"], d_["V"], *_upload_union(uoff, ublk, umask, 1, 0),
+                           O, lse, page_table=None, ws=ws, status=st)
+    assert s.read_status(st)[0] == 0
+    r3_check(O.float().cpu().numpy(), lse.cpu().numpy(), O64, lse64)
