@@ -362,68 +362,69 @@ __device__ __noinline__ MidState stage_second_half(uint32_t tS, uint32_t tOg, ui
                                                     uint64_t* p_empty, uint32_t parity, Abort ab,
                                                     int32_t* status) {
   const float ninf = -__int_as_float(0x7f800000);
-  float mx0 = ninf, mx1 = ninf;
+  float mx = ninf;
 #pragma unroll 1
-  for (int cc = 2; cc < 4; ++cc) {
-    uint32_t v[32];
-    tmem_ld32(tS + cc * 32, v);
+  for (int c = 0; c < 8; ++c) {  // keys 64 + 8 c ..
+    uint32_t v[8];
+    tmem_ld8(tS + 64 + 8 * c, v);
     tmem_wait_ld();
-    const uint32_t am = cc == 2 ? al2 : al3;
+    const uint32_t am = ((c < 4 ? al2 : al3) >> ((c & 3) * 8)) & 0xffu;
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      mx0 = fmaxf(mx0, ((am >> e) & 1u) ? __uint_as_float(v[e]) : ninf);
-      mx1 = fmaxf(mx1, ((am >> (e + 1)) & 1u) ? __uint_as_float(v[e + 1]) : ninf);
-    }
+    for (int e = 0; e < 8; ++e) mx = fmaxf(mx, ((am >> e) & 1u) ? __uint_as_float(v[e]) : ninf);
   }
-  const float mx = fmaxf(mx0, mx1) * sl2;
+  mx *= sl2;
   const bool raise = mx > m_used + kLazy;
   const float f = raise ? ex2(m_used - mx) : 1.0f;
   MidState r{m_used, l, rs0, rs1, false};
   if (!__all_sync(FULL, mbar_wait(p_empty, parity, ab, status, 214))) return r;
   tc_fence_after();
+  // O, then the P of keys 0..63 (columns 0..31, bf16 pairs), scaled by f
 #pragma unroll 1
-  for (int cc = 0; cc < D / 32; ++cc) {
-    uint32_t ov[32];
-    tmem_ld32(tOg + cc * 32, ov);
+  for (int c = 0; c < D / 8 + 4; ++c) {
+    const bool isO = c < D / 8;
+    const uint32_t ta = isO ? tOg + 8 * c : tS + 8 * (c - D / 8);
+    uint32_t v[8];
+    tmem_ld8(ta, v);
     tmem_wait_ld();
 #pragma unroll
-    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
-    tmem_st32(tOg + cc * 32, ov);
-  }
-  {
-    uint32_t pw[32];
-    tmem_ld32(tS, pw);
-    tmem_wait_ld();
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const float lo = __uint_as_float(pw[e] << 16);
-      const float hi = __uint_as_float(pw[e] & 0xffff0000u);
-      pw[e] = pack_bf16x2(lo * f, hi * f);
+    for (int e = 0; e < 8; ++e) {
+      if (isO) {
+        v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
+      } else {
+        const float lo = __uint_as_float(v[e] << 16);
+        const float hi = __uint_as_float(v[e] & 0xffff0000u);
+        v[e] = pack_bf16x2(lo * f, hi * f);
+      }
     }
-    tmem_st32(tS, pw);
+    tmem_st8(ta, v);
   }
   r.l = l * f;
   r.rs0 = rs0 * f;
   r.rs1 = rs1 * f;
   if (raise) r.m_used = mx;
   const float msub = r.m_used;
-  uint32_t v0[32], v1[32];
-  tmem_ld32(tS + 64, v0);
-  tmem_ld32(tS + 96, v1);
-  tmem_wait_ld();
-  uint32_t pk[32];
+  // P of keys 64..127 into columns 32..63, 16 keys (8 columns) at a time
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t v0[8], v1[8], pk[8];
+    tmem_ld8(tS + 64 + 16 * c, v0);
+    tmem_ld8(tS + 72 + 16 * c, v1);
+    tmem_wait_ld();
+    const uint32_t am = ((c < 2 ? al2 : al3) >> ((c & 1) * 16)) & 0xffffu;
 #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
-    const float p0 = ((al2 >> e) & 1u) ? ex2(fmaf(__uint_as_float(v0[e]), sl2, -msub)) : 0.0f;
-    const float p1 = ((al2 >> (e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v0[e + 1]), sl2, -msub)) : 0.0f;
-    const float p2 = ((al3 >> e) & 1u) ? ex2(fmaf(__uint_as_float(v1[e]), sl2, -msub)) : 0.0f;
-    const float p3 = ((al3 >> (e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v1[e + 1]), sl2, -msub)) : 0.0f;
-    r.rs0 += p0 + p2;
-    r.rs1 += p1 + p3;
-    pk[e >> 1] = pack_bf16x2(p0, p1);
-    pk[16 + (e >> 1)] = pack_bf16x2(p2, p3);
+    for (int e = 0; e < 8; e += 2) {
+      const float p0 = ((am >> e) & 1u) ? ex2(fmaf(__uint_as_float(v0[e]), sl2, -msub)) : 0.0f;
+      const float p1 = ((am >> (e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v0[e + 1]), sl2, -msub)) : 0.0f;
+      const float p2 = ((am >> (8 + e)) & 1u) ? ex2(fmaf(__uint_as_float(v1[e]), sl2, -msub)) : 0.0f;
+      const float p3 =
+          ((am >> (9 + e)) & 1u) ? ex2(fmaf(__uint_as_float(v1[e + 1]), sl2, -msub)) : 0.0f;
+      r.rs0 += p0 + p2;
+      r.rs1 += p1 + p3;
+      pk[e >> 1] = pack_bf16x2(p0, p1);
+      pk[4 + (e >> 1)] = pack_bf16x2(p2, p3);
+    }
+    tmem_st8(tS + 32 + 8 * c, pk);
   }
-  tmem_st32(tS + 32, pk);
   tmem_wait_st();
   r.ok = true;
   return r;
