@@ -176,10 +176,15 @@ SGQA_API int sgqa_topk_union(const sgqa_params* p, const float* scores, int32_t 
  * O in the dtype of Q; lse[h][t] = log of the softmax denominator, with the
  * maximum added back.  Runs on tcgen05 tensor cores (bf16 operands, fp32
  * accumulation and fp32 online softmax).  The workspace receives the staged
- * operands: fp32 inputs rounded to bf16, and for B >= 8 a block-packed copy
- * of K and V (each block contiguous, in the tensor cores' shared-memory
- * layout) that the kernel gathers with one bulk copy per block.  Union arrays
- * as written by sgqa_topk_union for all tiles of the call.  Workspace:
+ * operands: fp32 inputs rounded to bf16 (K and V, when gathered key by key,
+ * into a contiguous copy read through the page table), and for B >= 8, when
+ * the call selects at least as many blocks as the cache holds (seq_q * k / B
+ * >= nblk) or the inputs are fp32, a block-packed copy of K and V (each block
+ * contiguous, in the tensor cores' shared-memory layout) that the kernel
+ * gathers with one bulk copy per block.  Otherwise (B < 8, or a few queries
+ * over a long cache) keys are gathered four rows at a time straight from K
+ * and V; bf16 inputs then need no workspace.  Union arrays as written by
+ * sgqa_topk_union for all tiles of the call.  Workspace:
  * sgqa_workspace_bytes(p, SGQA_WS_SPARSE_ATTN). */
 SGQA_API int sgqa_sparse_attn_fwd(const sgqa_params* p, const void* Q, const void* K,
                                   const void* V, const int32_t* page_table,

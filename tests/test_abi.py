@@ -114,3 +114,26 @@ def test_topk_union_range_validation(s):
     assert f(*args(0, 70, 1 << 30)) == s.ERR_INVALID_ARG       # q_end not tile aligned nor T
     assert f(*args(0, 301, 1 << 30)) == s.ERR_INVALID_ARG
     assert f(*args(0, 64, 1)) == s.ERR_WORKSPACE               # union capacity too small
+
+
+def test_kv_packing_rule(s):
+    """K/V are block-packed (B >= 8) only when the call selects at least as
+    many blocks as the cache holds, or for fp32 inputs: a decode step over a
+    1M paged cache carves no packed copies, a chunk of 8192 queries does, and
+    the launch plan differs by exactly the two packing launches around the
+    threshold."""
+    big = dict(seq_kv=1 << 20, n_q_heads=64, n_kv_heads=8, head_dim=128, block_size=8,
+               topk_tokens=4096, tile_q=64, page_size=64)
+    packed = 2 * 8 * ((1 << 20) // 8 + 1) * 8 * 128 * 2  # K and V, one zero block per head
+    dec = s.params(seq_q=1, q_offset=(1 << 20) - 1, **big)
+    pre = s.params(seq_q=8192, q_offset=(1 << 20) - 8192, **big)
+    assert s.workspace_bytes(dec, s.WS_SPARSE_ATTN) < (1 << 20)
+    assert s.workspace_bytes(pre, s.WS_SPARSE_ATTN) >= packed
+    dec32 = s.params(seq_q=1, q_offset=(1 << 20) - 1, dtype=s.FP32, **big)
+    assert s.workspace_bytes(dec32, s.WS_SPARSE_ATTN) >= packed
+    # 516 blocks of 8; 16 selected per query: 32 queries select 512 < 516, 40 select 640
+    small = dict(n_q_heads=8, n_kv_heads=2, head_dim=128, block_size=8, topk_tokens=128,
+                 tile_q=64)
+    below = s.params(seq_q=32, seq_kv=4128, q_offset=4096, **small)
+    above = s.params(seq_q=40, seq_kv=4136, q_offset=4096, **small)
+    assert s.sgqa_prefill_plan(above)[1] - s.sgqa_prefill_plan(below)[1] == 2
