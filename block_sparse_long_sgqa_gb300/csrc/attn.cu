@@ -362,6 +362,7 @@ __device__ __noinline__ MidState stage_second_half(uint32_t tS, uint32_t tOg, ui
                                                     uint64_t* p_empty, uint32_t parity, Abort ab,
                                                     int32_t* status) {
   const float ninf = -__int_as_float(0x7f800000);
+  tmem_wait_st();  // the P of keys 0..63 is read back below
   float mx = ninf;
 #pragma unroll 1
   for (int c = 0; c < 8; ++c) {  // keys 64 + 8 c ..
