@@ -52,6 +52,8 @@ def _load():
     lib.orc_sparse_attn.argtypes = [vp, vp, vp, i64, i64, i64, i32, i32, i32, i32, i32, vp, i64,
                                     vp, vp, i32, f64, vp, i64, vp, vp]
     lib.orc_dense_attn.argtypes = [vp, vp, vp, i64, i64, i64, i32, i32, i32, f64, vp, i64, vp, vp]
+    lib.orc_sparse_attn_bwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, i32, i32,
+                                        vp, i64, vp, vp, i32, f64, vp, i64, vp, vp, vp]
     _lib = lib
     return lib
 
@@ -172,6 +174,36 @@ def sparse_attn(Q, K, V, q_offset: int, B: int, sel: Optional[np.ndarray], mode:
                                    _p(sel), Ks, _p(uoff), _p(ublk), W, scale, _p(r), len(r),
                                    _p(O), _p(lse)), "sparse_attn")
     return O, lse
+
+
+def sparse_attn_bwd(Q, K, V, dO, q_offset: int, B: int, sel: Optional[np.ndarray], mode: int = 0,
+                    union_csr=None, W: int = 64, scale: Optional[float] = None, rows=None):
+    """Gradients of L = sum(dO * O) for the attention of sparse_attn (same
+    arguments; dO [nrows][H][d]).  Returns dQ [nrows][H][d], dK and dV
+    [Tkv][Hkv][d] (fp64)."""
+    Q, K, V = _f32(Q), _f32(K), _f32(V)
+    T, H, d = Q.shape
+    Tkv, Hkv, _ = K.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    r = _rows(rows, T)
+    dO = np.ascontiguousarray(dO, np.float64)
+    assert dO.shape == (len(r), H, d)
+    if sel is None:
+        sel = np.full((Hkv, T, 1), -1, np.int32)
+    sel = np.ascontiguousarray(sel, np.int32)
+    Ks = sel.shape[2]
+    uoff = ublk = None
+    if mode == 1:
+        uoff, ublk, _ = union_csr if union_csr is not None else union(sel, W, Tkv // B)
+        uoff = np.ascontiguousarray(uoff, np.int32)
+        ublk = np.ascontiguousarray(ublk, np.int32)
+    dQ = np.empty((len(r), H, d), np.float64)
+    dK = np.empty((Tkv, Hkv, d), np.float64)
+    dV = np.empty((Tkv, Hkv, d), np.float64)
+    _check(_load().orc_sparse_attn_bwd(_p(Q), _p(K), _p(V), _p(dO), T, Tkv, q_offset, H, Hkv, d,
+                                       B, mode, _p(sel), Ks, _p(uoff), _p(ublk), W, scale, _p(r),
+                                       len(r), _p(dQ), _p(dK), _p(dV)), "sparse_attn_bwd")
+    return dQ, dK, dV
 
 
 def dense_attn(Q, K, V, q_offset: int, scale: Optional[float] = None, rows=None):

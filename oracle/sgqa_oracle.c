@@ -273,14 +273,42 @@ int64_t orc_union(const int32_t* sel, int64_t T, int Hkv, int64_t Ks, int W, int
  * sel [Hkv][T][Ks] (mode A) or the union CSR of orc_union (mode B).
  * Outputs: O [nrows][H][d] and lse [H][nrows], fp64.
  * ------------------------------------------------------------------------- */
-static void attend_row(const float* Q, const float* K, const float* V, int64_t t, int h, int g,
-                       int H, int Hkv, int d, int B, int64_t pos, const int32_t* blocks,
-                       int64_t nblocks, double scale, double* z, int64_t* ps, double* o,
-                       double* lse) {
+/* The allowed positions of a row: every position of its historical blocks,
+ * then its own block up to pos.  Returns their number. */
+static int64_t row_positions(int B, int64_t pos, const int32_t* blocks, int64_t nblocks,
+                             int64_t* ps) {
   int64_t n = 0;
   for (int64_t x = 0; x < nblocks; ++x)
     for (int r = 0; r < B; ++r) ps[n++] = (int64_t)blocks[x] * B + r;
   for (int64_t p = (pos / B) * B; p <= pos; ++p) ps[n++] = p;
+  return n;
+}
+
+/* The historical blocks a row attends: its selection (mode A), or its tile's
+ * union blocks before its own block (mode B).  Returns their number. */
+static int64_t row_blocks(int mode, int64_t T, int g, int64_t t, int64_t cur,
+                          const int32_t* sel, int64_t Ks, const int32_t* uoff,
+                          const int32_t* ublk, int W, int64_t ntiles, int32_t* blocks) {
+  int64_t nb = 0;
+  if (mode == 0) {
+    const int32_t* s = sel + ((int64_t)g * T + t) * Ks;
+    for (int64_t x = 0; x < Ks; ++x)
+      if (s[x] >= 0) blocks[nb++] = s[x];
+  } else {
+    const int64_t tau = t / W;
+    const int64_t a = uoff[(int64_t)g * (ntiles + 1) + tau];
+    const int64_t b = uoff[(int64_t)g * (ntiles + 1) + tau + 1];
+    for (int64_t x = a; x < b; ++x)
+      if (ublk[x] < cur) blocks[nb++] = ublk[x];
+  }
+  return nb;
+}
+
+static void attend_row(const float* Q, const float* K, const float* V, int64_t t, int h, int g,
+                       int H, int Hkv, int d, int B, int64_t pos, const int32_t* blocks,
+                       int64_t nblocks, double scale, double* z, int64_t* ps, double* o,
+                       double* lse) {
+  const int64_t n = row_positions(B, pos, blocks, nblocks, ps);
   const float* q = Q + (t * H + h) * (int64_t)d;
   double mx = NEG_INF;
   for (int64_t a = 0; a < n; ++a) {
@@ -335,18 +363,7 @@ int orc_sparse_attn(const float* Q, const float* K, const float* V, int64_t T, i
       const int64_t r = rh / H;
       const int h = (int)(rh % H), g = h / G;
       const int64_t t = rows[r], pos = q_offset + t, cur = pos / B;
-      int64_t nb = 0;
-      if (mode == 0) {
-        const int32_t* s = sel + ((int64_t)g * T + t) * Ks;
-        for (int64_t x = 0; x < Ks; ++x)
-          if (s[x] >= 0) blocks[nb++] = s[x];
-      } else {
-        const int64_t tau = t / W;
-        const int64_t a = uoff[(int64_t)g * (ntiles + 1) + tau];
-        const int64_t b = uoff[(int64_t)g * (ntiles + 1) + tau + 1];
-        for (int64_t x = a; x < b; ++x)
-          if (ublk[x] < cur) blocks[nb++] = ublk[x];
-      }
+      const int64_t nb = row_blocks(mode, T, g, t, cur, sel, Ks, uoff, ublk, W, ntiles, blocks);
       double l;
       attend_row(Q, K, V, t, h, g, H, Hkv, d, B, pos, blocks, nb, scale, z, ps,
                  O + (r * H + h) * (int64_t)d, &l);
@@ -358,6 +375,99 @@ int orc_sparse_attn(const float* Q, const float* K, const float* V, int64_t T, i
     free(o);
   }
   (void)Tkv;
+  return err;
+}
+
+/* ---------------------------------------------------------------------------
+ * Backward of step 6 (the training side of the same layer: the pages apply
+ * the sparse attention in training and inference alike, section Sparse GQA;
+ * they give no backward, so this is the derivative of orc_sparse_attn written
+ * out).  For the loss L = sum over the given rows and heads of dO . O, with
+ * P_p = e^{z_p - lse} over the row's allowed positions (as in orc_sparse_attn):
+ *   dV[p][g] += P_p dO
+ *   dz_p      = P_p (dO . V[p][g] - dO . O)
+ *   dQ[t][h]  = scale * sum_p dz_p K[p][g]
+ *   dK[p][g] += scale * dz_p Q[t][h]
+ * dO [nrows][H][d] and dQ [nrows][H][d]; dK and dV [Tkv][Hkv][d] are zeroed
+ * here and accumulated over the rows (serially: rows share keys).
+ * ------------------------------------------------------------------------- */
+int orc_sparse_attn_bwd(const float* Q, const float* K, const float* V, const double* dO,
+                        int64_t T, int64_t Tkv, int64_t q_offset, int H, int Hkv, int d, int B,
+                        int mode, const int32_t* sel, int64_t Ks, const int32_t* uoff,
+                        const int32_t* ublk, int W, double scale, const int32_t* rows,
+                        int64_t nrows, double* dQ, double* dK, double* dV) {
+  if (Hkv < 1 || H % Hkv) return -1;
+  const int G = H / Hkv;
+  const int64_t ntiles = (T + W - 1) / W;
+  int64_t maxk = Ks;
+  if (mode == 1) {
+    for (int64_t x = 0; x < Hkv * (ntiles + 1) - 1; ++x) {
+      int64_t len = (int64_t)uoff[x + 1] - uoff[x];
+      if (len > maxk) maxk = len;
+    }
+  }
+  const int64_t cap = maxk * B + B;
+  double* z = (double*)malloc(sizeof(double) * (size_t)cap);
+  double* pr = (double*)malloc(sizeof(double) * (size_t)cap);
+  int64_t* ps = (int64_t*)malloc(sizeof(int64_t) * (size_t)cap);
+  int32_t* blocks = (int32_t*)malloc(sizeof(int32_t) * (size_t)(maxk > 0 ? maxk : 1));
+  double* o = (double*)malloc(sizeof(double) * (size_t)d);
+  int err = (!z || !pr || !ps || !blocks || !o) ? -2 : 0;
+  const int64_t nkv = Tkv * Hkv * (int64_t)d;
+  for (int64_t x = 0; x < nkv && !err; ++x) {
+    dK[x] = 0.0;
+    dV[x] = 0.0;
+  }
+  for (int64_t rh = 0; rh < nrows * H && !err; ++rh) {
+    const int64_t r = rh / H;
+    const int h = (int)(rh % H), g = h / G;
+    const int64_t t = rows[r], pos = q_offset + t, cur = pos / B;
+    const int64_t nb = row_blocks(mode, T, g, t, cur, sel, Ks, uoff, ublk, W, ntiles, blocks);
+    const int64_t n = row_positions(B, pos, blocks, nb, ps);
+    const float* q = Q + (t * H + h) * (int64_t)d;
+    const double* go = dO + (r * H + h) * (int64_t)d;
+    double mx = NEG_INF;
+    for (int64_t a = 0; a < n; ++a) {
+      const float* k = K + (ps[a] * Hkv + g) * (int64_t)d;
+      double s = 0.0;
+      for (int i = 0; i < d; ++i) s += (double)q[i] * (double)k[i];
+      z[a] = scale * s;
+      if (z[a] > mx) mx = z[a];
+    }
+    double l = 0.0;
+    for (int64_t a = 0; a < n; ++a) {
+      pr[a] = exp(z[a] - mx);
+      l += pr[a];
+    }
+    for (int i = 0; i < d; ++i) o[i] = 0.0;
+    for (int64_t a = 0; a < n; ++a) {
+      pr[a] /= l;
+      const float* v = V + (ps[a] * Hkv + g) * (int64_t)d;
+      for (int i = 0; i < d; ++i) o[i] += pr[a] * (double)v[i];
+    }
+    double dOO = 0.0;  /* dO . O */
+    for (int i = 0; i < d; ++i) dOO += go[i] * o[i];
+    double* gq = dQ + (r * H + h) * (int64_t)d;
+    for (int i = 0; i < d; ++i) gq[i] = 0.0;
+    for (int64_t a = 0; a < n; ++a) {
+      const int64_t kv = (ps[a] * Hkv + g) * (int64_t)d;
+      const float* k = K + kv;
+      const float* v = V + kv;
+      double dP = 0.0;
+      for (int i = 0; i < d; ++i) dP += go[i] * (double)v[i];
+      const double dz = pr[a] * (dP - dOO);
+      for (int i = 0; i < d; ++i) {
+        dV[kv + i] += pr[a] * go[i];
+        gq[i] += scale * dz * (double)k[i];
+        dK[kv + i] += scale * dz * (double)q[i];
+      }
+    }
+  }
+  free(z);
+  free(pr);
+  free(ps);
+  free(blocks);
+  free(o);
   return err;
 }
 

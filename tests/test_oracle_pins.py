@@ -342,3 +342,97 @@ def test_synth_workload_small():
     wl = synth.WORKLOADS["step5_128k"].replace(seq_q=512, seq_kv=512)
     inp = synth.make_inputs(wl)
     assert inp["needles"].shape == (8, 8, 16)
+
+
+# ------------------------------------------------------ attention backward (training side)
+
+def _grid(seed, *shape):
+    """Values on a 2^-6 grid in [-1, 1]: x +- 2^-10 is exact in fp32."""
+    return (np.random.default_rng(seed).integers(-64, 65, shape) / 64.0).astype(np.float32)
+
+
+def _rand_sel(seed, Hkv, T, off, B, Ks):
+    """A valid selection: per (group, query) min(Ks, nh) distinct historical
+    blocks, ascending, -1 padded."""
+    rng = np.random.default_rng(seed)
+    sel = np.full((Hkv, T, Ks), -1, np.int32)
+    for g in range(Hkv):
+        for t in range(T):
+            nh = (off + t) // B
+            k = min(Ks, nh)
+            if k:
+                sel[g, t, :k] = np.sort(rng.choice(nh, size=k, replace=False))
+    return sel
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_attn_bwd_finite_differences(mode):
+    """The attention backward against central differences of L = sum(dO * O)
+    through the forward oracle, on entries of Q, K and V (modes A and B)."""
+    T, H, Hkv, d, B, off, Ks, W = 6, 4, 2, 8, 2, 6, 2, 4
+    Q, K, V = _grid(30, T, H, d), _grid(31, off + T, Hkv, d), _grid(32, off + T, Hkv, d)
+    sel = _rand_sel(33, Hkv, T, off, B, Ks)
+    dO = np.random.default_rng(34).standard_normal((T, H, d))
+    dQ, dK, dV = oracle.sparse_attn_bwd(Q, K, V, dO, off, B, sel, mode=mode, W=W)
+
+    def loss(X, which):
+        args = {"Q": (X, K, V), "K": (Q, X, V), "V": (Q, K, X)}[which]
+        O, _ = oracle.sparse_attn(*args, off, B, sel, mode=mode, W=W)
+        return float((dO * O).sum())
+
+    eps = 2.0 ** -10
+    rng = np.random.default_rng(35)
+    for which, X, grad in (("Q", Q, dQ), ("K", K, dK), ("V", V, dV)):
+        for _ in range(8):
+            idx = tuple(int(rng.integers(0, n)) for n in X.shape)
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += eps
+            Xm[idx] -= eps
+            fd = (loss(Xp, which) - loss(Xm, which)) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-7 + 1e-6 * abs(fd), (which, idx, fd, grad[idx])
+
+
+def test_attn_bwd_full_selection_vs_autograd():
+    """With every historical block selected, the backward is that of dense
+    causal GQA attention: torch autograd in fp64."""
+    T, H, Hkv, d, B, off = 20, 4, 2, 8, 4, 12
+    Q, K, V = rnd(36, T, H, d), rnd(37, off + T, Hkv, d), rnd(38, off + T, Hkv, d)
+    nblk = (off + T) // B
+    sel = np.full((Hkv, T, nblk), -1, np.int32)
+    for t in range(T):
+        nh = (off + t) // B
+        sel[:, t, :nh] = np.arange(nh)
+    dO = np.random.default_rng(39).standard_normal((T, H, d))
+    dQ, dK, dV = oracle.sparse_attn_bwd(Q, K, V, dO, off, B, sel)
+    q, k, v = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (Q, K, V))
+    G, scale = H // Hkv, 1.0 / math.sqrt(d)
+    pos = off + torch.arange(T)
+    allowed = torch.arange(off + T)[None, :] <= pos[:, None]
+    outs = []
+    for h in range(H):
+        s = scale * q[:, h] @ k[:, h // G].T
+        outs.append(torch.softmax(s.masked_fill(~allowed, float("-inf")), -1) @ v[:, h // G])
+    (torch.stack(outs, 1) * torch.tensor(dO)).sum().backward()
+    np.testing.assert_allclose(dQ, q.grad.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dK, k.grad.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dV, v.grad.numpy(), rtol=0, atol=1e-11)
+
+
+def test_attn_bwd_invariants():
+    """Each row's weights sum to one and its score gradients to zero: the sum
+    of dV over a group's keys is the sum of dO over the group's query heads,
+    the sum of dK over them is zero, and dQ does not change when one vector is
+    added to every key."""
+    T, H, Hkv, d, B, off, Ks = 16, 4, 2, 8, 2, 10, 3
+    Q, K, V = _grid(40, T, H, d), _grid(41, off + T, Hkv, d), _grid(42, off + T, Hkv, d)
+    sel = _rand_sel(43, Hkv, T, off, B, Ks)
+    dO = np.random.default_rng(44).standard_normal((T, H, d))
+    dQ, dK, dV = oracle.sparse_attn_bwd(Q, K, V, dO, off, B, sel)
+    G = H // Hkv
+    for g in range(Hkv):
+        np.testing.assert_allclose(dV[:, g].sum(0), dO[:, g * G:(g + 1) * G].sum((0, 1)),
+                                   rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dK[:, g].sum(0), 0.0, rtol=0, atol=1e-12)
+    c = _grid(45, d)
+    dQ2, _, _ = oracle.sparse_attn_bwd(Q, K + c[None, None, :], V, dO, off, B, sel)
+    np.testing.assert_allclose(dQ2, dQ, rtol=0, atol=1e-11)
