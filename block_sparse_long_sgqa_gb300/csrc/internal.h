@@ -148,7 +148,9 @@ int launch_topk_union(const Dims& dm, const float* scores, int64_t q_begin, int6
                       uint64_t* union_mask, int64_t union_cap, int32_t* status, cudaStream_t st);
 
 // Attention over the tiles [tau_begin, tau_end) of the call.  Q/K/V are bf16;
-// for B >= 8, Kp/Vp are their block-packed copies (launch_kv_pack).
+// Kp/Vp are their block-packed copies (launch_kv_pack, B >= 8) or null, in
+// which case keys are gathered from K/V (contiguous, or paged through
+// page_table).
 int launch_sparse_attn(const Dims& dm, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                        const __nv_bfloat16* V, const __nv_bfloat16* Kp, const __nv_bfloat16* Vp,
                        const int32_t* page_table, const int64_t* union_off,
