@@ -296,6 +296,50 @@ def test_mode_b_contains_mode_a_and_w1_equal():
     assert (lseB > lseA + 1e-9).any()
 
 
+@pytest.mark.parametrize("B,W,off", [(2, 8, 5), (4, 16, 0), (1, 4, 3)])
+def test_mode_b_allowed_set_vs_masked_sdpa(B, W, off):
+    """Mode B's key set, written out by hand: every block of the query's tile
+    union that lies strictly before the query's own block, plus the causal
+    part of that block.  The selections are built so that later tile-mates
+    select the earlier queries' current block and blocks past it (which mode B
+    must hide from them), so dropping the cut or letting the current block in
+    as a historical one changes the result."""
+    T, H, Hkv, d, Ks = 48, 4, 2, 16, 3
+    Q, K, V = rnd(31 + B, T, H, d), rnd(32 + B, off + T, Hkv, d), rnd(33 + B, off + T, Hkv, d)
+    rng = np.random.default_rng(34 + B)
+    sel = np.full((Hkv, T, Ks), -1, np.int32)
+    for g in range(Hkv):
+        for t in range(T):
+            nh = (off + t) // B
+            if nh == 0:
+                continue
+            # the most recent historical block, plus a few older ones
+            older = rng.choice(nh - 1, size=min(Ks - 1, nh - 1), replace=False) if nh > 1 else []
+            sel[g, t, :len(older) + 1] = sorted(list(older) + [nh - 1])
+    # the hand-built allowed mask of mode B
+    G = H // Hkv
+    allowed = np.zeros((H, T, off + T), bool)
+    n_cur = n_future = 0
+    for g in range(Hkv):
+        for t in range(T):
+            tau = t // W
+            mates = range(tau * W, min(tau * W + W, T))
+            union = {int(j) for m in mates for j in sel[g, m] if j >= 0}
+            cur = (off + t) // B
+            n_cur += cur in union
+            n_future += any(j > cur for j in union)
+            for h in range(g * G, (g + 1) * G):
+                for j in union:
+                    if j < cur:
+                        allowed[h, t, j * B:(j + 1) * B] = True
+                allowed[h, t, cur * B:off + t + 1] = True
+    assert n_cur > 0 and n_future > 0  # both branches of the cut are exercised
+    O, lse = oracle.sparse_attn(Q, K, V, off, B, sel, mode=1, W=W)
+    Or, lser = _sdpa_ref(Q, K, V, off, allowed)
+    np.testing.assert_allclose(O, Or, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lser, rtol=0, atol=1e-12)
+
+
 def test_coverage_monotone_in_k():
     """Selections are nested in k (one total order), so the attention mass they
     cover, exp(lse_sparse - lse_dense), never decreases with k and reaches 1."""
