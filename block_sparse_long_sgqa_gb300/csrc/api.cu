@@ -55,7 +55,7 @@ int derive(const sgqa_params* p, Dims* dm) {
     return SGQA_ERR_INVALID_ARG;
   if (!(p->softmax_scale >= 0.0f) || !std::isfinite(p->softmax_scale))
     return SGQA_ERR_INVALID_ARG;
-  if (p->page_size < 0) return SGQA_ERR_INVALID_ARG;
+  if (p->page_size < 0 || p->batch < 0) return SGQA_ERR_INVALID_ARG;
   const int B = p->block_size;
   if (B != 1 && B != 2 && B != 4 && B != 8 && B != 16) return SGQA_ERR_UNSUPPORTED;
   if (p->head_dim != 64 && p->head_dim != 128) return SGQA_ERR_UNSUPPORTED;
@@ -79,6 +79,7 @@ int derive(const sgqa_params* p, Dims* dm) {
   dm->mode = p->union_mode;
   dm->scale = p->softmax_scale > 0.0f ? p->softmax_scale : 1.0f / std::sqrt((float)p->head_dim);
   dm->elem = p->dtype == SGQA_BF16 ? 2 : 4;
+  dm->batch = p->batch > 1 ? p->batch : 1;
   return SGQA_OK;
 }
 
@@ -271,6 +272,38 @@ PrefillWs carve_prefill(Carve& c, const Dims& dm) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA; }
 
+// Element strides between consecutive sequences of a batched call (the
+// batch layout of include/sgqa.h).  A paged cache shares its page pool, so
+// only the page table moves.
+struct SeqStride {
+  int64_t q_bytes;    // Q and O
+  int64_t kv_bytes;   // contiguous K and V (0 when paged)
+  int64_t pt;         // page-table entries
+  int64_t kbar;       // Kbar floats
+  int64_t lse;        // lse floats
+  int64_t tiles;      // union_off / union_len entries
+};
+SeqStride seq_stride(const Dims& dm) {
+  SeqStride s;
+  s.q_bytes = dm.T * dm.H * dm.d * dm.elem;
+  s.kv_bytes = dm.ps > 0 ? 0 : dm.Tkv * dm.Hkv * dm.d * dm.elem;
+  s.pt = dm.ps > 0 ? (dm.Tkv + dm.ps - 1) / dm.ps : 0;
+  s.kbar = (int64_t)dm.Hkv * dm.nblk * dm.d;
+  s.lse = (int64_t)dm.H * dm.T;
+  s.tiles = (int64_t)dm.Hkv * dm.ntiles;
+  return s;
+}
+template <typename T>
+inline T* at_b(T* p, int64_t b, int64_t stride) {
+  return p == nullptr ? nullptr : p + b * stride;
+}
+inline const void* at_bytes(const void* p, int64_t b, int64_t stride) {
+  return p == nullptr ? nullptr : static_cast<const uint8_t*>(p) + b * stride;
+}
+inline void* at_bytes(void* p, int64_t b, int64_t stride) {
+  return p == nullptr ? nullptr : static_cast<uint8_t*>(p) + b * stride;
+}
+
 // Attention operands: fp32 inputs rounded to bf16, and with use_pack the
 // block-packed K/V.  Sets q/k/v to the buffers the attention kernel reads and
 // `ad` to the dims it reads them with: fp32 K/V that are gathered key by key
@@ -344,7 +377,7 @@ SGQA_API size_t sgqa_workspace_bytes(const sgqa_params* p, int which) {
 SGQA_API int64_t sgqa_union_capacity(const sgqa_params* p) {
   Dims dm;
   if (derive(p, &dm) != SGQA_OK) return -1;
-  return group_cap(dm) * dm.Hkv;
+  return group_cap(dm) * dm.Hkv * dm.batch;
 }
 
 static void* align_ws(void* ws) {
@@ -363,8 +396,15 @@ SGQA_API int sgqa_block_merge(const sgqa_params* p, const void* K, const int32_t
     return SGQA_ERR_INVALID_ARG;
   if (!aligned16(K) || !aligned16(Kbar)) return SGQA_ERR_ALIGNMENT;
   (void)status;
-  return cuda_rc(launch_block_merge(dm, K, page_table, blk_begin, blk_end, Kbar, nullptr, nullptr,
-                                    reinterpret_cast<cudaStream_t>(stream)));
+  const SeqStride ss = seq_stride(dm);
+  for (int64_t b = 0; b < dm.batch; ++b) {
+    const cudaError_t e = launch_block_merge(dm, at_bytes(K, b, ss.kv_bytes),
+                                             at_b(page_table, b, ss.pt), blk_begin, blk_end,
+                                             at_b(Kbar, b, ss.kbar), nullptr, nullptr,
+                                             reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return SGQA_ERR_CUDA;
+  }
+  return SGQA_OK;
 }
 
 SGQA_API int sgqa_index_scores(const sgqa_params* p, const void* Q, const float* Kbar,
@@ -383,11 +423,18 @@ SGQA_API int sgqa_index_scores(const sgqa_params* p, const void* Q, const float*
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   Carve c(align_ws(ws));
   IndexWs w = carve_index(c, dm, q_end - q_begin);
-  cudaError_t e = launch_split_kbar(dm, Kbar, w.khi, w.klo, st);
-  if (e == cudaSuccess) e = launch_index_query(dm, Q, q_begin, q_end, w.qhi, w.qlo, st);
-  if (e != cudaSuccess) return SGQA_ERR_CUDA;
-  return launch_index_scores(dm, w.qhi, w.qlo, w.khi, w.klo, q_begin, q_end, scores, true,
-                             status, st);
+  const SeqStride ss = seq_stride(dm);
+  const int64_t sc_stride = (int64_t)dm.Hkv * (q_end - q_begin) * dm.nblk;
+  for (int64_t b = 0; b < dm.batch; ++b) {
+    cudaError_t e = launch_split_kbar(dm, at_b(Kbar, b, ss.kbar), w.khi, w.klo, st);
+    if (e == cudaSuccess)
+      e = launch_index_query(dm, at_bytes(Q, b, ss.q_bytes), q_begin, q_end, w.qhi, w.qlo, st);
+    if (e != cudaSuccess) return SGQA_ERR_CUDA;
+    rc = launch_index_scores(dm, w.qhi, w.qlo, w.khi, w.klo, q_begin, q_end,
+                             at_b(scores, b, sc_stride), true, status, st);
+    if (rc != SGQA_OK) return rc;
+  }
+  return SGQA_OK;
 }
 
 SGQA_API int sgqa_topk_union(const sgqa_params* p, const float* scores, int32_t q_begin,
@@ -406,14 +453,24 @@ SGQA_API int sgqa_topk_union(const sgqa_params* p, const float* scores, int32_t 
     return SGQA_ERR_INVALID_ARG;
   if (scores && !aligned16(scores)) return SGQA_ERR_ALIGNMENT;
   if (union_cap < sgqa_union_capacity(p)) return SGQA_ERR_WORKSPACE;
-  int32_t* sel = topk_idx;
-  if (sel == nullptr) {
-    if (ws == nullptr || ws_bytes < sgqa_workspace_bytes(p, SGQA_WS_TOPK_UNION))
-      return SGQA_ERR_WORKSPACE;
-    sel = static_cast<int32_t*>(align_ws(ws));
+  if (topk_idx == nullptr &&
+      (ws == nullptr || ws_bytes < sgqa_workspace_bytes(p, SGQA_WS_TOPK_UNION)))
+    return SGQA_ERR_WORKSPACE;
+  const SeqStride ss = seq_stride(dm);
+  const int64_t nq = q_end - q_begin;
+  const int64_t sc_stride = (int64_t)dm.Hkv * nq * dm.nblk;
+  const int64_t sel_stride = (int64_t)dm.Hkv * nq * dm.Ks;
+  // the union slots of one sequence (sgqa_union_capacity / batch)
+  const int64_t ucap_b = group_cap(dm) * dm.Hkv;
+  for (int64_t b = 0; b < dm.batch; ++b) {
+    int32_t* sel = topk_idx ? topk_idx + b * sel_stride : static_cast<int32_t*>(align_ws(ws));
+    rc = launch_topk_union(dm, at_b(scores, b, sc_stride), q_begin, q_end, sel,
+                           union_off + b * ss.tiles, union_len + b * ss.tiles,
+                           union_blk + b * ucap_b, union_mask + b * ucap_b, ucap_b, status,
+                           reinterpret_cast<cudaStream_t>(stream));
+    if (rc != SGQA_OK) return rc;
   }
-  return launch_topk_union(dm, scores, q_begin, q_end, sel, union_off, union_len, union_blk,
-                           union_mask, union_cap, status, reinterpret_cast<cudaStream_t>(stream));
+  return SGQA_OK;
 }
 
 SGQA_API int sgqa_sparse_attn_fwd(const sgqa_params* p, const void* Q, const void* K,
@@ -437,30 +494,33 @@ SGQA_API int sgqa_sparse_attn_fwd(const sgqa_params* p, const void* Q, const voi
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   Carve c(align_ws(ws));
   AttnWs w = carve_attn(c, dm);
-  const __nv_bfloat16 *q, *k, *v;
-  Dims ad;
-  if (stage_attn(dm, Q, K, V, page_table, w, &q, &k, &v, &ad, st) != cudaSuccess)
-    return SGQA_ERR_CUDA;
-  return launch_sparse_attn(ad, q, k, v, w.Kp, w.Vp, ad.ps > 0 ? page_table : nullptr, union_off,
-                            union_len, union_blk, union_mask, O, lse, 0, dm.ntiles, status, st);
+  const SeqStride ss = seq_stride(dm);
+  // the union slots of one sequence: its groups' capacity (sgqa_union_capacity / batch)
+  const int64_t ucap_b = group_cap(dm) * dm.Hkv;
+  for (int64_t b = 0; b < dm.batch; ++b) {
+    const __nv_bfloat16 *q, *k, *v;
+    Dims ad;
+    const int32_t* pt = at_b(page_table, b, ss.pt);
+    if (stage_attn(dm, at_bytes(Q, b, ss.q_bytes), at_bytes(K, b, ss.kv_bytes),
+                   at_bytes(V, b, ss.kv_bytes), pt, w, &q, &k, &v, &ad, st) != cudaSuccess)
+      return SGQA_ERR_CUDA;
+    rc = launch_sparse_attn(ad, q, k, v, w.Kp, w.Vp, ad.ps > 0 ? pt : nullptr,
+                            union_off + b * ss.tiles, union_len + b * ss.tiles,
+                            union_blk + b * ucap_b, union_mask + b * ucap_b,
+                            at_bytes(O, b, ss.q_bytes), lse + b * ss.lse, 0, dm.ntiles, status,
+                            st);
+    if (rc != SGQA_OK) return rc;
+  }
+  return SGQA_OK;
 }
 
-SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, const void* V,
-                          const int32_t* page_table, float* Kbar, int32_t kbar_valid_blocks,
-                          void* O, float* lse, void* ws, size_t ws_bytes, int32_t* status,
-                          sgqa_stream_t stream) {
-  Dims dm;
-  int rc = derive(p, &dm);
-  if (rc != SGQA_OK) return rc;
-  if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr || lse == nullptr ||
-      Kbar == nullptr || kbar_valid_blocks < 0 || kbar_valid_blocks > dm.nblk ||
-      ((dm.ps > 0) != (page_table != nullptr)))
-    return SGQA_ERR_INVALID_ARG;
-  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(Kbar))
-    return SGQA_ERR_ALIGNMENT;
-  if (ws == nullptr || ws_bytes < sgqa_workspace_bytes(p, SGQA_WS_PREFILL))
-    return SGQA_ERR_WORKSPACE;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+namespace {
+
+// One sequence of sgqa_prefill (arguments validated by the caller).
+int prefill_one(const Dims& dm, const void* Q, const void* K, const void* V,
+                const int32_t* page_table, float* Kbar, int32_t kbar_valid_blocks, void* O,
+                float* lse, void* ws, int32_t* status, cudaStream_t st) {
+  int rc = SGQA_OK;
   Carve c(align_ws(ws));
   PrefillWs w = carve_prefill(c, dm);
 
@@ -531,6 +591,35 @@ SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, co
   return SGQA_OK;
 }
 
+}  // namespace
+
+SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, const void* V,
+                          const int32_t* page_table, float* Kbar, int32_t kbar_valid_blocks,
+                          void* O, float* lse, void* ws, size_t ws_bytes, int32_t* status,
+                          sgqa_stream_t stream) {
+  Dims dm;
+  int rc = derive(p, &dm);
+  if (rc != SGQA_OK) return rc;
+  if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr || lse == nullptr ||
+      Kbar == nullptr || kbar_valid_blocks < 0 || kbar_valid_blocks > dm.nblk ||
+      ((dm.ps > 0) != (page_table != nullptr)))
+    return SGQA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(Kbar))
+    return SGQA_ERR_ALIGNMENT;
+  if (ws == nullptr || ws_bytes < sgqa_workspace_bytes(p, SGQA_WS_PREFILL))
+    return SGQA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const SeqStride ss = seq_stride(dm);
+  for (int64_t b = 0; b < dm.batch; ++b) {
+    rc = prefill_one(dm, at_bytes(Q, b, ss.q_bytes), at_bytes(K, b, ss.kv_bytes),
+                     at_bytes(V, b, ss.kv_bytes), at_b(page_table, b, ss.pt),
+                     at_b(Kbar, b, ss.kbar), kbar_valid_blocks, at_bytes(O, b, ss.q_bytes),
+                     at_b(lse, b, ss.lse), ws, status, st);
+    if (rc != SGQA_OK) return rc;
+  }
+  return SGQA_OK;
+}
+
 SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int32_t* launches) {
   Dims dm;
   const int rc = derive(p, &dm);
@@ -555,7 +644,7 @@ SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int
       const bool filt = any_filt && chunk_filtered(dm, q0, q1);
       n += (dm.nblk > 0 ? 2 : 0) + 1 + (filt ? 4 + 2 : topk_union_launches(dm, q0, q1));
     }
-    *launches = (int32_t)n;
+    *launches = (int32_t)(n * dm.batch);
   }
   return SGQA_OK;
 }

@@ -465,6 +465,7 @@ __global__ void __launch_bounds__(384, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 37);
   int* abort_flag = reinterpret_cast<int*>(bars + 38);
   volatile int* n_stages = reinterpret_cast<volatile int*>(bars + 39);  // set once known
+  uint64_t* stall_bar = bars + 40;  // nothing arrives on it (the debug stall below)
   float* xmax = reinterpret_cast<float*>(smem + C::OFF_X);  // [2 group][BM]
   float* xsum = xmax + 2 * C::BM;                            // [2 group][BM]
 
@@ -505,6 +506,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(l_bar, 8);
     *n_stages = 0x7fffffff;
     mbar_init(mma_done, 1);
+    mbar_init(stall_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -613,6 +615,11 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t idesc_pv = idesc_bf16_f32(C::BM, D, 0, 1);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q);
       bool ok = mbar_wait(q_full, 0, ab, a.status, 205);
+      // Debug request (host-set status[3]): the first work item waits on a
+      // barrier nothing arrives on, so the pipeline gives up (detail 220) while
+      // its K and V copies are in flight.
+      if (ok && blockIdx.x == 0 && debug_request(a.status) == SGQA_DEBUG_STALL)
+        ok = mbar_wait(stall_bar, 0, ab, a.status, 220, kDebugStallNs);
       // S_j = Q K_j^T into TMEM buffer j % 2 (operands ready)
       auto do_qk = [&](int j) {
         const int ks = j % C::SK;

@@ -112,23 +112,34 @@ struct Abort {
 };
 
 // Wait for phase `parity` of `bar` to complete.  Bounded: gives up after
-// kWaitLimitNs (raising the abort flag and the status word) or as soon as
+// limit_ns (raising the abort flag and the status word) or as soon as
 // another role has aborted.  Returns false when it gave up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Abort& ab,
-                                          int32_t* status, int where) {
+                                          int32_t* status, int where,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63) == 0) {
       if (ab.set()) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         ab.raise(status, where);
         return false;
       }
     }
   }
 }
+
+// The debug request word of a status buffer (status[3]): 0 in normal use.
+// SGQA_DEBUG_STALL asks the first work item of the attention kernel to wait,
+// with a 1 ms limit, on a barrier that nothing arrives on, so that the
+// give-up path (abort flag, drain of the copies in flight, TMEM release,
+// SGQA_ERR_TIMEOUT in the status word) can be exercised without a fault.
+__device__ __forceinline__ int debug_request(const int32_t* status) {
+  return status == nullptr ? 0 : *reinterpret_cast<const volatile int32_t*>(status + 3);
+}
+constexpr uint64_t kDebugStallNs = 1000000ull;
 
 // Same, without an abort flag: used for the final drain of in-flight copies
 // and MMAs.  A drain that gives up is reported too (detail = where).

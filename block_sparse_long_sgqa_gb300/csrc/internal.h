@@ -21,6 +21,7 @@ struct Dims {
   int dtype, mode;           // enum sgqa_dtype, enum sgqa_union_mode
   float scale;               // softmax scale
   int elem;                  // bytes per Q/K/V element
+  int batch;                 // sequences in the call (processed one after another)
 };
 
 // Validate `p` and fill `dm`; returns SGQA_OK or an error code.

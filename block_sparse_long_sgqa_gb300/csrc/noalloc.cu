@@ -68,7 +68,8 @@ extern "C" SGQA_API int sgqa_topk_union_noalloc(const sgqa_params* p, const floa
     return SGQA_ERR_INVALID_ARG;
   if (scores && (reinterpret_cast<uintptr_t>(scores) & 15u)) return SGQA_ERR_ALIGNMENT;
   if (union_cap < sgqa_union_capacity(p)) return SGQA_ERR_WORKSPACE;
-  // the selection lists must fit the fixed scratch array
+  // the selection lists of one sequence must fit the fixed scratch array
+  // (the sequences of a batch reuse it one after another on the stream)
   const int64_t need = (int64_t)dm.Hkv * (q_end - q_begin) * (dm.Ks > 0 ? dm.Ks : 1);
   if (need > kNoAllocSelEntries) return SGQA_ERR_WORKSPACE;
   int32_t* sel = nullptr;
@@ -76,6 +77,16 @@ extern "C" SGQA_API int sgqa_topk_union_noalloc(const sgqa_params* p, const floa
   if (src != SGQA_OK) return src;
   // Every entry the union step reads is written first by the same launch, so
   // the array needs no clearing between calls.
-  return launch_topk_union(dm, scores, q_begin, q_end, sel, union_off, union_len, union_blk,
-                           union_mask, union_cap, status, reinterpret_cast<cudaStream_t>(stream));
+  const int64_t nq = q_end - q_begin;
+  const int64_t sc_stride = (int64_t)dm.Hkv * nq * dm.nblk;
+  const int64_t tiles = (int64_t)dm.Hkv * dm.ntiles;
+  const int64_t ucap_b = group_cap(dm) * dm.Hkv;
+  for (int64_t b = 0; b < dm.batch; ++b) {
+    const int rc2 = launch_topk_union(dm, scores ? scores + b * sc_stride : nullptr, q_begin, q_end,
+                                      sel, union_off + b * tiles, union_len + b * tiles,
+                                      union_blk + b * ucap_b, union_mask + b * ucap_b, ucap_b,
+                                      status, reinterpret_cast<cudaStream_t>(stream));
+    if (rc2 != SGQA_OK) return rc2;
+  }
+  return SGQA_OK;
 }

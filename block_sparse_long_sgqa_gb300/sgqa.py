@@ -28,6 +28,7 @@ ERR_CAPACITY, ERR_TIMEOUT, ERR_BOUNDS = 6, 7, 8
 BF16, FP32 = 0, 1
 UNION_MASKED, UNION_FULL = 0, 1
 WS_INDEX_SCORES, WS_TOPK_UNION, WS_SPARSE_ATTN, WS_PREFILL = 1, 2, 3, 4
+DEBUG_STALL = 0x5354414C  # SGQA_DEBUG_STALL: written into word 3 of a status buffer
 
 EXPORTED = ("sgqa_workspace_bytes", "sgqa_union_capacity", "sgqa_block_merge", "sgqa_index_scores",
             "sgqa_topk_union", "sgqa_topk_union_noalloc", "sgqa_sparse_attn_fwd", "sgqa_prefill",
@@ -44,7 +45,8 @@ KERNEL_NAMES = {1: "merge", 2: "split", 3: "index_query", 4: "index_scores", 5: 
 class Params(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "seq_q", "seq_kv", "q_offset", "n_q_heads", "n_kv_heads", "head_dim", "block_size",
-        "topk_tokens", "tile_q", "page_size", "dtype", "union_mode")] + [("softmax_scale", ctypes.c_float)]
+        "topk_tokens", "tile_q", "page_size", "dtype", "union_mode")] + [
+        ("softmax_scale", ctypes.c_float), ("batch", ctypes.c_int32)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -90,16 +92,17 @@ for _f in ("sgqa_block_merge", "sgqa_index_scores", "sgqa_topk_union", "sgqa_top
 
 
 def params(seq_q, seq_kv, q_offset, n_q_heads, n_kv_heads, head_dim, block_size, topk_tokens,
-           tile_q, page_size=0, dtype=BF16, union_mode=UNION_MASKED, softmax_scale=0.0) -> Params:
+           tile_q, page_size=0, dtype=BF16, union_mode=UNION_MASKED, softmax_scale=0.0,
+           batch=1) -> Params:
     return Params(seq_q, seq_kv, q_offset, n_q_heads, n_kv_heads, head_dim, block_size,
-                  topk_tokens, tile_q, page_size, dtype, union_mode, softmax_scale)
+                  topk_tokens, tile_q, page_size, dtype, union_mode, softmax_scale, batch)
 
 
-def params_for(wl, union_mode=UNION_MASKED) -> Params:
-    """Params of a synth.Workload."""
+def params_for(wl, union_mode=UNION_MASKED, batch=1) -> Params:
+    """Params of a synth.Workload (batch sequences of its shape)."""
     return params(wl.seq_q, wl.seq_kv, wl.q_offset, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
                   wl.block_size, wl.topk_tokens, wl.tile_q, wl.page_size,
-                  BF16 if wl.dtype == "bf16" else FP32, union_mode)
+                  BF16 if wl.dtype == "bf16" else FP32, union_mode, batch=batch)
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -252,25 +255,34 @@ def alloc_workspace(p: Params, which: int, device="cuda") -> torch.Tensor:
     return torch.empty(max(workspace_bytes(p, which), 1), dtype=torch.uint8, device=device)
 
 
+def _nb(p: Params) -> int:
+    return p.batch if p.batch > 1 else 1
+
+
+def _bshape(p: Params, *shape):
+    """A per-sequence shape, with the outer batch dimension when batch > 1."""
+    return (p.batch, *shape) if p.batch > 1 else shape
+
+
 def alloc_union(p: Params, device="cuda"):
     """(union_off, union_len, union_blk, union_mask) sized for the whole call."""
     ntiles = (p.seq_q + p.tile_q - 1) // p.tile_q
     cap = max(union_capacity(p), 1)
-    return (torch.zeros(p.n_kv_heads * ntiles, dtype=torch.int64, device=device),
-            torch.zeros(p.n_kv_heads * ntiles, dtype=torch.int32, device=device),
+    return (torch.zeros(_nb(p) * p.n_kv_heads * ntiles, dtype=torch.int64, device=device),
+            torch.zeros(_nb(p) * p.n_kv_heads * ntiles, dtype=torch.int32, device=device),
             torch.zeros(cap, dtype=torch.int32, device=device),
             torch.zeros(cap, dtype=torch.int64, device=device))
 
 
 def alloc_outputs(p: Params, device="cuda"):
-    O = torch.empty(p.seq_q, p.n_q_heads, p.head_dim, dtype=_odt(p), device=device)
-    lse = torch.empty(p.n_q_heads, p.seq_q, dtype=torch.float32, device=device)
+    O = torch.empty(_bshape(p, p.seq_q, p.n_q_heads, p.head_dim), dtype=_odt(p), device=device)
+    lse = torch.empty(_bshape(p, p.n_q_heads, p.seq_q), dtype=torch.float32, device=device)
     return O, lse
 
 
 def kbar_empty(p: Params, device="cuda") -> torch.Tensor:
-    return torch.zeros(p.n_kv_heads, p.seq_kv // p.block_size, p.head_dim, dtype=torch.float32,
-                       device=device)
+    return torch.zeros(_bshape(p, p.n_kv_heads, p.seq_kv // p.block_size, p.head_dim),
+                       dtype=torch.float32, device=device)
 
 
 def default_scale(p: Params) -> float:

@@ -16,10 +16,17 @@ tokens, contexts up to 1M):
   Q[t][h] = 2.1 * u[g(h)][c(pos(t))] + noise whose lanes follow a stationary
   AR(1) process along t (marginal N(0, 1), correlation ``rho_q`` between
   neighbours; ``rho_q = 0`` gives i.i.d. noise).  2.1 = 0.7 * 3.
-* needles (the 128K workload): each block j of group g carries a signature
-  unit vector s[g][j], added to its keys with weight 2; every query tile of
-  ``tile_q`` queries gets 16 distinct historical blocks whose signatures are
-  summed, scaled by 4 and added to all of that group's query heads.
+* needles (the 128K workload): every (query tile, KV group) draws one random
+  unit direction r and 16 distinct historical blocks (the planted needles);
+  8 r is added to all of that group's query heads in the tile, and 2 r to
+  every key of each of the 16 blocks (a block planted by several tiles
+  carries the sum of their directions).  A needle block then scores about
+  8 * 2 = 16 above what it would score otherwise, while another block's score
+  moves by 8 r against its keys' random part (a standard deviation near 3 at
+  128 dimensions, the same for every query of the tile), so planted blocks
+  sit far above the k-th score and a correct selection finds them.  The
+  larger share sits on the query side so that the keys, which every tile
+  reads, stay close to the clustered distribution.
 """
 from __future__ import annotations
 
@@ -42,7 +49,7 @@ N_TOPICS = 64
 TOPIC_MEAN_RUN = 64.0
 NEEDLES_PER_TILE = 16
 NEEDLE_KEY_WEIGHT = 2.0
-NEEDLE_QUERY_WEIGHT = 4.0
+NEEDLE_QUERY_WEIGHT = 8.0
 DEFAULT_RHO_Q = 0.99
 
 
@@ -202,20 +209,18 @@ def make_inputs(wl: Workload, rho_q: Optional[float] = None) -> dict:
 
     key_add = q_add = None
     if wl.needles:
-        nblk = wl.n_blocks
-        sig = np.empty((nblk, Hkv, d), np.float32)  # [block][group][d]
-        lib.synth_unit_dirs(seed, STREAM_SIG, nblk * Hkv, d, _ptr(sig))
-        key_add = sig
         ntiles = (T + wl.tile_q - 1) // wl.tile_q
+        tdir = np.empty((ntiles, Hkv, d), np.float32)  # one direction per (tile, group)
+        lib.synth_unit_dirs(seed, STREAM_SIG, ntiles * Hkv, d, _ptr(tdir))
+        key_add = np.zeros((-(-Tkv // B), Hkv, d), np.float32)  # [block][group][d], tail included
         needles = np.full((ntiles, Hkv, wl.needles), -1, np.int32)
-        q_add = np.zeros((ntiles, Hkv, d), np.float32)
         for tau in range(ntiles):
             nh = (wl.q_offset + tau * wl.tile_q) // B
             for g in range(Hkv):
                 js = _choose_distinct(seed, STREAM_NEEDLE, tau * Hkv + g, nh, wl.needles)
                 needles[tau, g, :len(js)] = js
-                if len(js):
-                    q_add[tau, g] = sig[js, g].sum(0)
+                key_add[js, g] += tdir[tau, g]
+        q_add = tdir
         out["needles"] = needles
 
     K = np.empty((Tkv, Hkv, d), edt)

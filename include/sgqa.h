@@ -31,6 +31,9 @@
  *     caller zeroes (sgqa_reset_status).  Kernels record the first
  *     device-side error there (SGQA_ERR_CAPACITY, SGQA_ERR_TIMEOUT,
  *     SGQA_ERR_BOUNDS) with a detail word; outputs are undefined after one.
+ *     Word 0 = code, word 1 = detail (the place that reported it), word 2 =
+ *     count of errors, word 3 = debug request (0 in normal use; see
+ *     SGQA_DEBUG_STALL).
  *   - The return value reports host-side validation (SGQA_ERR_INVALID_ARG,
  *     SGQA_ERR_UNSUPPORTED, SGQA_ERR_ALIGNMENT, SGQA_ERR_WORKSPACE) and
  *     launch failures (SGQA_ERR_CUDA); nothing is enqueued when it is not
@@ -49,6 +52,20 @@
  *     (natural log).
  *   - Union tiles are tau = [tau * tile_q, min(tau * tile_q + tile_q, seq_q)),
  *     aligned to query 0 of the call; ntiles = ceil(seq_q / tile_q).
+ *   - Batches: with batch = N > 1 the call covers N independent sequences of
+ *     the same lengths and every per-sequence tensor gains an outer dimension
+ *     of N: Q and O [N][seq_q][n_q_heads][head_dim]; contiguous K and V
+ *     [N][seq_kv][n_kv_heads][head_dim]; Kbar [N][n_kv_heads][nblk][head_dim];
+ *     scores [N][n_kv_heads][q_end - q_begin][nblk]; topk_idx
+ *     [N][n_kv_heads][q_end - q_begin][k / B]; lse [N][n_q_heads][seq_q];
+ *     union_off and union_len [N][n_kv_heads][ntiles]; union_blk and
+ *     union_mask [N][sgqa_union_capacity(p) / N], each sequence's offsets
+ *     relative to its own part.  A paged cache keeps one page pool shared by all sequences
+ *     (K and V [n_pages][n_kv_heads][page_size][head_dim]) and page_table
+ *     [N][ceil(seq_kv / page_size)].  The sequences are enqueued one after
+ *     another on the stream and share the workspace and the status word, so
+ *     sgqa_workspace_bytes is that of one sequence, while
+ *     sgqa_union_capacity and sgqa_prefill_plan's launch count cover all N.
  */
 #ifndef SGQA_H
 #define SGQA_H
@@ -83,6 +100,17 @@ enum sgqa_status_code {
 
 enum sgqa_dtype { SGQA_BF16 = 0, SGQA_FP32 = 1 };
 
+/* Debug request, written by the caller into word 3 of a status buffer.  With
+ * SGQA_DEBUG_STALL there, the first work item of the next attention launch
+ * (sgqa_sparse_attn_fwd, or the attention inside sgqa_prefill) waits on a
+ * barrier that nothing arrives on; after 1 ms it gives up the way any stalled
+ * pipeline wait does: every role of the work item stops, the copies it has in
+ * flight land, its tensor memory is released and the kernel returns, leaving
+ * SGQA_ERR_TIMEOUT with detail 220 in the status buffer (outputs of that call
+ * are undefined; the stream and context stay usable).  It exists to test the
+ * give-up path without a fault.  sgqa_reset_status clears the word. */
+#define SGQA_DEBUG_STALL 0x5354414c
+
 /* Union semantics ("Efficient implementation of sparse attention").
  * MASKED (default): the union only batches work; query t attends to its own
  * selected blocks plus its current block, so results do not depend on tile_q.
@@ -104,6 +132,7 @@ typedef struct sgqa_params {
   int32_t dtype;        /* enum sgqa_dtype of Q, K, V and O */
   int32_t union_mode;   /* enum sgqa_union_mode */
   float softmax_scale;  /* 0 -> 1 / sqrt(head_dim) */
+  int32_t batch;        /* sequences of these lengths in one call; 0 or 1 = one */
 } sgqa_params;
 
 /* Workspace queries: `which` names the entry point. */
@@ -205,7 +234,10 @@ SGQA_API int sgqa_sparse_attn_fwd(const sgqa_params* p, const void* Q, const voi
  *     SGQA_ERR_WORKSPACE (call it on smaller query ranges).
  *   - Allocates nothing.  The first call on a device looks up the array's
  *     device address (cudaGetSymbolAddress) with that device current; make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  The address is kept for
+ *     the life of the process: after cudaDeviceReset (or anything else that
+ *     destroys the device's primary context) it is stale, so do not call
+ *     this entry point on that device again after such a reset.
  *   - All calls share the one array, so calls whose kernels overlap on the GPU
  *     (different streams, or different host threads) race; serialise them.
  *     Nothing in the array needs to start at zero. */

@@ -137,3 +137,32 @@ def test_kv_packing_rule(s):
     below = s.params(seq_q=32, seq_kv=4128, q_offset=4096, **small)
     above = s.params(seq_q=40, seq_kv=4136, q_offset=4096, **small)
     assert s.sgqa_prefill_plan(above)[1] - s.sgqa_prefill_plan(below)[1] == 2
+
+
+def test_params_struct_matches_header(s):
+    """The binding's Params fields are the header's sgqa_params fields, in order."""
+    text = open(os.path.join(ROOT, "include", "sgqa.h")).read()
+    body = re.search(r"typedef struct sgqa_params \{(.*?)\} sgqa_params;", text, re.S).group(1)
+    fields = re.findall(r"^\s*(?:int32_t|float)\s+(\w+);", body, re.M)
+    assert fields == [n for n, _ in s.Params._fields_]
+    assert ctypes.sizeof(s.Params) == 4 * len(fields)
+
+
+def test_batch_scales_capacity_and_plan(s):
+    """batch = N covers N sequences: N times the union capacity and launches,
+    the workspace of one sequence; a negative batch is rejected."""
+    one = p_small(s)
+    three = p_small(s, batch=3)
+    assert s.union_capacity(three) == 3 * s.union_capacity(one)
+    assert s.sgqa_prefill_plan(three)[1] == 3 * s.sgqa_prefill_plan(one)[1]
+    assert s.sgqa_prefill_plan(three)[0] == s.sgqa_prefill_plan(one)[0]
+    for w in (s.WS_INDEX_SCORES, s.WS_TOPK_UNION, s.WS_SPARSE_ATTN, s.WS_PREFILL):
+        assert s.workspace_bytes(three, w) == s.workspace_bytes(one, w)
+    assert s.union_capacity(p_small(s, batch=0)) == s.union_capacity(one)
+    assert _call_prefill(s, p_small(s, batch=-1)) == s.ERR_INVALID_ARG
+
+
+def test_debug_stall_constant_matches_header(s):
+    text = open(os.path.join(ROOT, "include", "sgqa.h")).read()
+    m = re.search(r"#define SGQA_DEBUG_STALL (0x[0-9a-fA-F]+)", text)
+    assert m and int(m.group(1), 16) == s.DEBUG_STALL

@@ -247,3 +247,97 @@ def test_decode_step_paged(s, pos):
     rows = np.arange(1, dtype=np.int32)
     _, frac = check_end_to_end(s, wl, inp, O, lse, rows, Kbar, d)
     assert frac >= 0.5  # groups whose k-th score is a near-tie are checked by R2 only
+
+
+def _batch2_inputs(s, paged):
+    """Two sequences of one shape (different seeds) laid out for batch = 2: an
+    outer dimension on Q, K and V, or one page pool shared by both with a
+    page table per sequence."""
+    base = SMALL["paged" if paged else "b8"]
+    wls = [base, base.replace(seed=base.seed + 17)]
+    inps = [synth.make_inputs(w) for w in wls]
+    singles = [dev_inputs(i) for i in inps]
+    d = {"Q": torch.stack([x["Q"] for x in singles])}
+    if paged:
+        npages = singles[0]["K"].shape[0]
+        d["K"] = torch.cat([x["K"] for x in singles]).contiguous()
+        d["V"] = torch.cat([x["V"] for x in singles]).contiguous()
+        d["page_table"] = torch.stack([singles[0]["page_table"],
+                                       singles[1]["page_table"] + npages]).contiguous()
+    else:
+        d["K"] = torch.stack([x["K"] for x in singles])
+        d["V"] = torch.stack([x["V"] for x in singles])
+        d["page_table"] = None
+    return wls, inps, singles, d
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_prefill_batch2_vs_single_calls_and_oracle(s, paged):
+    """batch = 2 in one sgqa_prefill call: each sequence equals its own
+    single-sequence call bit for bit and matches the oracle end to end."""
+    wls, inps, singles, d = _batch2_inputs(s, paged)
+    p2 = s.params_for(wls[0], batch=2)
+    O, lse = s.alloc_outputs(p2)
+    Kbar = s.kbar_empty(p2)
+    st = s.new_status()
+    s.sgqa_prefill(p2, d["Q"], d["K"], d["V"], Kbar, O, lse, s.alloc_workspace(p2, s.WS_PREFILL),
+                   page_table=d["page_table"], status=st)
+    assert s.read_status(st)[0] == 0
+    p1 = s.params_for(wls[0])
+    rows = np.arange(wls[0].seq_q, dtype=np.int32)
+    for b in range(2):
+        O1, l1, Kb1 = run_prefill(s, p1, singles[b])
+        assert torch.equal(O[b], O1) and torch.equal(lse[b], l1) and torch.equal(Kbar[b], Kb1)
+        _, frac = check_end_to_end(s, wls[b], inps[b], O[b], lse[b], rows, Kb1, singles[b])
+        assert frac > 0.9
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_steps_batch2_vs_single_calls(s, paged):
+    """The step entry points with batch = 2 (merge, scores, top-k and union,
+    attention, and the no-allocation top-k) equal single calls bit for bit."""
+    wls, inps, singles, d = _batch2_inputs(s, paged)
+    wl = wls[0]
+    p2, p1 = s.params_for(wl, batch=2), s.params_for(wl)
+    T, Hkv, nblk, Ks = wl.seq_q, wl.n_kv_heads, wl.n_blocks, wl.k_blocks
+    st = s.new_status()
+    Kbar = s.kbar_empty(p2)
+    s.sgqa_block_merge(p2, d["K"], Kbar, page_table=d["page_table"], status=st)
+    scores = torch.empty(2, Hkv, T, nblk, device="cuda")
+    s.sgqa_index_scores(p2, d["Q"], Kbar, 0, T, scores, s.alloc_workspace(p2, s.WS_INDEX_SCORES))
+    sel = torch.empty(2, Hkv, T, Ks, dtype=torch.int32, device="cuda")
+    u2 = s.alloc_union(p2)
+    s.sgqa_topk_union(p2, scores, 0, T, sel, *u2, status=st)
+    un = s.alloc_union(p2)
+    s.sgqa_topk_union_noalloc(p2, scores, 0, T, *un, status=st)
+    O, lse = s.alloc_outputs(p2)
+    s.sgqa_sparse_attn_fwd(p2, d["Q"], d["K"], d["V"], *u2, O, lse, page_table=d["page_table"],
+                           ws=s.alloc_workspace(p2, s.WS_SPARSE_ATTN), status=st)
+    assert s.read_status(st)[0] == 0
+    cap1 = s.union_capacity(p1)
+    ntl = Hkv * ((T + wl.tile_q - 1) // wl.tile_q)
+    for b in range(2):
+        x = singles[b]
+        Kb1 = s.kbar_empty(p1)
+        s.sgqa_block_merge(p1, x["K"], Kb1, page_table=x["page_table"])
+        sc1 = torch.empty(Hkv, T, nblk, device="cuda")
+        s.sgqa_index_scores(p1, x["Q"], Kb1, 0, T, sc1, s.alloc_workspace(p1, s.WS_INDEX_SCORES))
+        sel1 = torch.empty(Hkv, T, Ks, dtype=torch.int32, device="cuda")
+        u1 = s.alloc_union(p1)
+        s.sgqa_topk_union(p1, sc1, 0, T, sel1, *u1, status=st)
+        O1, l1 = s.alloc_outputs(p1)
+        s.sgqa_sparse_attn_fwd(p1, x["Q"], x["K"], x["V"], *u1, O1, l1,
+                               page_table=x["page_table"],
+                               ws=s.alloc_workspace(p1, s.WS_SPARSE_ATTN), status=st)
+        assert s.read_status(st)[0] == 0
+        assert torch.equal(Kbar[b], Kb1)
+        assert torch.equal(scores[b], sc1)
+        assert torch.equal(sel[b], sel1)
+        for u in (u2, un):   # offsets, lengths, then the slots of sequence b
+            assert torch.equal(u[0][b * ntl:(b + 1) * ntl], u1[0])
+            assert torch.equal(u[1][b * ntl:(b + 1) * ntl], u1[1])
+            for k in (2, 3):
+                a = u[k][b * cap1:(b + 1) * cap1]
+                for o, n in zip(u1[0].tolist(), u1[1].tolist()):
+                    assert torch.equal(a[o:o + n], u1[k][o:o + n])
+        assert torch.equal(O[b], O1) and torch.equal(lse[b], l1)
