@@ -49,6 +49,13 @@ constexpr unsigned FULL = 0xffffffffu;
 // the same relative precision at any of these magnitudes; 2^16 leaves ample
 // range for sums of a stage's products into fp32.
 constexpr float kLazy = 16.0f;
+// The one-pass check on 64 keys: their P values (relative to the reference
+// maximum) are computed first and kept only when their sum stays at or below
+// 2^kLazy, which bounds every one of them by 2^kLazy.  (A sum of many
+// moderate values can trip it without any key exceeding the bound; the stage
+// then takes the exact path below, which gives the same result.)
+constexpr float kLazySum = 65536.0f;
+static_assert(kLazySum == (float)(1 << 16) && kLazy == 16.0f, "the sum bound is 2^kLazy");
 
 template <int NBPS>
 struct MetaT {         // one stage's block list
@@ -811,19 +818,20 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       // One pass when possible: p = 2^(s * scale * log2(e) - m_used) with the
-      // running reference maximum, as long as no allowed key of the stage
-      // exceeds it by more than 2^kLazy (checked per 64 keys before their
-      // exponentials).  When keys 0..63 exceed it the stage is done in two
-      // passes below; when only keys 64..127 do, the maximum is raised in place
-      // (stage_second_half), since P of keys 0..63 already lies over their S
-      // values.
+      // running reference maximum, as long as the P values of each 64 keys
+      // sum to at most 2^kLazy (checked before they are written).  When keys
+      // 0..63 fail the check the stage is done in two passes below; when only
+      // keys 64..127 do, the maximum is raised in place (stage_second_half),
+      // since P of keys 0..63 already lies over their S values.  The exponent
+      // arguments and the sums use packed f32x2 arithmetic.
       float rs0 = 0.0f, rs1 = 0.0f;
       bool fast = __all_sync(FULL, m_used != ninf || (al0 | al1 | al2 | al3) == 0u);
       bool mid = false;  // keys 64..127 need a higher maximum: the path below
       // Stages whose blocks are all historical (B >= 8) take the mask per
-      // block: block maxima, and -m or -inf as the exponent's additive term.
+      // block: -m or -inf as the exponent's additive term.
       bool by_block = false;
       if constexpr (B >= 8) by_block = m.diag >= nb;
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
       if (fast && by_block) {
         constexpr int BPHh = 64 / B;  // blocks per 64 keys
         const uint32_t hb = row_ok ? qbits_of(m, qi) : 0u;
@@ -834,18 +842,27 @@ __global__ void __launch_bounds__(384, 1)
           tmem_ld32(tS + (2 * hh + 1) * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
           tmem_wait_ld();
           const uint32_t hbh = hb >> (hh * BPHh);
-          float cm = ninf;
-          float cb[BPHh];
+          uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+          uint32_t pk[32];
 #pragma unroll
           for (int jj = 0; jj < BPHh; ++jj) {
-            float bm = __uint_as_float(v[jj * B]);
+            const float cbv = ((hbh >> jj) & 1u) ? -m_used : ninf;
+            const uint64_t cb2 = f2_pack(cbv, cbv);
 #pragma unroll
-            for (int k = 1; k < B; ++k) bm = fmaxf(bm, __uint_as_float(v[jj * B + k]));
-            const bool al = (hbh >> jj) & 1u;
-            cm = fmaxf(cm, al ? bm : ninf);
-            cb[jj] = al ? -m_used : ninf;
+            for (int e = jj * B; e < jj * B + B; e += 2) {
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2,
+                               cb2),
+                        x0, x1);
+              const float p0 = ex2(x0), p1 = ex2(x1);
+              acc[(e >> 1) & 3] = f2_add(acc[(e >> 1) & 3], f2_pack(p0, p1));
+              pk[e >> 1] = pack_bf16x2(p0, p1);
+            }
           }
-          if (__any_sync(FULL, cm * sl2 > m_used + kLazy)) {
+          float s0, s1;
+          f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
+          const float hs = s0 + s1;
+          if (__any_sync(FULL, !(hs <= kLazySum))) {
             if (hh == 0) {  // nothing written yet: the two passes below
               fast = false;
               break;
@@ -853,15 +870,7 @@ __global__ void __launch_bounds__(384, 1)
             mid = true;
             break;
           }
-          uint32_t pk[32];
-#pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            const float p0 = ex2(fmaf(__uint_as_float(v[e]), sl2, cb[e / B]));
-            const float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl2, cb[(e + 1) / B]));
-            rs0 += p0;
-            rs1 += p1;
-            pk[e >> 1] = pack_bf16x2(p0, p1);
-          }
+          rs0 += hs;
           tmem_st32(tS + hh * 32, pk);  // S columns 0..63 have been read by now
         }
       } else if (fast) {
@@ -872,13 +881,32 @@ __global__ void __launch_bounds__(384, 1)
           tmem_ld32(tS + (2 * hh + 1) * 32, v1);
           tmem_wait_ld();
           const uint32_t a0 = hh == 0 ? al0 : al2, a1 = hh == 0 ? al1 : al3;
-          float cm0 = ninf, cm1 = ninf;
+          uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+          uint32_t pk[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            cm0 = fmaxf(cm0, ((a0 >> e) & 1u) ? __uint_as_float(v0[e]) : ninf);
-            cm1 = fmaxf(cm1, ((a1 >> e) & 1u) ? __uint_as_float(v1[e]) : ninf);
+          for (int e = 0; e < 32; e += 2) {
+            // the additive term is -m for an allowed key and -inf otherwise
+            float x0, x1, x2, x3;
+            const float c0 = ((a0 >> e) & 1u) ? -m_used : ninf;
+            const float c1 = ((a0 >> (e + 1)) & 1u) ? -m_used : ninf;
+            const float c2 = ((a1 >> e) & 1u) ? -m_used : ninf;
+            const float c3 = ((a1 >> (e + 1)) & 1u) ? -m_used : ninf;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(v0[e]), __uint_as_float(v0[e + 1])), sl2x2,
+                             f2_pack(c0, c1)),
+                      x0, x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(v1[e]), __uint_as_float(v1[e + 1])), sl2x2,
+                             f2_pack(c2, c3)),
+                      x2, x3);
+            const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+            acc[(e >> 1) & 1] = f2_add(acc[(e >> 1) & 1], f2_pack(p0, p1));
+            acc[2 + ((e >> 1) & 1)] = f2_add(acc[2 + ((e >> 1) & 1)], f2_pack(p2, p3));
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+            pk[16 + (e >> 1)] = pack_bf16x2(p2, p3);
           }
-          if (__any_sync(FULL, fmaxf(cm0, cm1) * sl2 > m_used + kLazy)) {
+          float s0, s1;
+          f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
+          const float hs = s0 + s1;
+          if (__any_sync(FULL, !(hs <= kLazySum))) {
             if (hh == 0) {  // nothing written yet: the two passes below
               fast = false;
               break;
@@ -886,20 +914,7 @@ __global__ void __launch_bounds__(384, 1)
             mid = true;
             break;
           }
-          uint32_t pk[32];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float p0 = ((a0 >> e) & 1u) ? ex2(fmaf(__uint_as_float(v0[e]), sl2, -m_used)) : 0.0f;
-            const float p1 =
-                ((a0 >> (e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v0[e + 1]), sl2, -m_used)) : 0.0f;
-            const float p2 = ((a1 >> e) & 1u) ? ex2(fmaf(__uint_as_float(v1[e]), sl2, -m_used)) : 0.0f;
-            const float p3 =
-                ((a1 >> (e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(v1[e + 1]), sl2, -m_used)) : 0.0f;
-            rs0 += p0 + p2;
-            rs1 += p1 + p3;
-            pk[e >> 1] = pack_bf16x2(p0, p1);
-            pk[16 + (e >> 1)] = pack_bf16x2(p2, p3);
-          }
+          rs0 += hs;
           tmem_st32(tS + hh * 32, pk);  // S columns 0..63 have been read by now
         }
       }
