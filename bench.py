@@ -53,6 +53,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-quality", action="store_true",
                     help="skip the union / recall / coverage report (computed after timing)")
+    ap.add_argument("--index-mode", choices=["split", "bf16"], default="split",
+                    help="indexer precision: fp32 scores from a bf16 split (exact selection) "
+                         "or bf16 scores (one product; recall against split reported)")
     ap.add_argument("--no-stress", action="store_true",
                     help="skip the i.i.d. query-noise run reported beside the headline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -308,7 +311,7 @@ def run_reference(args, wl, rank):
     return line
 
 
-def quality(wl, inp, Q, K, V, pt, Kbar, lse, dev, nq_max=1024):
+def quality(wl, inp, Q, K, V, pt, Kbar, lse, dev, nq_max=1024, index_mode=0):
     """Selection quality on the last nq_max queries (a whole number of tiles),
     through the C ABI and outside the timed region:
       union inflation |U| / min(k/B, nh) per (tile, group) of the standalone
@@ -326,18 +329,22 @@ def quality(wl, inp, Q, K, V, pt, Kbar, lse, dev, nq_max=1024):
         return None
     q0 = wl.seq_q - nq
     sub = wl.replace(seq_q=nq, q_offset=wl.q_offset + q0)
-    ps = sgqa.params_for(sub)
+    ps = sgqa.params_for(sub, index_mode=index_mode)
     Qs = Q[q0:].contiguous()
     nblk = wl.seq_kv // B
     Ks = wl.topk_tokens // B
-    scores = torch.empty(wl.n_kv_heads, nq, nblk, device=dev)
-    sgqa.sgqa_index_scores(ps, Qs, Kbar, 0, nq, scores,
-                           sgqa.alloc_workspace(ps, sgqa.WS_INDEX_SCORES, dev))
-    sel = torch.empty(wl.n_kv_heads, nq, Ks, dtype=torch.int32, device=dev)
-    uo, ul, ub, um = sgqa.alloc_union(ps, dev)
     st = sgqa.new_status(dev)
-    sgqa.sgqa_topk_union(ps, scores, 0, nq, sel, uo, ul, ub, um, status=st)
-    del scores
+
+    def select_sub(p_):
+        sc = torch.empty(wl.n_kv_heads, nq, nblk, device=dev)
+        sgqa.sgqa_index_scores(p_, Qs, Kbar, 0, nq, sc,
+                               sgqa.alloc_workspace(p_, sgqa.WS_INDEX_SCORES, dev))
+        sl = torch.empty(wl.n_kv_heads, nq, Ks, dtype=torch.int32, device=dev)
+        u_ = sgqa.alloc_union(p_, dev)
+        sgqa.sgqa_topk_union(p_, sc, 0, nq, sl, *u_, status=st)
+        return sl, u_
+
+    sel, (uo, ul, ub, um) = select_sub(ps)
     t = np.arange(q0, wl.seq_q)
     nh = np.minimum((wl.q_offset + t) // B, nblk)
     tiles = np.arange(nq // W)
@@ -345,6 +352,12 @@ def quality(wl, inp, Q, K, V, pt, Kbar, lse, dev, nq_max=1024):
     infl = (ul.cpu().numpy().reshape(wl.n_kv_heads, -1)[:, :len(tiles)] / np.maximum(kcap, 1))
     out = {"queries": f"last {nq}", "union_inflation_mean": float(infl.mean()),
            "union_inflation_p99": float(np.percentile(infl, 99))}
+    if index_mode == sgqa.INDEX_BF16:  # recall of the exact (split) selection
+        ref_sel, _ = select_sub(sgqa.params_for(sub))
+        a, b = ref_sel.cpu().numpy(), sel.cpu().numpy()
+        hit = sum(len(np.intersect1d(a[g, r][a[g, r] >= 0], b[g, r]))
+                  for g in range(a.shape[0]) for r in range(a.shape[1]))
+        out["recall_vs_split_index"] = hit / max(1, int((a >= 0).sum()))
     if "needles" in inp:
         seln = sel.cpu().numpy()
         nd = inp["needles"]
@@ -360,7 +373,7 @@ def quality(wl, inp, Q, K, V, pt, Kbar, lse, dev, nq_max=1024):
     del sel
     # dense reference: every historical block selected
     dense = sub.replace(topk_tokens=nblk * B)
-    pd = sgqa.params_for(dense)
+    pd = sgqa.params_for(dense, index_mode=index_mode)
     Od, lsed = sgqa.alloc_outputs(pd, dev)
     Kb = sgqa.kbar_empty(pd, dev)
     sgqa.sgqa_prefill(pd, Qs, K, V, Kb, Od, lsed, sgqa.alloc_workspace(pd, sgqa.WS_PREFILL, dev),
@@ -379,6 +392,7 @@ def config_of(wl, args):
             "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
             "block_size": wl.block_size, "topk_tokens": wl.topk_tokens, "tile_q": wl.tile_q,
             "page_size": wl.page_size, "union_mode": args.union_mode,
+            "index_mode": args.index_mode,
             "inputs": f"seeded {wl.dist}" + (f", AR(1) query noise rho={wl.rho_q if args.rho_q is None else args.rho_q}"
                                               if wl.dist == "clustered" else "")
                       + (f", {wl.needles} needle blocks per tile" if wl.needles else ""),
@@ -409,7 +423,9 @@ def main(argv=None):
     torch.cuda.set_device(local)
     dist_init(world, "nccl")
     dev = torch.device("cuda", local)
-    p = sgqa.params_for(wl, union_mode=1 if args.union_mode == "full" else 0)
+    index_mode = sgqa.INDEX_BF16 if args.index_mode == "bf16" else sgqa.INDEX_SPLIT
+    p = sgqa.params_for(wl, union_mode=1 if args.union_mode == "full" else 0,
+                        index_mode=index_mode)
     chunk, launches = sgqa.sgqa_prefill_plan(p)
 
     t_gen = time.perf_counter()
@@ -562,7 +578,7 @@ def main(argv=None):
     # ---------------- selection quality (rank 0, after timing)
     qual = None
     if rank == 0 and not args.no_quality:
-        qual = quality(wl, inp, Q, K, V, pt, Kbar, lse, dev)
+        qual = quality(wl, inp, Q, K, V, pt, Kbar, lse, dev, index_mode=index_mode)
 
     # ---------------- the literal input reading (rank 0, after the headline)
     # The headline's query noise is AR(1) along the sequence (rho 0.99); the
@@ -597,7 +613,7 @@ def main(argv=None):
                   "kernels_ms_per_step": per0,
                   "step_roofline_frac": t_roof * 1e3 / ms0}
         if not args.no_quality:
-            q0 = quality(wl, inp0, Q, K, V, pt, Kbar, lse, dev)
+            q0 = quality(wl, inp0, Q, K, V, pt, Kbar, lse, dev, index_mode=index_mode)
             if q0:
                 stress.update({k: q0[k] for k in ("union_inflation_mean", "union_inflation_p99",
                                                    "needle_recall", "coverage_mean") if k in q0})

@@ -55,7 +55,8 @@ int derive(const sgqa_params* p, Dims* dm) {
     return SGQA_ERR_INVALID_ARG;
   if (!(p->softmax_scale >= 0.0f) || !std::isfinite(p->softmax_scale))
     return SGQA_ERR_INVALID_ARG;
-  if (p->page_size < 0 || p->batch < 0) return SGQA_ERR_INVALID_ARG;
+  if (p->page_size < 0 || p->batch < 0 || p->index_mode < 0 || p->index_mode > 1)
+    return SGQA_ERR_INVALID_ARG;
   const int B = p->block_size;
   if (B != 1 && B != 2 && B != 4 && B != 8 && B != 16) return SGQA_ERR_UNSUPPORTED;
   if (p->head_dim != 64 && p->head_dim != 128) return SGQA_ERR_UNSUPPORTED;
@@ -80,6 +81,7 @@ int derive(const sgqa_params* p, Dims* dm) {
   dm->scale = p->softmax_scale > 0.0f ? p->softmax_scale : 1.0f / std::sqrt((float)p->head_dim);
   dm->elem = p->dtype == SGQA_BF16 ? 2 : 4;
   dm->batch = p->batch > 1 ? p->batch : 1;
+  dm->index_bf16 = p->index_mode == SGQA_INDEX_BF16 ? 1 : 0;
   return SGQA_OK;
 }
 
@@ -516,17 +518,28 @@ SGQA_API int sgqa_sparse_attn_fwd(const sgqa_params* p, const void* Q, const voi
 
 namespace {
 
-// One sequence of sgqa_prefill (arguments validated by the caller).
-int prefill_one(const Dims& dm, const void* Q, const void* K, const void* V,
-                const int32_t* page_table, float* Kbar, int32_t kbar_valid_blocks, void* O,
-                float* lse, void* ws, int32_t* status, cudaStream_t st) {
+// One sequence of sgqa_prefill (arguments validated by the caller).  Qidx
+// (nullable) replaces the mean of each group's query heads as the index
+// query, Kidx (nullable) replaces K as the merge's input.
+int prefill_one(const Dims& dm, const void* Q, const void* K, const void* V, const void* Qidx,
+                const void* Kidx, const int32_t* page_table, float* Kbar,
+                int32_t kbar_valid_blocks, void* O, float* lse, void* ws, int32_t* status,
+                cudaStream_t st) {
   int rc = SGQA_OK;
   Carve c(align_ws(ws));
   PrefillWs w = carve_prefill(c, dm);
+  // the index query's source: Q with G heads per group, or Qidx with one
+  Dims qd = dm;
+  const void* qsrc = Q;
+  if (Qidx != nullptr) {
+    qd.H = dm.Hkv;
+    qd.G = 1;
+    qsrc = Qidx;
+  }
 
   // step 1: merge the blocks not yet in the cache (and split all of them for the indexer)
-  cudaError_t e = launch_block_merge(dm, K, page_table, kbar_valid_blocks, dm.nblk, Kbar, w.ix.khi,
-                                     w.ix.klo, st);
+  cudaError_t e = launch_block_merge(dm, Kidx != nullptr ? Kidx : K, page_table,
+                                     kbar_valid_blocks, dm.nblk, Kbar, w.ix.khi, w.ix.klo, st);
   if (e == cudaSuccess && kbar_valid_blocks > 0) {
     Dims part = dm;  // split the cached prefix: per group, blocks [0, kbar_valid_blocks)
     for (int g = 0; g < dm.Hkv && e == cudaSuccess; ++g) {
@@ -547,7 +560,7 @@ int prefill_one(const Dims& dm, const void* Q, const void* K, const void* V,
     const int64_t tau0 = q0 / dm.W, tau1 = (q1 + dm.W - 1) / dm.W;
     const bool filt = w.filt && chunk_filtered(dm, q0, q1);
     if (dm.nblk > 0) {
-      e = launch_index_query(dm, Q, q0, q1, w.ix.qhi, w.ix.qlo, st);
+      e = launch_index_query(qd, qsrc, q0, q1, w.ix.qhi, w.ix.qlo, st);
       if (e != cudaSuccess) return SGQA_ERR_CUDA;
       IndexMode mode{};
       if (filt) {  // thresholds from the sampled blocks' scores, then candidates
@@ -593,10 +606,10 @@ int prefill_one(const Dims& dm, const void* Q, const void* K, const void* V,
 
 }  // namespace
 
-SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, const void* V,
-                          const int32_t* page_table, float* Kbar, int32_t kbar_valid_blocks,
-                          void* O, float* lse, void* ws, size_t ws_bytes, int32_t* status,
-                          sgqa_stream_t stream) {
+SGQA_API int sgqa_prefill_ex(const sgqa_params* p, const void* Q, const void* K, const void* V,
+                             const sgqa_index_inputs* idx, const int32_t* page_table,
+                             float* Kbar, int32_t kbar_valid_blocks, void* O, float* lse,
+                             void* ws, size_t ws_bytes, int32_t* status, sgqa_stream_t stream) {
   Dims dm;
   int rc = derive(p, &dm);
   if (rc != SGQA_OK) return rc;
@@ -604,20 +617,33 @@ SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, co
       Kbar == nullptr || kbar_valid_blocks < 0 || kbar_valid_blocks > dm.nblk ||
       ((dm.ps > 0) != (page_table != nullptr)))
     return SGQA_ERR_INVALID_ARG;
-  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(Kbar))
+  const void* Qidx = idx ? idx->Qidx : nullptr;
+  const void* Kidx = idx ? idx->Kidx : nullptr;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(Kbar) ||
+      (Qidx && !aligned16(Qidx)) || (Kidx && !aligned16(Kidx)))
     return SGQA_ERR_ALIGNMENT;
   if (ws == nullptr || ws_bytes < sgqa_workspace_bytes(p, SGQA_WS_PREFILL))
     return SGQA_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const SeqStride ss = seq_stride(dm);
+  const int64_t qidx_bytes = dm.T * dm.Hkv * dm.d * dm.elem;
   for (int64_t b = 0; b < dm.batch; ++b) {
     rc = prefill_one(dm, at_bytes(Q, b, ss.q_bytes), at_bytes(K, b, ss.kv_bytes),
-                     at_bytes(V, b, ss.kv_bytes), at_b(page_table, b, ss.pt),
+                     at_bytes(V, b, ss.kv_bytes), at_bytes(Qidx, b, qidx_bytes),
+                     at_bytes(Kidx, b, ss.kv_bytes), at_b(page_table, b, ss.pt),
                      at_b(Kbar, b, ss.kbar), kbar_valid_blocks, at_bytes(O, b, ss.q_bytes),
                      at_b(lse, b, ss.lse), ws, status, st);
     if (rc != SGQA_OK) return rc;
   }
   return SGQA_OK;
+}
+
+SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, const void* V,
+                          const int32_t* page_table, float* Kbar, int32_t kbar_valid_blocks,
+                          void* O, float* lse, void* ws, size_t ws_bytes, int32_t* status,
+                          sgqa_stream_t stream) {
+  return sgqa_prefill_ex(p, Q, K, V, nullptr, page_table, Kbar, kbar_valid_blocks, O, lse, ws,
+                         ws_bytes, status, stream);
 }
 
 SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int32_t* launches) {

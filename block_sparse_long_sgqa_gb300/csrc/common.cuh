@@ -389,6 +389,12 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return d;
 }
 
+// fp32 bits rounded to the nearest bf16 value (ties to even), as fp32 bits.
+// Finite inputs only (the indexer's scores).
+__device__ __forceinline__ uint32_t bf16_round_bits(uint32_t u) {
+  return (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

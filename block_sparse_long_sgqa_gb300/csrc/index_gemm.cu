@@ -36,6 +36,10 @@
 // a threshold are stored in full.  Refill mode scores only listed row tiles
 // (those whose candidates could not decide a row), counting its items on the
 // device.
+//
+// The bf16 indexer (SGQA_INDEX_BF16) runs every mode with the single product
+// hi * hi and rounds each score to bf16 (nearest even) as it leaves TMEM, so
+// masks, thresholds, candidates and stored rows all see the rounded scores.
 #include <algorithm>
 #include <cstring>
 
@@ -74,6 +78,8 @@ struct IdxArgs {
   int64_t nblk_full;  // complete blocks of the call (bounds nh)
   int B, Hkv;
   int sample;      // columns are the sampled blocks: a row has (nh / 64) * 8 of them
+  int single;      // one product hi * hi (sampled mode, and the bf16 indexer)
+  int round_bf16;  // scores rounded to bf16 (nearest even) before any use
   int64_t total;   // work items of the launch
   int fill_tail;   // write -inf for the columns past a row tile's last item
   int tma_store;   // scores rows are 16-byte multiples: store through the tensor map
@@ -227,22 +233,22 @@ __global__ void __launch_bounds__(320, 1)
       for (int64_t k = 0; k < hi - lo; ++k, item_next(a, w)) {
         const int s = (int)(k % C::STAGES);
         if (!mbar_wait(&b_empty[s], (uint32_t)((k / C::STAGES) & 1) ^ 1, ab, status, 101)) break;
-        // sampled mode: the hi halves only (one product)
-        mbar_expect_tx(&b_full[s], a.sample ? C::B_BYTES : C::STAGE_BYTES);
+        // one product: the hi halves only
+        mbar_expect_tx(&b_full[s], a.single ? C::B_BYTES : C::STAGE_BYTES);
         uint8_t* sb = smem + C::OFF_B + s * C::STAGE_BYTES;
         const int32_t brow = (int32_t)(w.g * a.nblk + w.n * C::BN);
         for (int c = 0; c < C::KC; ++c) {
           tma_load_2d(sb + c * C::B_TILE, &mk_hi, &b_full[s], c * 64, brow);
-          if (!a.sample) tma_load_2d(sb + C::B_BYTES + c * C::B_TILE, &mk_lo, &b_full[s], c * 64, brow);
+          if (!a.single) tma_load_2d(sb + C::B_BYTES + c * C::B_TILE, &mk_lo, &b_full[s], c * 64, brow);
         }
         ++issued[s];
         if (w.rt != cur_rt || w.g != cur_g) {  // new query operand
           if (a_loads > 0 && !mbar_wait(a_empty, (a_loads - 1) & 1, ab, status, 100)) break;
-          mbar_expect_tx(a_full, a.sample ? C::A_BYTES : 2 * C::A_BYTES);
+          mbar_expect_tx(a_full, a.single ? C::A_BYTES : 2 * C::A_BYTES);
           const int32_t arow = (int32_t)(w.g * a.nq + w.rt * C::BM);
           for (int c = 0; c < C::KC; ++c) {
             tma_load_2d(smem + C::OFF_AHI + c * C::A_TILE, &mq_hi, a_full, c * 64, arow);
-            if (!a.sample) tma_load_2d(smem + C::OFF_ALO + c * C::A_TILE, &mq_lo, a_full, c * 64, arow);
+            if (!a.single) tma_load_2d(smem + C::OFF_ALO + c * C::A_TILE, &mq_lo, a_full, c * 64, arow);
           }
           ++a_loads;
           cur_rt = w.rt;
@@ -288,7 +294,7 @@ __global__ void __launch_bounds__(320, 1)
           const uint64_t bhi = sdesc_sw128(b_hi + boff, 16, 1024);
           const uint64_t blo = sdesc_sw128(b_lo + boff, 16, 1024);
           umma_f16(d_t, ahi, bhi, idesc, kk > 0 ? 1u : 0u);
-          if (!a.sample) {
+          if (!a.single) {
             umma_f16(d_t, ahi, blo, idesc, 1u);
             umma_f16(d_t, alo, bhi, idesc, 1u);
           }
@@ -343,6 +349,13 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        if (a.round_bf16) {  // the bf16 indexer: every score rounded before any use
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            va[i] = bf16_round_bits(va[i]);
+            vb[i] = bf16_round_bits(vb[i]);
+          }
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t(&v)[32] = h == 0 ? va : vb;
@@ -491,6 +504,8 @@ int launch_impl(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* q
   a.q_offset = dm.off;
   a.nblk_full = dm.nblk;
   a.sample = mode.sample ? 1 : 0;
+  a.single = (mode.sample || dm.index_bf16) ? 1 : 0;
+  a.round_bf16 = (!mode.sample && dm.index_bf16) ? 1 : 0;
   a.nblk = mode.sample ? sampled_cols(dm) : dm.nblk;
   a.B = dm.B;
   a.Hkv = dm.Hkv;

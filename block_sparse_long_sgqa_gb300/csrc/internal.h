@@ -22,6 +22,7 @@ struct Dims {
   float scale;               // softmax scale
   int elem;                  // bytes per Q/K/V element
   int batch;                 // sequences in the call (processed one after another)
+  int index_bf16;            // SGQA_INDEX_BF16: one bf16 product, scores rounded to bf16
 };
 
 // Validate `p` and fill `dm`; returns SGQA_OK or an error code.

@@ -27,12 +27,13 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CUDA = 0
 ERR_CAPACITY, ERR_TIMEOUT, ERR_BOUNDS = 6, 7, 8
 BF16, FP32 = 0, 1
 UNION_MASKED, UNION_FULL = 0, 1
+INDEX_SPLIT, INDEX_BF16 = 0, 1
 WS_INDEX_SCORES, WS_TOPK_UNION, WS_SPARSE_ATTN, WS_PREFILL = 1, 2, 3, 4
 DEBUG_STALL = 0x5354414C  # SGQA_DEBUG_STALL: written into word 3 of a status buffer
 
 EXPORTED = ("sgqa_workspace_bytes", "sgqa_union_capacity", "sgqa_block_merge", "sgqa_index_scores",
             "sgqa_topk_union", "sgqa_topk_union_noalloc", "sgqa_sparse_attn_fwd", "sgqa_prefill",
-            "sgqa_prefill_plan",
+            "sgqa_prefill_ex", "sgqa_prefill_plan",
             "sgqa_set_launch_log", "sgqa_reset_status", "sgqa_read_status", "sgqa_status_string",
             "sgqa_version")
 (K_MERGE, K_SPLIT, K_INDEX_QUERY, K_INDEX_SCORES, K_TOPK_UNION, K_ATTN, K_STAGE, K_TILE_UNION,
@@ -46,10 +47,15 @@ class Params(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "seq_q", "seq_kv", "q_offset", "n_q_heads", "n_kv_heads", "head_dim", "block_size",
         "topk_tokens", "tile_q", "page_size", "dtype", "union_mode")] + [
-        ("softmax_scale", ctypes.c_float), ("batch", ctypes.c_int32)]
+        ("softmax_scale", ctypes.c_float), ("batch", ctypes.c_int32),
+        ("index_mode", ctypes.c_int32)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class IndexInputs(ctypes.Structure):
+    _fields_ = [("Qidx", ctypes.c_void_p), ("Kidx", ctypes.c_void_p)]
 
 
 class LaunchLog(ctypes.Structure):
@@ -77,6 +83,8 @@ _lib.sgqa_topk_union_noalloc.argtypes = [_P, _vp, _i32, _i32, _vp, _vp, _vp, _vp
 _lib.sgqa_sparse_attn_fwd.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                       _vp, _vp]
 _lib.sgqa_prefill.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp, _vp]
+_lib.sgqa_prefill_ex.argtypes = [_P, _vp, _vp, _vp, ctypes.POINTER(IndexInputs), _vp, _vp, _i32,
+                                 _vp, _vp, _vp, _sz, _vp, _vp]
 _lib.sgqa_prefill_plan.argtypes = [_P, ctypes.POINTER(_i64), ctypes.POINTER(_i32)]
 _lib.sgqa_set_launch_log.argtypes = [ctypes.POINTER(LaunchLog)]
 _lib.sgqa_reset_status.argtypes = [_vp, _vp]
@@ -86,23 +94,25 @@ _lib.sgqa_status_string.restype = ctypes.c_char_p
 _lib.sgqa_version.restype = ctypes.c_int
 for _f in ("sgqa_block_merge", "sgqa_index_scores", "sgqa_topk_union", "sgqa_topk_union_noalloc",
            "sgqa_sparse_attn_fwd",
-           "sgqa_prefill", "sgqa_prefill_plan", "sgqa_set_launch_log", "sgqa_reset_status",
+           "sgqa_prefill", "sgqa_prefill_ex", "sgqa_prefill_plan", "sgqa_set_launch_log", "sgqa_reset_status",
            "sgqa_read_status"):
     getattr(_lib, _f).restype = ctypes.c_int
 
 
 def params(seq_q, seq_kv, q_offset, n_q_heads, n_kv_heads, head_dim, block_size, topk_tokens,
            tile_q, page_size=0, dtype=BF16, union_mode=UNION_MASKED, softmax_scale=0.0,
-           batch=1) -> Params:
+           batch=1, index_mode=INDEX_SPLIT) -> Params:
     return Params(seq_q, seq_kv, q_offset, n_q_heads, n_kv_heads, head_dim, block_size,
-                  topk_tokens, tile_q, page_size, dtype, union_mode, softmax_scale, batch)
+                  topk_tokens, tile_q, page_size, dtype, union_mode, softmax_scale, batch,
+                  index_mode)
 
 
-def params_for(wl, union_mode=UNION_MASKED, batch=1) -> Params:
+def params_for(wl, union_mode=UNION_MASKED, batch=1, index_mode=INDEX_SPLIT) -> Params:
     """Params of a synth.Workload (batch sequences of its shape)."""
     return params(wl.seq_q, wl.seq_kv, wl.q_offset, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
                   wl.block_size, wl.topk_tokens, wl.tile_q, wl.page_size,
-                  BF16 if wl.dtype == "bf16" else FP32, union_mode, batch=batch)
+                  BF16 if wl.dtype == "bf16" else FP32, union_mode, batch=batch,
+                  index_mode=index_mode)
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -201,6 +211,17 @@ def sgqa_prefill(p, Q, K, V, Kbar, O, lse, ws, page_table=None, kbar_valid_block
                              kbar_valid_blocks, _ptr(O), _ptr(lse), _ptr(ws),
                              ws.numel() * ws.element_size(), _ptr(status), _stream(stream)),
            "sgqa_prefill")
+
+
+def sgqa_prefill_ex(p, Q, K, V, Kbar, O, lse, ws, Qidx=None, Kidx=None, page_table=None,
+                    kbar_valid_blocks=0, status=None, stream=None):
+    """sgqa_prefill with separate index queries [T][Hkv][d] and/or index keys (K's layout)."""
+    idx = IndexInputs(None if Qidx is None else _ptr(Qidx).value,
+                      None if Kidx is None else _ptr(Kidx).value)
+    _check(_lib.sgqa_prefill_ex(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), ctypes.byref(idx),
+                                _ptr(page_table), _ptr(Kbar), kbar_valid_blocks, _ptr(O), _ptr(lse),
+                                _ptr(ws), ws.numel() * ws.element_size(), _ptr(status),
+                                _stream(stream)), "sgqa_prefill_ex")
 
 
 def sgqa_prefill_plan(p):

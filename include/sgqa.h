@@ -118,6 +118,17 @@ enum sgqa_dtype { SGQA_BF16 = 0, SGQA_FP32 = 1 };
  * lie strictly before its own block, plus its current block. */
 enum sgqa_union_mode { SGQA_UNION_MASKED = 0, SGQA_UNION_FULL = 1 };
 
+/* Precision of the indexer scores.
+ * SPLIT (default): fp32 scores from a two-term bf16 split of both operands
+ * (about 1e-5 of |qt| |Kbar|), so selections follow the exact scores.
+ * BF16: the lower-precision indexer: one bf16 product (both operands rounded
+ * to bf16 from their fp32 values, fp32 accumulation) with each score then
+ * rounded to bf16 (nearest even; stored in the fp32 score layout).  A third
+ * of the tensor work; selections are exact on these scores (ties to the
+ * lower block index) and differ from the SPLIT selection near the k-th score
+ * (its recall against SPLIT is what to measure). */
+enum sgqa_index_mode { SGQA_INDEX_SPLIT = 0, SGQA_INDEX_BF16 = 1 };
+
 typedef struct sgqa_params {
   int32_t seq_q;        /* T >= 1 */
   int32_t seq_kv;       /* Tkv >= q_offset + seq_q */
@@ -133,6 +144,7 @@ typedef struct sgqa_params {
   int32_t union_mode;   /* enum sgqa_union_mode */
   float softmax_scale;  /* 0 -> 1 / sqrt(head_dim) */
   int32_t batch;        /* sequences of these lengths in one call; 0 or 1 = one */
+  int32_t index_mode;   /* enum sgqa_index_mode */
 } sgqa_params;
 
 /* Workspace queries: `which` names the entry point. */
@@ -257,6 +269,30 @@ SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, co
                           const int32_t* page_table, float* Kbar, int32_t kbar_valid_blocks,
                           void* O, float* lse, void* ws, size_t ws_bytes, int32_t* status,
                           sgqa_stream_t stream);
+
+/* Separate index inputs for sgqa_prefill_ex (the index keys the Figure 3
+ * caption speaks of, and the query side of a separate index projection).
+ * Either pointer may be NULL.
+ *   Qidx: [seq_q][n_kv_heads][head_dim] (batch: an outer dimension), in the
+ *         dtype of Q: the index query of each KV group, used as is in place
+ *         of the mean of the group's query heads.
+ *   Kidx: the index keys, in K's layout and dtype (contiguous, or paged
+ *         through the same page table): the block merge reads them in place
+ *         of K, so Kbar holds their block means.  The attention still reads
+ *         K and V.
+ * Both must be 16-byte aligned. */
+typedef struct sgqa_index_inputs {
+  const void* Qidx;
+  const void* Kidx;
+} sgqa_index_inputs;
+
+/* sgqa_prefill with separate index inputs (idx may be NULL, or have NULL
+ * members, which then default as in sgqa_prefill).  With both NULL the
+ * results equal sgqa_prefill's bit for bit.  Same workspace. */
+SGQA_API int sgqa_prefill_ex(const sgqa_params* p, const void* Q, const void* K, const void* V,
+                             const sgqa_index_inputs* idx, const int32_t* page_table,
+                             float* Kbar, int32_t kbar_valid_blocks, void* O, float* lse,
+                             void* ws, size_t ws_bytes, int32_t* status, sgqa_stream_t stream);
 
 /* Plan of one sgqa_prefill call: queries per chunk (*chunk_queries) and the
  * number of kernel launches it enqueues (*launches).  Either pointer may be

@@ -46,6 +46,7 @@ def _load():
     lib.orc_merge_f64.argtypes = [vp, i64, i32, i32, i32, vp]
     lib.orc_index_query.argtypes = [vp, i64, i32, i32, i32, vp, i64, vp]
     lib.orc_scores.argtypes = [vp, vp, i64, i32, i32, i32, i64, vp, i64, vp]
+    lib.orc_scores_bf16.argtypes = [vp, vp, i64, i32, i32, i32, i64, vp, i64, vp]
     lib.orc_select.argtypes = [vp, i32, i64, i32, i32, i64, vp, i64, i64, vp]
     lib.orc_union.argtypes = [vp, i64, i32, i64, i32, i64, i64, vp, vp, vp]
     lib.orc_union.restype = i64
@@ -117,6 +118,20 @@ def scores(qt: np.ndarray, Kbar: np.ndarray, B: int, q_offset: int, rows) -> np.
     out = np.empty((Hkv, len(r), nblk), np.float64)
     _check(_load().orc_scores(_p(qt), _p(Kbar), nblk, Hkv, d, B, q_offset, _p(r), len(r), _p(out)),
            "scores")
+    return out
+
+
+def scores_bf16(qt32: np.ndarray, Kbar32: np.ndarray, B: int, q_offset: int, rows) -> np.ndarray:
+    """The bf16 indexer: qt32 [nrows][Hkv][d] and Kbar32 [Hkv][nblk][d] (fp32) ->
+    S [Hkv][nrows][nblk] fp32 holding bf16 values (operands and score rounded
+    to bf16, the products summed exactly), -inf where block j is not historical."""
+    qt32 = np.ascontiguousarray(qt32, np.float32)
+    Kbar32 = np.ascontiguousarray(Kbar32, np.float32)
+    Hkv, nblk, d = Kbar32.shape
+    r = np.ascontiguousarray(rows, np.int32)
+    out = np.empty((Hkv, len(r), nblk), np.float32)
+    _check(_load().orc_scores_bf16(_p(qt32), _p(Kbar32), nblk, Hkv, d, B, q_offset, _p(r), len(r),
+                                   _p(out)), "scores_bf16")
     return out
 
 
@@ -219,15 +234,17 @@ def dense_attn(Q, K, V, q_offset: int, scale: Optional[float] = None, rows=None)
     return O, lse
 
 
-def prefill_rows(Q, K, V, q_offset: int, B: int, Ks: int, rows, scale=None):
+def prefill_rows(Q, K, V, q_offset: int, B: int, Ks: int, rows, scale=None, Qidx=None, Kidx=None):
     """Mode-A prefill for a subset of query rows, end to end in fp64: merge,
     index query, scores, top-k, attention.  Returns (S, sel_rows, O, lse) with
-    S [Hkv][nrows][nblk], sel_rows [Hkv][nrows][Ks]."""
+    S [Hkv][nrows][nblk], sel_rows [Hkv][nrows][Ks].  Qidx [T][Hkv][d] and Kidx
+    (K's shape), when given, are the index queries and keys: the index query of
+    group g is Qidx[t][g] itself and the block keys are Kidx's block means."""
     T, H, d = Q.shape
     Tkv, Hkv, _ = K.shape
     r = np.ascontiguousarray(rows, np.int32)
-    Kbar = merge_f64(K, B)
-    qt = index_query(Q, Hkv, r)
+    Kbar = merge_f64(K if Kidx is None else Kidx, B)
+    qt = index_query(Q if Qidx is None else Qidx, Hkv, r)
     S = scores(qt, Kbar, B, q_offset, r)
     sel_rows = select(S, B, q_offset, r, Ks)
     # scatter the rows' selections into a full-size table for the attention step

@@ -139,6 +139,59 @@ int orc_scores(const double* qt, const double* Kbar, int64_t nblk, int Hkv, int 
 }
 
 /* ---------------------------------------------------------------------------
+ * Step 3, lower-precision variant: bf16 index scores.  The Step 5 pages leave
+ * the indexer's precision open; the DeepSeek-V4 notes (section on FP4 QAT)
+ * report that keeping index scores in bf16 instead of fp32 makes the top-k
+ * twice as fast at 99.7% recall.  Here both operands are rounded to bf16
+ * (nearest, ties to even) from their fp32 values, the products are summed
+ * exactly (each product of two bf16 values is exact in fp64, and so is the
+ * sum at these sizes), and the score is rounded to bf16 the same way.
+ * qt32 [nrows][Hkv][d] and Kbar32 [Hkv][nblk][d] are fp32; S [Hkv][nrows][nblk]
+ * is fp32 holding bf16 values, -inf where j >= nh(t_r).
+ * ------------------------------------------------------------------------- */
+static float round_bf16(double x) {
+  /* nearest bf16 value of x, ties to even, decided on the exact value x
+   * (its nearest fp32 value only locates the two bf16 neighbours) */
+  float f = (float)x; /* nearest fp32 */
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  const uint32_t base = u & 0xFFFF0000u;
+  uint32_t down = base, up = base + 0x10000u;
+  float fd, fu;
+  memcpy(&fd, &down, 4);
+  memcpy(&fu, &up, 4);
+  /* the two bf16 neighbours of x (fd, fu share the sign of f); pick the
+   * nearer by the exact distance, ties to the even mantissa */
+  const double dd = fabs(x - (double)fd), du = fabs(x - (double)fu);
+  if (dd < du) return fd;
+  if (du < dd) return fu;
+  return (down & 0x10000u) ? fu : fd;
+}
+
+int orc_scores_bf16(const float* qt32, const float* Kbar32, int64_t nblk, int Hkv, int d, int B,
+                    int64_t q_offset, const int32_t* rows, int64_t nrows,
+                    float* S /* [Hkv][nrows][nblk] */) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < nrows; ++r) {
+    const int64_t nh = (q_offset + rows[r]) / B;
+    for (int g = 0; g < Hkv; ++g) {
+      const float* q = qt32 + (r * Hkv + g) * (int64_t)d;
+      for (int64_t j = 0; j < nblk; ++j) {
+        float s = NEG_INF;
+        if (j < nh) {
+          const float* k = Kbar32 + ((int64_t)g * nblk + j) * d;
+          double acc = 0.0;
+          for (int i = 0; i < d; ++i) acc += (double)round_bf16(q[i]) * (double)round_bf16(k[i]);
+          s = round_bf16(acc);
+        }
+        S[((int64_t)g * nrows + r) * nblk + j] = s;
+      }
+    }
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------
  * Step 4: top-k block selection ("Trade-off between top-k and block size":
  * k tokens = k/B blocks).  Row r keeps min(Ks, nh) blocks under the total
  * order "larger score first, equal scores: lower block index first", and

@@ -480,3 +480,48 @@ def test_attn_bwd_invariants():
     c = _grid(45, d)
     dQ2, _, _ = oracle.sparse_attn_bwd(Q, K + c[None, None, :], V, dO, off, B, sel)
     np.testing.assert_allclose(dQ2, dQ, rtol=0, atol=1e-11)
+
+
+# --------------------------------------------------------------------------- bf16 indexer
+
+def _bf16_case_scores(q, k):
+    q = np.array(q, np.float32)[None, None, :]          # [1 row][1 group][d]
+    k = np.array(k, np.float32)[None, None, :]          # [1 group][1 block][d]
+    return oracle.scores_bf16(q, k, 1, 1, np.array([0], np.int32))[0, 0, 0]
+
+
+def test_scores_bf16_fixture():
+    """Hand-worked sums and tie cases of the bf16 indexer (tests/golden/scores_bf16.json)."""
+    for c in gold("scores_bf16.json")["cases"]:
+        assert _bf16_case_scores(c["q"], c["k"]) == np.float32(c["score"]), c
+
+
+def test_scores_bf16_operand_rounding_vs_torch():
+    """Against a unit key the score is the query element rounded to bf16:
+    compare with torch's own fp32 -> bfloat16 conversion."""
+    q = rnd(40, 64).astype(np.float32) * np.float32(37.0)
+    ref = torch.from_numpy(q).to(torch.bfloat16).float().numpy()
+    for i in range(64):
+        e = np.zeros(64, np.float32)
+        e[i] = 1.0
+        assert _bf16_case_scores(q, e) == ref[i], i
+
+
+def test_scores_bf16_integer_sums_vs_torch():
+    """Integer operands make every sum exact in fp32, so torch's fp32 ->
+    bfloat16 rounding of the exact dot product is the reference; also the
+    causal -inf pattern."""
+    rng = np.random.default_rng(41)
+    Hkv, nblk, d, B, off = 2, 40, 128, 4, 37
+    qt = rng.integers(-20, 21, size=(5, Hkv, d)).astype(np.float32)
+    kb = rng.integers(-20, 21, size=(Hkv, nblk, d)).astype(np.float32)
+    rows = np.array([0, 3, 50, 90, 120], np.int32)
+    S = oracle.scores_bf16(qt, kb, B, off, rows)
+    exact = np.einsum("rgi,gji->grj", qt.astype(np.float64), kb.astype(np.float64))
+    ref = torch.from_numpy(exact.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    nh = (off + rows) // B
+    for r in range(len(rows)):
+        n = min(nh[r], nblk)
+        assert np.array_equal(S[:, r, :n], ref[:, r, :n])
+        assert (S[:, r, n:] == -np.inf).all()
+    assert (np.abs(exact) > 512).any()  # sums large enough for the rounding to drop bits
