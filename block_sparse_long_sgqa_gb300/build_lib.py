@@ -13,7 +13,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsgqa.so")
 SOURCES = ["api.cu", "merge.cu", "index_gemm.cu", "topk_union.cu", "select_long.cu", "attn.cu",
-           "noalloc.cu"]
+           "attn_bwd.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 

@@ -371,6 +371,13 @@ SGQA_API size_t sgqa_workspace_bytes(const sgqa_params* p, int which) {
     case SGQA_WS_TOPK_UNION: c.take<int32_t>(topk_union_ws_bytes(dm, dm.T) / 4); break;
     case SGQA_WS_SPARSE_ATTN: carve_attn(c, dm); break;
     case SGQA_WS_PREFILL: carve_prefill(c, dm); break;
+    case SGQA_WS_ATTN_BWD: {
+      c.take<__nv_bfloat16>((size_t)kv_pack_elems(dm));
+      c.take<__nv_bfloat16>((size_t)kv_pack_elems(dm));
+      size_t a, b, f;
+      c.take<uint8_t>(attn_bwd_ws_bytes(dm, &a, &b, &f));
+      break;
+    }
     default: return 0;
   }
   return c.used + kAlign;  // slack to align the caller's base
@@ -511,6 +518,54 @@ SGQA_API int sgqa_sparse_attn_fwd(const sgqa_params* p, const void* Q, const voi
                             union_blk + b * ucap_b, union_mask + b * ucap_b,
                             at_bytes(O, b, ss.q_bytes), lse + b * ss.lse, 0, dm.ntiles, status,
                             st);
+    if (rc != SGQA_OK) return rc;
+  }
+  return SGQA_OK;
+}
+
+SGQA_API int sgqa_sparse_attn_bwd(const sgqa_params* p, const void* Q, const void* K,
+                                  const void* V, const int32_t* page_table,
+                                  const int64_t* union_off, const int32_t* union_len,
+                                  const int32_t* union_blk, const uint64_t* union_mask,
+                                  const void* O, const float* lse, const void* dO, float* dQ,
+                                  float* dK, float* dV, void* ws, size_t ws_bytes,
+                                  int32_t* status, sgqa_stream_t stream) {
+  Dims dm;
+  int rc = derive(p, &dm);
+  if (rc != SGQA_OK) return rc;
+  if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr || lse == nullptr ||
+      dO == nullptr || dQ == nullptr || dK == nullptr || dV == nullptr || union_off == nullptr ||
+      union_len == nullptr || union_blk == nullptr || union_mask == nullptr ||
+      ((dm.ps > 0) != (page_table != nullptr)))
+    return SGQA_ERR_INVALID_ARG;
+  if (dm.dtype != SGQA_BF16 || dm.B < 8 || (dm.G & (dm.G - 1)) != 0 ||
+      group_cap(dm) * dm.Hkv >= (int64_t(1) << 31))
+    return SGQA_ERR_UNSUPPORTED;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) ||
+      !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
+    return SGQA_ERR_ALIGNMENT;
+  if (ws == nullptr || ws_bytes < sgqa_workspace_bytes(p, SGQA_WS_ATTN_BWD))
+    return SGQA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Carve c(align_ws(ws));
+  __nv_bfloat16* Kp = c.take<__nv_bfloat16>((size_t)kv_pack_elems(dm));
+  __nv_bfloat16* Vp = c.take<__nv_bfloat16>((size_t)kv_pack_elems(dm));
+  size_t a0, b0, f0;
+  uint8_t* rest = c.take<uint8_t>(attn_bwd_ws_bytes(dm, &a0, &b0, &f0));
+  const SeqStride ss = seq_stride(dm);
+  const int64_t ucap_b = group_cap(dm) * dm.Hkv;
+  const int64_t kv_elems = dm.Tkv * dm.Hkv * dm.d;
+  for (int64_t b = 0; b < dm.batch; ++b) {
+    const int32_t* pt = at_b(page_table, b, ss.pt);
+    cudaError_t e = launch_kv_pack(dm, at_bytes(K, b, ss.kv_bytes), pt, Kp, st);
+    if (e == cudaSuccess) e = launch_kv_pack(dm, at_bytes(V, b, ss.kv_bytes), pt, Vp, st);
+    if (e != cudaSuccess) return SGQA_ERR_CUDA;
+    rc = launch_attn_bwd(dm, static_cast<const __nv_bfloat16*>(at_bytes(Q, b, ss.q_bytes)), Kp, Vp,
+                         union_off + b * ss.tiles, union_len + b * ss.tiles,
+                         union_blk + b * ucap_b, union_mask + b * ucap_b,
+                         at_bytes(O, b, ss.q_bytes), lse + b * ss.lse,
+                         at_bytes(dO, b, ss.q_bytes), dQ + b * (dm.T * dm.H * dm.d),
+                         dK + b * kv_elems, dV + b * kv_elems, rest, status, st);
     if (rc != SGQA_OK) return rc;
   }
   return SGQA_OK;

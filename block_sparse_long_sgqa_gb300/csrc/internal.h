@@ -160,4 +160,14 @@ int launch_sparse_attn(const Dims& dm, const __nv_bfloat16* Q, const __nv_bfloat
                        const uint64_t* union_mask, void* O, float* lse, int64_t tau_begin,
                        int64_t tau_end, int32_t* status, cudaStream_t st);
 
+// Attention backward over the union lists of the whole call (B >= 8, bf16):
+// K/V from their block-packed copies; ws holds D, the per-stage tile bitmaps
+// and first slots, laid out by attn_bwd_ws_bytes (offsets returned).
+size_t attn_bwd_ws_bytes(const Dims& dm, size_t* off_D, size_t* off_bits, size_t* off_first);
+int launch_attn_bwd(const Dims& dm, const __nv_bfloat16* Q, const __nv_bfloat16* Kp,
+                    const __nv_bfloat16* Vp, const int64_t* union_off, const int32_t* union_len,
+                    const int32_t* union_blk, const uint64_t* union_mask, const void* O,
+                    const float* lse, const void* dO, float* dQ, float* dK, float* dV, void* ws,
+                    int32_t* status, cudaStream_t st);
+
 }  // namespace sgqa

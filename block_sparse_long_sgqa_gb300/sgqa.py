@@ -28,19 +28,20 @@ ERR_CAPACITY, ERR_TIMEOUT, ERR_BOUNDS = 6, 7, 8
 BF16, FP32 = 0, 1
 UNION_MASKED, UNION_FULL = 0, 1
 INDEX_SPLIT, INDEX_BF16 = 0, 1
-WS_INDEX_SCORES, WS_TOPK_UNION, WS_SPARSE_ATTN, WS_PREFILL = 1, 2, 3, 4
+WS_INDEX_SCORES, WS_TOPK_UNION, WS_SPARSE_ATTN, WS_PREFILL, WS_ATTN_BWD = 1, 2, 3, 4, 5
 DEBUG_STALL = 0x5354414C  # SGQA_DEBUG_STALL: written into word 3 of a status buffer
 
 EXPORTED = ("sgqa_workspace_bytes", "sgqa_union_capacity", "sgqa_block_merge", "sgqa_index_scores",
-            "sgqa_topk_union", "sgqa_topk_union_noalloc", "sgqa_sparse_attn_fwd", "sgqa_prefill",
+            "sgqa_topk_union", "sgqa_topk_union_noalloc", "sgqa_sparse_attn_fwd",
+            "sgqa_sparse_attn_bwd", "sgqa_prefill",
             "sgqa_prefill_ex", "sgqa_prefill_plan",
             "sgqa_set_launch_log", "sgqa_reset_status", "sgqa_read_status", "sgqa_status_string",
             "sgqa_version")
 (K_MERGE, K_SPLIT, K_INDEX_QUERY, K_INDEX_SCORES, K_TOPK_UNION, K_ATTN, K_STAGE, K_TILE_UNION,
- K_SAMPLE_SCORES, K_ROW_TAU) = (1, 2, 3, 4, 5, 6, 7, 8, 9, 10)
+ K_SAMPLE_SCORES, K_ROW_TAU, K_ATTN_BWD) = (1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11)
 KERNEL_NAMES = {1: "merge", 2: "split", 3: "index_query", 4: "index_scores", 5: "topk_union",
                 6: "sparse_attn", 7: "stage_bf16", 8: "tile_union", 9: "sample_scores",
-                10: "row_tau"}
+                10: "row_tau", 11: "sparse_attn_bwd"}
 
 
 class Params(ctypes.Structure):
@@ -82,6 +83,8 @@ _lib.sgqa_topk_union.argtypes = [_P, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _
 _lib.sgqa_topk_union_noalloc.argtypes = [_P, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp]
 _lib.sgqa_sparse_attn_fwd.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                       _vp, _vp]
+_lib.sgqa_sparse_attn_bwd.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                      _vp, _vp, _vp, _vp, _sz, _vp, _vp]
 _lib.sgqa_prefill.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp, _vp]
 _lib.sgqa_prefill_ex.argtypes = [_P, _vp, _vp, _vp, ctypes.POINTER(IndexInputs), _vp, _vp, _i32,
                                  _vp, _vp, _vp, _sz, _vp, _vp]
@@ -93,7 +96,7 @@ _lib.sgqa_status_string.argtypes = [ctypes.c_int]
 _lib.sgqa_status_string.restype = ctypes.c_char_p
 _lib.sgqa_version.restype = ctypes.c_int
 for _f in ("sgqa_block_merge", "sgqa_index_scores", "sgqa_topk_union", "sgqa_topk_union_noalloc",
-           "sgqa_sparse_attn_fwd",
+           "sgqa_sparse_attn_fwd", "sgqa_sparse_attn_bwd",
            "sgqa_prefill", "sgqa_prefill_ex", "sgqa_prefill_plan", "sgqa_set_launch_log", "sgqa_reset_status",
            "sgqa_read_status"):
     getattr(_lib, _f).restype = ctypes.c_int
@@ -203,6 +206,16 @@ def sgqa_sparse_attn_fwd(p, Q, K, V, union_off, union_len, union_blk, union_mask
                                      _ptr(union_mask), _ptr(O), _ptr(lse), _ptr(ws),
                                      0 if ws is None else ws.numel() * ws.element_size(),
                                      _ptr(status), _stream(stream)), "sgqa_sparse_attn_fwd")
+
+
+def sgqa_sparse_attn_bwd(p, Q, K, V, union_off, union_len, union_blk, union_mask, O, lse, dO,
+                         dQ, dK, dV, ws, page_table=None, status=None, stream=None):
+    """Gradients of the main-path attention: dQ [T][H][d], dK and dV [Tkv][Hkv][d], fp32."""
+    _check(_lib.sgqa_sparse_attn_bwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(page_table),
+                                     _ptr(union_off), _ptr(union_len), _ptr(union_blk),
+                                     _ptr(union_mask), _ptr(O), _ptr(lse), _ptr(dO), _ptr(dQ),
+                                     _ptr(dK), _ptr(dV), _ptr(ws), ws.numel() * ws.element_size(),
+                                     _ptr(status), _stream(stream)), "sgqa_sparse_attn_bwd")
 
 
 def sgqa_prefill(p, Q, K, V, Kbar, O, lse, ws, page_table=None, kbar_valid_blocks=0, status=None,

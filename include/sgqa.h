@@ -152,7 +152,8 @@ enum sgqa_ws_kind {
   SGQA_WS_INDEX_SCORES = 1,
   SGQA_WS_TOPK_UNION = 2,
   SGQA_WS_SPARSE_ATTN = 3,
-  SGQA_WS_PREFILL = 4
+  SGQA_WS_PREFILL = 4,
+  SGQA_WS_ATTN_BWD = 5
 };
 
 /* Bytes of device workspace the entry point `which` needs for these params
@@ -234,6 +235,30 @@ SGQA_API int sgqa_sparse_attn_fwd(const sgqa_params* p, const void* Q, const voi
                                   float* lse, void* ws, size_t ws_bytes, int32_t* status,
                                   sgqa_stream_t stream);
 
+/* Backward of step 6: the gradients of the main-path attention, for training
+ * (the Step 5 pages use the layer in training as well as inference).  With
+ * the softmax weights P of each (query, head) row over the same allowed
+ * positions as sgqa_sparse_attn_fwd (same params, union_mode and union
+ * arrays), O and lse the forward's outputs and dO the gradient of O:
+ *   D = rowsum(dO * O),  dS = P * (dO V^T - D),
+ *   dQ = scale * dS K,   dK = scale * dS^T Q,   dV = P^T dO,
+ * dK and dV summed over every row (all heads of the group) that attends the
+ * key.  P is recomputed from lse.  Outputs are fp32: dQ [seq_q][n_q_heads]
+ * [head_dim], dK and dV [seq_kv][n_kv_heads][head_dim] at logical positions
+ * (also for a paged K/V), every element written (0 for keys nothing attends).
+ * Deterministic: each output element is accumulated in one place in a fixed
+ * order.  Supported: bf16 inputs, block_size 8 or 16, n_q_heads / n_kv_heads
+ * a power of two (SGQA_ERR_UNSUPPORTED otherwise).  Workspace:
+ * sgqa_workspace_bytes(p, SGQA_WS_ATTN_BWD) (block-packed K and V, D, and the
+ * key stages each union tile attends). */
+SGQA_API int sgqa_sparse_attn_bwd(const sgqa_params* p, const void* Q, const void* K,
+                                  const void* V, const int32_t* page_table,
+                                  const int64_t* union_off, const int32_t* union_len,
+                                  const int32_t* union_blk, const uint64_t* union_mask,
+                                  const void* O, const float* lse, const void* dO, float* dQ,
+                                  float* dK, float* dV, void* ws, size_t ws_bytes,
+                                  int32_t* status, sgqa_stream_t stream);
+
 /* Top-k and tile union without a workspace, for callers that cannot
  * allocate device memory (code running inside another framework's memory
  * pool, serving loops whose device memory is carved once up front, runtimes
@@ -310,7 +335,8 @@ enum sgqa_kernel_kind {
   SGQA_K_STAGE = 7,        /* attention operand staging: bf16 rounding, K/V block packing */
   SGQA_K_TILE_UNION = 8,   /* tile union and member masks */
   SGQA_K_SAMPLE_SCORES = 9, /* indexer GEMM over the sampled blocks (fused prefill) */
-  SGQA_K_ROW_TAU = 10       /* candidate thresholds from the sampled scores */
+  SGQA_K_ROW_TAU = 10,      /* candidate thresholds from the sampled scores */
+  SGQA_K_ATTN_BWD = 11      /* attention backward (dQ; dK and dV) */
 };
 
 /* Optional launch log for measurement.  While a log is installed, every

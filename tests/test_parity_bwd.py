@@ -1,0 +1,98 @@
+"""GPU parity of the attention backward (sgqa_sparse_attn_bwd) against the
+oracle's fp64 backward (orc_sparse_attn_bwd, pinned in test_oracle_pins.py by
+finite differences, autograd on the dense case and invariants).
+
+The GPU backward is fed what a training step has: the GPU forward's O (bf16)
+and log-sum-exp on the same block lists, and a seeded upstream gradient dO.
+Its tensor cores see bf16 operands (Q, K, V, dO, and P and dS rounded to bf16
+for the products), so its error against fp64 is bounded like the forward's:
+max-abs within 2.5e-2 and mean-abs within 2.5e-3 of each gradient's largest
+magnitude.  Results are deterministic (each gradient element is summed in one
+place in a fixed order): two calls agree bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_long_sgqa_gb300 import synth
+from helpers import dev_inputs, to_dev, widened
+from test_parity_steps import SMALL, _upload_union, inputs
+
+pytestmark = pytest.mark.gpu
+
+CASES = ["b8", "b16", "w16_g8", "d64_g2", "paged", "needles", "few_b8", "few_b16_paged"]
+TOL_MAX, TOL_MEAN = 2.5e-2, 2.5e-3
+
+
+@pytest.fixture(scope="module")
+def s():
+    from block_sparse_long_sgqa_gb300 import sgqa
+
+    return sgqa
+
+
+def run_bwd(s, p, d, union, O, lse, dO, wl):
+    dQ = torch.empty(wl.seq_q, wl.n_q_heads, wl.head_dim, device="cuda")
+    dK = torch.full((wl.seq_kv, wl.n_kv_heads, wl.head_dim), float("nan"), device="cuda")
+    dV = torch.full_like(dK, float("nan"))
+    st = s.new_status()
+    s.sgqa_sparse_attn_bwd(p, d["Q"], d["K"], d["V"], *union, O, lse, dO, dQ, dK, dV,
+                           s.alloc_workspace(p, s.WS_ATTN_BWD), page_table=d["page_table"],
+                           status=st)
+    code, det = s.read_status(st)
+    assert code == 0, (s.status_string(code), det)
+    return dQ, dK, dV
+
+
+def close(got, ref, name):
+    got = got.double().cpu().numpy()
+    scale = max(1e-30, float(np.abs(ref).max()))
+    err = np.abs(got - ref)
+    assert np.isfinite(got).all(), name
+    assert err.max() <= TOL_MAX * scale, (name, err.max() / scale)
+    assert err.mean() <= TOL_MEAN * scale, (name, err.mean() / scale)
+    return err.max() / scale, err.mean() / scale
+
+
+@pytest.mark.parametrize("name", CASES)
+@pytest.mark.parametrize("mode", [0, 1])
+def test_attn_bwd_vs_oracle(s, name, mode):
+    wl, inp = SMALL[name], inputs(name)
+    p = s.params_for(wl, union_mode=mode)
+    rows = np.arange(wl.seq_q, dtype=np.int32)
+    Q, K, V = widened(inp)
+    S = oracle.scores(oracle.index_query(Q, wl.n_kv_heads, rows), oracle.merge_f64(K, wl.block_size),
+                      wl.block_size, wl.q_offset, rows)
+    sel = oracle.select(S, wl.block_size, wl.q_offset, rows, wl.k_blocks)
+    csr = oracle.union(sel, wl.tile_q, wl.n_blocks)
+    d = dev_inputs(inp)
+    union = _upload_union(*csr, wl.n_kv_heads, 0)
+    O, lse = s.alloc_outputs(p)
+    st = s.new_status()
+    s.sgqa_sparse_attn_fwd(p, d["Q"], d["K"], d["V"], *union, O, lse, page_table=d["page_table"],
+                           ws=s.alloc_workspace(p, s.WS_SPARSE_ATTN), status=st)
+    assert s.read_status(st)[0] == 0
+    rng = np.random.default_rng(77)
+    dOb = synth.to_bf16_bits(rng.standard_normal((wl.seq_q, wl.n_q_heads, wl.head_dim)).astype(np.float32))
+    dO = to_dev(dOb)
+    dQ, dK, dV = run_bwd(s, p, d, union, O, lse, dO, wl)
+    dQ64, dK64, dV64 = oracle.sparse_attn_bwd(Q, K, V, synth.widen(dOb).astype(np.float64),
+                                              wl.q_offset, wl.block_size, sel, mode, csr, wl.tile_q)
+    close(dQ, dQ64, "dQ")
+    close(dK, dK64, "dK")
+    close(dV, dV64, "dV")
+    # deterministic: a second call gives the same bits
+    dQ2, dK2, dV2 = run_bwd(s, p, d, union, O, lse, dO, wl)
+    assert torch.equal(dQ, dQ2) and torch.equal(dK, dK2) and torch.equal(dV, dV2)
+
+
+def test_attn_bwd_rejects_unsupported(s):
+    """B < 8 and fp32 inputs are rejected on the host before anything runs."""
+    import ctypes
+
+    vp = ctypes.c_void_p
+    for wl in (SMALL["b4"], SMALL["tiny_2k"]):
+        p = s.params_for(wl)
+        args = [ctypes.byref(p)] + [vp(0x1000)] * 3 + [None] + [vp(0x1000)] * 11 + [1 << 40, None, None]
+        assert s._lib.sgqa_sparse_attn_bwd(*args) == s.ERR_UNSUPPORTED
