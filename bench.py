@@ -56,6 +56,8 @@ def parse_args(argv=None):
     ap.add_argument("--index-mode", choices=["split", "bf16"], default="split",
                     help="indexer precision: fp32 scores from a bf16 split (exact selection) "
                          "or bf16 scores (one product; recall against split reported)")
+    ap.add_argument("--no-bwd", action="store_true",
+                    help="skip timing the attention backward on the workload's selection")
     ap.add_argument("--no-stress", action="store_true",
                     help="skip the i.i.d. query-noise run reported beside the headline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -387,6 +389,79 @@ def quality(wl, inp, Q, K, V, pt, Kbar, lse, dev, nq_max=1024, index_mode=0):
     return out
 
 
+def time_backward(wl, p, Q, K, V, pt, Kbar, alg, tensor_peak, dev, steps=3):
+    """The attention's forward alone and its backward (sgqa_sparse_attn_bwd)
+    on the union lists of the whole workload (built by the step entry points
+    on ranges of 4096 queries), with a seeded upstream gradient dO; CUDA
+    events on the launch stream.  Algorithmic FLOPs: the forward's two
+    products over each query's own keys, the backward's five (S, dP, dV, dK,
+    dQ: 2.5 times the forward)."""
+    import torch
+
+    from block_sparse_long_sgqa_gb300 import sgqa
+
+    u = sgqa.alloc_union(p, dev)
+    nblk = wl.seq_kv // wl.block_size
+    st = sgqa.new_status(dev)
+    ws_t = sgqa.alloc_workspace(p, sgqa.WS_TOPK_UNION, dev)
+    ws_i = sgqa.alloc_workspace(p, sgqa.WS_INDEX_SCORES, dev)
+    for q0 in range(0, wl.seq_q, 4096):
+        q1 = min(wl.seq_q, q0 + 4096)
+        sc = torch.empty(wl.n_kv_heads, q1 - q0, nblk, device=dev)
+        sgqa.sgqa_index_scores(p, Q, Kbar, q0, q1, sc, ws_i)
+        sgqa.sgqa_topk_union(p, sc, q0, q1, None, *u, ws=ws_t, status=st)
+        del sc
+    del ws_t, ws_i
+    O2, lse2 = sgqa.alloc_outputs(p, dev)
+    ws_f = sgqa.alloc_workspace(p, sgqa.WS_SPARSE_ATTN, dev)
+    ws_b = sgqa.alloc_workspace(p, sgqa.WS_ATTN_BWD, dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20261299)
+    dO = torch.randn(O2.shape, generator=gen, device=dev).to(torch.bfloat16)
+    dQ = torch.empty(O2.shape, dtype=torch.float32, device=dev)
+    dK = torch.empty(wl.seq_kv, wl.n_kv_heads, wl.head_dim, dtype=torch.float32, device=dev)
+    dV = torch.empty_like(dK)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        sgqa.sgqa_sparse_attn_fwd(p, Q, K, V, *u, O2, lse2, page_table=pt, ws=ws_f, status=st)
+
+    def bwd():
+        sgqa.sgqa_sparse_attn_bwd(p, Q, K, V, *u, O2, lse2, dO, dQ, dK, dV, ws_b, page_table=pt,
+                                  status=st)
+
+    out = {}
+    for name, fn in (("forward", fwd), ("backward", bwd)):
+        fn()
+        torch.cuda.synchronize(dev)
+        log = sgqa.launch_log(steps * 16)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with log:
+            e0.record(stream)
+            for _ in range(steps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+        out[name] = {"ms": e0.elapsed_time(e1) / steps, "launches": log.entries()}
+    code, det = sgqa.read_status(st)
+    if code != 0:
+        raise RuntimeError(f"device status in the backward timing: {sgqa.status_string(code)} ({det})")
+    f_fwd = alg["attn_flops"]
+    bl = [t for k, t in out["backward"]["launches"] if k == sgqa.K_ATTN_BWD]
+    res = {"workload": "the prefill's own selection (whole-call union lists), seeded dO",
+           "fwd_attn_ms": out["forward"]["ms"], "bwd_ms": out["backward"]["ms"],
+           "bwd_flops_alg": 2.5 * f_fwd,
+           "bwd_tflops_alg": 2.5 * f_fwd / (out["backward"]["ms"] * 1e-3) / 1e12,
+           "fwd_tflops_alg": f_fwd / (out["forward"]["ms"] * 1e-3) / 1e12,
+           "peak_tflops": tensor_peak}
+    res["bwd_frac"] = res["bwd_tflops_alg"] / tensor_peak
+    res["fwd_frac"] = res["fwd_tflops_alg"] / tensor_peak
+    if len(bl) >= 2 * steps:  # per call: the dQ kernel, then the dK/dV kernel
+        res["dq_ms"] = sum(bl[0::2]) / steps
+        res["dkv_ms"] = sum(bl[1::2]) / steps
+    return res
+
+
 def config_of(wl, args):
     return {"workload": wl.name, "seq_q": wl.seq_q, "seq_kv": wl.seq_kv, "q_offset": wl.q_offset,
             "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
@@ -580,6 +655,12 @@ def main(argv=None):
     if rank == 0 and not args.no_quality:
         qual = quality(wl, inp, Q, K, V, pt, Kbar, lse, dev, index_mode=index_mode)
 
+    # ---------------- attention backward on the workload's own selection
+    bwd = None
+    if (rank == 0 and not args.no_bwd and wl.dtype == "bf16" and wl.block_size >= 8
+            and args.index_mode == "split"):
+        bwd = time_backward(wl, p, Q, K, V, pt, Kbar, alg, tensor_peak, dev)
+
     # ---------------- the literal input reading (rank 0, after the headline)
     # The headline's query noise is AR(1) along the sequence (rho 0.99); the
     # workload text's "N(0,1) noise" read literally is i.i.d. (rho 0), which
@@ -633,7 +714,7 @@ def main(argv=None):
                 "data": "synthetic", "config": config_of(wl, args), "clocks": clocks,
                 "e2e": e2e, "gpu_launches": n_launch, "roofline": roofline,
                 "step_roofline": step_roof, "kernels": kernels, "quality": qual,
-                "stress_iid_query_noise": stress, "cpu_baseline": cpu,
+                "backward": bwd, "stress_iid_query_noise": stress, "cpu_baseline": cpu,
                 "input_gen_s": round(t_gen, 2)}
         print(json.dumps(line), flush=True)
     return 0

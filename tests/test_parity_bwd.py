@@ -96,3 +96,92 @@ def test_attn_bwd_rejects_unsupported(s):
         p = s.params_for(wl)
         args = [ctypes.byref(p)] + [vp(0x1000)] * 3 + [None] + [vp(0x1000)] * 11 + [1 << 40, None, None]
         assert s._lib.sgqa_sparse_attn_bwd(*args) == s.ERR_UNSUPPORTED
+
+
+def whole_call_union(s, p, Q, Kbar, chunk=4096):
+    """Union lists of every tile of the call, from the step entry points run
+    on query ranges of `chunk` (a multiple of tile_q) so the scores stay small."""
+    u = s.alloc_union(p)
+    nblk = p.seq_kv // p.block_size
+    ws = s.alloc_workspace(p, s.WS_TOPK_UNION)
+    st = s.new_status()
+    for q0 in range(0, p.seq_q, chunk):
+        q1 = min(p.seq_q, q0 + chunk)
+        sc = torch.empty(p.n_kv_heads, q1 - q0, nblk, device="cuda")
+        s.sgqa_index_scores(p, Q, Kbar, q0, q1, sc, s.alloc_workspace(p, s.WS_INDEX_SCORES))
+        s.sgqa_topk_union(p, sc, q0, q1, None, *u, ws=ws, status=st)
+        del sc
+    assert s.read_status(st)[0] == 0
+    return u
+
+
+def _tile_sel(u, wl, tau0, n):
+    """The GPU union's per-query selections of queries [tau0 W, tau0 W + n)
+    (whole tiles), as the oracle's [Hkv][n][Ks] table."""
+    uo, ul, ub, um = u
+    ntiles = (wl.seq_q + wl.tile_q - 1) // wl.tile_q
+    W, Ks = wl.tile_q, wl.k_blocks
+    sel = np.full((wl.n_kv_heads, n, Ks), -1, np.int32)
+    for g in range(wl.n_kv_heads):
+        for i in range(n):
+            tau = tau0 + i // W
+            o, ln = uo[g * ntiles + tau], ul[g * ntiles + tau]
+            blks, masks = ub[o:o + ln], um[o:o + ln].view(np.uint64)
+            mine = blks[((masks >> np.uint64(i % W)) & np.uint64(1)) == 1]
+            sel[g, i, :len(mine)] = mine
+    return sel
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["gqa_32k", "step5_128k"])
+def test_attn_bwd_full_size(s, name):
+    """The full workload: the GPU's own selection, forward and backward.
+    Against the oracle: dQ of sampled tiles (each tile's queries as a
+    sub-problem, their lists from the GPU union), and dK, dV of the last 128
+    keys, which only the last 128 queries attend, so the oracle's backward of
+    those queries alone gives them in full.  Over all keys, the identities
+    sum_p dV_p = sum_rows dO and sum_p dK_p = 0 per group (a row's softmax
+    weights sum to one) hold up to rounding.  Two calls are bit-identical."""
+    wl = synth.WORKLOADS[name]
+    inp = synth.make_inputs(wl)
+    p = s.params_for(wl)
+    d = dev_inputs(inp)
+    Kbar = s.kbar_empty(p)
+    s.sgqa_block_merge(p, d["K"], Kbar)
+    u = whole_call_union(s, p, d["Q"], Kbar)
+    O, lse = s.alloc_outputs(p)
+    st = s.new_status()
+    s.sgqa_sparse_attn_fwd(p, d["Q"], d["K"], d["V"], *u, O, lse,
+                           ws=s.alloc_workspace(p, s.WS_SPARSE_ATTN), status=st)
+    assert s.read_status(st)[0] == 0
+    rng = np.random.default_rng(78)
+    dOb = synth.to_bf16_bits(rng.standard_normal((wl.seq_q, wl.n_q_heads, wl.head_dim)).astype(np.float32))
+    dO = to_dev(dOb)
+    dQ, dK, dV = run_bwd(s, p, d, u, O, lse, dO, wl)
+    # identities over every key and row
+    G = wl.n_q_heads // wl.n_kv_heads
+    sdO = dO.float().view(wl.seq_q, wl.n_kv_heads, G, wl.head_dim).double().sum((0, 2))
+    rel_v = (dV.double().sum(0) - sdO).abs().max().item() / sdO.abs().max().item()
+    rel_k = dK.double().sum(0).abs().max().item() / dK.double().abs().sum(0).max().item()
+    assert rel_v < 1e-2 and rel_k < 1e-2, (rel_v, rel_k)
+    # against the oracle
+    Q, K, V = widened(inp)
+    dOw = synth.widen(dOb).astype(np.float64)
+    uh = tuple(x.cpu().numpy() for x in u)
+    ntiles = (wl.seq_q + wl.tile_q - 1) // wl.tile_q
+    W = wl.tile_q
+    for tau in (0, ntiles // 3):
+        q0 = tau * W
+        n = min(W, wl.seq_q - q0)
+        dQ64, _, _ = oracle.sparse_attn_bwd(Q[q0:q0 + n], K, V, dOw[q0:q0 + n], wl.q_offset + q0,
+                                            wl.block_size, _tile_sel(uh, wl, tau, n), 0, W=W)
+        close(dQ[q0:q0 + n], dQ64, f"dQ tile {tau}")
+    q0 = wl.seq_q - 2 * W
+    dQ64, dK64, dV64 = oracle.sparse_attn_bwd(Q[q0:], K, V, dOw[q0:], wl.q_offset + q0,
+                                              wl.block_size, _tile_sel(uh, wl, q0 // W, 2 * W), 0, W=W)
+    close(dQ[q0:], dQ64, "dQ last tiles")
+    k0 = wl.seq_kv - 128
+    close(dK[k0:], dK64[k0:], "dK last keys")
+    close(dV[k0:], dV64[k0:], "dV last keys")
+    dQ2, dK2, dV2 = run_bwd(s, p, d, u, O, lse, dO, wl)
+    assert torch.equal(dQ, dQ2) and torch.equal(dK, dK2) and torch.equal(dV, dV2)
