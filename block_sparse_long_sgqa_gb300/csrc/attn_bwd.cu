@@ -521,7 +521,8 @@ struct DkvCfg {
   static constexpr int OFF_Q = OFF_V + KV_BYTES;
   static constexpr int OFF_DO = OFF_Q + NQ * Q_BYTES;
   static constexpr int OFF_META = OFF_DO + NQ * Q_BYTES;
-  static constexpr int OFF_BAR = OFF_META + NM * 2048;
+  static constexpr int OFF_STG = OFF_META + NM * 2048;  // [32 tiles][16 blocks] union masks
+  static constexpr int OFF_BAR = OFF_STG + 32 * 16 * 8;
   static constexpr int SMEM = OFF_BAR + 512 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;  // S^T[2] 0/64, dP^T[2] 128/192, dV 256, dK 256 + D
   static constexpr int NTHREADS = 352;        // builder, loader, MMA, 8 softmax warps
@@ -564,7 +565,8 @@ __global__ void __launch_bounds__(352, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
   int* abort_flag = reinterpret_cast<int*>(bars + 19);
   volatile int* n_stages = reinterpret_cast<volatile int*>(bars + 20);
-  uint64_t* mloc = bars + 24;     // [16] the tile's union masks of the stage's blocks
+  uint64_t* ld_full = bars + 24;  // [NM] the stage's lse and D rows written (by the loader)
+  uint64_t* stg = reinterpret_cast<uint64_t*>(smem + C::OFF_STG);  // [32][16]
 
   const int64_t item = blockIdx.x;
   const int g = (int)(item % a.Hkv);
@@ -582,6 +584,7 @@ __global__ void __launch_bounds__(352, 1)
     for (int i = 0; i < C::NM; ++i) {
       mbar_init(&m_full[i], 1);
       mbar_init(&m_empty[i], 9);  // the loader + 8 softmax warps
+      mbar_init(&ld_full[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -601,36 +604,47 @@ __global__ void __launch_bounds__(352, 1)
 
   if (warp == 0) {
     // ========================================== query stages of this key stage
+    // 32 tiles at a time: each lane fetches its tile's first slot in the
+    // stage and the union entries there (at most one per block) into the
+    // staging table, then the tiles are walked in order.
     int j = 0;
     bool ok = true;
     const uint32_t* row = a.kbits + ((int64_t)g * a.nks + ks) * a.nw;
     for (int64_t w0 = 0; w0 < a.nw && ok; ++w0) {
       uint32_t bits = row[w0];
-      while (bits != 0u && ok) {
-        const int64_t tau = w0 * 32 + (__ffs(bits) - 1);
-        bits &= bits - 1u;
+      if (bits == 0u) continue;
+      {
+        const int64_t tau = w0 * 32 + lane;
+        const bool act = (bits >> lane) & 1u;
         const int64_t lt = (int64_t)g * a.ntiles + tau;
-        const int32_t fs = a.first[lt * a.nks + ks];
-        const int64_t end = a.uoff[lt] + a.ulen[lt];
-        if (lane < 16) mloc[lane] = 0ull;
-        __syncwarp();
-        if (fs >= 0 && lane < SB && fs + lane < end) {
-          const int64_t b = a.ublk[fs + lane];
-          if (b < kb0 + SB) mloc[b - kb0] = a.umask[fs + lane];
+        const int32_t fs = act ? a.first[lt * a.nks + ks] : -1;
+        const int64_t end = act ? a.uoff[lt] + a.ulen[lt] : 0;
+        uint64_t* my = stg + lane * 16;
+        int64_t bx[SB];
+#pragma unroll
+        for (int x = 0; x < SB; ++x) {
+          my[x] = 0ull;
+          bx[x] = (fs >= 0 && fs + x < end) ? a.ublk[fs + x] : INT64_MAX;
         }
-        __syncwarp();
+#pragma unroll
+        for (int x = 0; x < SB; ++x)
+          if (bx[x] < kb0 + SB) my[bx[x] - kb0] = a.umask[fs + x];
+      }
+      __syncwarp();
+      while (bits != 0u && ok) {
+        const int li = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        const int64_t tau = w0 * 32 + li;
         const int64_t t0 = tau * a.W;
         const int64_t len = (a.T - t0) < a.W ? (a.T - t0) : a.W;
         const int nsub = (int)((len + a.QS - 1) / a.QS);
+        const uint64_t um = lane < SB ? stg[li * 16 + lane] : 0ull;
         for (int sidx = 0; sidx < nsub; ++sidx) {
           const int64_t tq0 = t0 + (int64_t)sidx * a.QS;
           const int nq = (int)((len - (int64_t)sidx * a.QS) < a.QS ? (len - (int64_t)sidx * a.QS) : a.QS);
           const uint64_t qmask = nq >= 64 ? ~0ull : ((1ull << nq) - 1ull);
-          uint64_t hm = 0ull;
-          if (lane < SB) {
-            const uint64_t um = mloc[lane];
-            hm = a.mode == SGQA_UNION_MASKED ? ((um >> (sidx * a.QS)) & qmask) : (um ? qmask : 0ull);
-          }
+          const uint64_t hm =
+              a.mode == SGQA_UNION_MASKED ? ((um >> (sidx * a.QS)) & qmask) : (um ? qmask : 0ull);
           const int64_t c0 = (a.off + tq0) / B, cl = (a.off + tq0 + nq - 1) / B;
           const bool has_cur = cl >= kb0 && c0 < kb0 + SB;
           if (!__any_sync(FULL, hm != 0ull) && !has_cur) continue;
@@ -646,24 +660,12 @@ __global__ void __launch_bounds__(352, 1)
             st.nq = nq;
           }
           if (lane < 16) st.hm[lane] = hm;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int r = lane + 32 * k;
-            const int qi = r >> a.lgG, hh = r & (a.G - 1);
-            float nl = 0.0f, nd = 0.0f;
-            if (qi < nq) {
-              const int64_t hq = (int64_t)g * a.G + hh, t = tq0 + qi;
-              nl = -a.lse[hq * a.T + t] * kLog2e;
-              nd = -a.Dl[hq * a.T + t];
-            }
-            st.nlse2[r] = nl;
-            st.nD[r] = nd;
-          }
           __syncwarp();
           if (lane == 0) mbar_arrive(&m_full[ms]);
           ++j;
         }
       }
+      __syncwarp();  // the staging table is rewritten for the next 32 tiles
     }
     if (lane == 0) {
       *n_stages = ok ? j : 0;
@@ -683,34 +685,39 @@ __global__ void __launch_bounds__(352, 1)
     if (lane == 0) {
       tma_prefetch_desc(&mq);
       tma_prefetch_desc(&mdo);
-      const uint32_t box = (uint32_t)(C::KC * 128 * a.G * a.QS);
-      for (int j = 0;; ++j) {
-        const int ms = j % C::NM, qs = j % C::NQ;
-        bool have = true;
-        {
-          const uint64_t t0 = globaltimer();
-          for (uint32_t it = 0;; ++it) {
-            if (mbar_try_wait_ns(&m_full[ms], (uint32_t)((j / C::NM) & 1), 500)) break;
-            if (*n_stages <= j) {
+    }
+    const uint32_t box = (uint32_t)(C::KC * 128 * a.G * a.QS);
+    for (int j = 0;; ++j) {
+      const int ms = j % C::NM, qs = j % C::NQ;
+      bool have = true;
+      {
+        const uint64_t t0 = globaltimer();
+        for (uint32_t it = 0;; ++it) {
+          if (mbar_try_wait_ns(&m_full[ms], (uint32_t)((j / C::NM) & 1), 500)) break;
+          if (*n_stages <= j) {
+            have = false;
+            break;
+          }
+          if ((it & 15) == 15) {
+            if (ab.set()) {
               have = false;
               break;
             }
-            if ((it & 15) == 15) {
-              if (ab.set()) {
-                have = false;
-                break;
-              }
-              if (globaltimer() - t0 > kWaitLimitNs) {
-                ab.raise(a.status, 422);
-                have = false;
-                break;
-              }
+            if (globaltimer() - t0 > kWaitLimitNs) {
+              ab.raise(a.status, 422);
+              have = false;
+              break;
             }
           }
         }
-        if (!have) break;
-        if (!mbar_wait(&q_empty[qs], (uint32_t)(((j / C::NQ) & 1) ^ 1), ab, a.status, 423)) break;
-        const int64_t tq0 = qs_at(ms).tq0;
+      }
+      if (!__all_sync(FULL, have)) break;
+      const bool wq = mbar_wait(&q_empty[qs], (uint32_t)(((j / C::NQ) & 1) ^ 1), ab, a.status, 423);
+      if (!__all_sync(FULL, wq)) break;
+      QStage& st = qs_at(ms);
+      const int64_t tq0 = st.tq0;
+      const int nq = st.nq;
+      if (lane == 0) {
         mbar_expect_tx(&q_full[qs], 2 * box);
         for (int c = 0; c < C::KC; ++c) {
           tma_load_3d(smem + C::OFF_Q + qs * C::Q_BYTES + c * (128 * 128), &mq, &q_full[qs], c * 64,
@@ -718,14 +725,32 @@ __global__ void __launch_bounds__(352, 1)
           tma_load_3d(smem + C::OFF_DO + qs * C::Q_BYTES + c * (128 * 128), &mdo, &q_full[qs],
                       c * 64, g * a.G, (int32_t)tq0);
         }
-        ++issued[qs];
+      }
+      ++issued[qs];
+      // -lse * log2(e) and -D of the stage's query-head rows (0 past its queries)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int r = lane + 32 * k;
+        const int qi = r >> a.lgG, hh = r & (a.G - 1);
+        float nl = 0.0f, nd = 0.0f;
+        if (qi < nq) {
+          const int64_t hq = (int64_t)g * a.G + hh, t = tq0 + qi;
+          nl = -a.lse[hq * a.T + t] * kLog2e;
+          nd = -a.Dl[hq * a.T + t];
+        }
+        st.nlse2[r] = nl;
+        st.nD[r] = nd;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&ld_full[ms]);
         mbar_arrive(&m_empty[ms]);
       }
-      if (ab.set()) {
-        mbar_wait_drain(kv_full, 0, a.status, 493);
-        for (int k = 0; k < C::NQ; ++k)
-          if (issued[k] > 0) mbar_wait_drain(&q_full[k], (issued[k] - 1) & 1, a.status, 494);
-      }
+    }
+    if (lane == 0 && ab.set()) {
+      mbar_wait_drain(kv_full, 0, a.status, 493);
+      for (int k = 0; k < C::NQ; ++k)
+        if (issued[k] > 0) mbar_wait_drain(&q_full[k], (issued[k] - 1) & 1, a.status, 494);
     }
   } else if (warp == 2) {
     // ============================================================ MMA issuer
@@ -835,7 +860,7 @@ __global__ void __launch_bounds__(352, 1)
       {
         const uint64_t t0 = globaltimer();
         for (uint32_t it = 0;; ++it) {
-          if (mbar_try_wait_ns(&m_full[ms], (uint32_t)((j / C::NM) & 1), 500)) break;
+          if (mbar_try_wait_ns(&ld_full[ms], (uint32_t)((j / C::NM) & 1), 500)) break;
           if (*n_stages <= j) {
             have = false;
             break;
