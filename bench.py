@@ -56,6 +56,10 @@ def parse_args(argv=None):
     ap.add_argument("--index-mode", choices=["split", "bf16"], default="split",
                     help="indexer precision: fp32 scores from a bf16 split (exact selection) "
                          "or bf16 scores (one product; recall against split reported)")
+    ap.add_argument("--decode", action="store_true",
+                    help="time decode steps (one query at the end of the 1M paged cache) "
+                         "through sgqa_decode with a persistent block-key cache, beside "
+                         "sgqa_prefill on the same query; prints its own line")
     ap.add_argument("--no-bwd", action="store_true",
                     help="skip timing the attention backward on the workload's selection")
     ap.add_argument("--no-stress", action="store_true",
@@ -462,6 +466,66 @@ def time_backward(wl, p, Q, K, V, pt, Kbar, alg, tensor_peak, dev, steps=3):
     return res
 
 
+def run_decode(args, dev):
+    """Decode steps over the 1M paged cache: the block-key cache is built by
+    the first call, then each timed step is one query at the last position
+    (the cache already holds every complete block)."""
+    import torch
+
+    from block_sparse_long_sgqa_gb300 import sgqa, synth
+
+    base = synth.WORKLOADS["chunk_1m"]
+    pos = base.seq_kv - 1
+    wl = base.replace(name="decode_1m", seq_q=1, q_offset=pos)
+    inp = synth.make_inputs(wl)
+    p = sgqa.params_for(wl)
+    Kh = synth.to_paged(inp["K"], inp["page_table"], wl.page_size)
+    Vh = synth.to_paged(inp["V"], inp["page_table"], wl.page_size)
+    tod = lambda x: torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    Q, K, V = tod(inp["Q"]), tod(Kh), tod(Vh)
+    pt = torch.from_numpy(inp["page_table"]).to(dev)
+    O, lse = sgqa.alloc_outputs(p, dev)
+    st = sgqa.new_status(dev)
+    cache = sgqa.KeyCache(p, cap_blocks=wl.n_blocks, device=dev)
+    ws = sgqa.alloc_workspace(p, sgqa.WS_DECODE, dev)
+    sgqa.sgqa_decode(p, Q, K, V, cache, O, lse, ws, page_table=pt, status=st)  # builds the cache
+    Kbar = cache.Kbar.clone()
+    wsp = sgqa.alloc_workspace(p, sgqa.WS_PREFILL, dev)
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for name, fn in (("decode", lambda: sgqa.sgqa_decode(p, Q, K, V, cache, O, lse, ws,
+                                                         page_table=pt, status=st)),
+                     ("prefill_one_query", lambda: sgqa.sgqa_prefill(
+                         p, Q, K, V, Kbar, O, lse, wsp, page_table=pt,
+                         kbar_valid_blocks=wl.n_blocks, status=st))):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize(dev)
+        log = sgqa.launch_log(args.steps * 64)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with log:
+            e0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+        per = {}
+        for kind, t_ms in log.entries():
+            nm = sgqa.KERNEL_NAMES.get(kind, str(kind))
+            per[nm] = per.get(nm, 0.0) + t_ms / args.steps
+        out[name] = {"ms_per_step": e0.elapsed_time(e1) / args.steps, "kernels_ms": per}
+    code, det = sgqa.read_status(st)
+    if code != 0:
+        raise RuntimeError(f"device status in the decode timing: {sgqa.status_string(code)} ({det})")
+    return {"metric": "decode step latency, one query over a 1M-token paged cache",
+            "unit": "ms", "higher_is_better": False, "steps": args.steps,
+            "config": {"workload": wl.name, "seq_kv": wl.seq_kv, "n_q_heads": wl.n_q_heads,
+                       "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
+                       "block_size": wl.block_size, "topk_tokens": wl.topk_tokens,
+                       "page_size": wl.page_size},
+            **out}
+
+
 def config_of(wl, args):
     return {"workload": wl.name, "seq_q": wl.seq_q, "seq_kv": wl.seq_kv, "q_offset": wl.q_offset,
             "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
@@ -498,6 +562,10 @@ def main(argv=None):
     torch.cuda.set_device(local)
     dist_init(world, "nccl")
     dev = torch.device("cuda", local)
+    if args.decode:
+        if rank == 0:
+            print(json.dumps(run_decode(args, dev)), flush=True)
+        return 0
     index_mode = sgqa.INDEX_BF16 if args.index_mode == "bf16" else sgqa.INDEX_SPLIT
     p = sgqa.params_for(wl, union_mode=1 if args.union_mode == "full" else 0,
                         index_mode=index_mode)

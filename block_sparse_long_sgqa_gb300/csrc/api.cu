@@ -23,7 +23,8 @@ int launch_sparse_attn_layout(const Dims& dm, const __nv_bfloat16* Q, const __nv
                               const int64_t* union_off, const int32_t* union_len,
                               const int32_t* union_blk, const uint64_t* union_mask, void* O,
                               float* lse, int64_t tau_begin, int64_t tau_end, int64_t lay_tau0,
-                              int64_t lay_ntiles, int32_t* status, cudaStream_t st);
+                              int64_t lay_ntiles, int32_t* status, cudaStream_t st, int nsplit,
+                              float* opart, float* lpart);
 
 // ---------------------------------------------------------------- launch log
 static sgqa_launch_log* g_log = nullptr;
@@ -168,11 +169,13 @@ int64_t prefill_chunk(const Dims& dm) {
 struct IndexWs {
   __nv_bfloat16 *khi, *klo, *qhi, *qlo;
 };
-IndexWs carve_index(Carve& c, const Dims& dm, int64_t nq) {
-  IndexWs w;
+IndexWs carve_index(Carve& c, const Dims& dm, int64_t nq, bool key_split = true) {
+  IndexWs w{nullptr, nullptr, nullptr, nullptr};
   const size_t nk = (size_t)dm.Hkv * dm.nblk * dm.d, nqe = (size_t)dm.Hkv * nq * dm.d;
-  w.khi = c.take<__nv_bfloat16>(nk);
-  w.klo = c.take<__nv_bfloat16>(nk);
+  if (key_split) {
+    w.khi = c.take<__nv_bfloat16>(nk);
+    w.klo = c.take<__nv_bfloat16>(nk);
+  }
   w.qhi = c.take<__nv_bfloat16>(nqe);
   w.qlo = c.take<__nv_bfloat16>(nqe);
   return w;
@@ -232,11 +235,11 @@ struct PrefillWs {
   uint64_t* umask;
   int64_t ucap, chunk, chunk_tiles, capG;
 };
-PrefillWs carve_prefill(Carve& c, const Dims& dm) {
+PrefillWs carve_prefill(Carve& c, const Dims& dm, bool key_split = true) {
   PrefillWs w;
   w.chunk = prefill_chunk(dm);
   w.chunk_tiles = w.chunk / dm.W;
-  w.ix = carve_index(c, dm, w.chunk);
+  w.ix = carve_index(c, dm, w.chunk, key_split);
   w.at = carve_attn(c, dm);
   w.filt = dm.nblk > 0 && chunk_filtered(dm, 0, dm.T);
   w.shi = nullptr;
@@ -273,6 +276,32 @@ PrefillWs carve_prefill(Carve& c, const Dims& dm) {
 }
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA; }
+
+struct AttnSplitWs {
+  int n;
+  float* opart;
+  float* lpart;
+};
+
+// Attention splits of a decode call: enough work items to cover every SM
+// about twice, up to 16 per item, and only when the call is one chunk.
+constexpr int kMaxSplit = 16;
+int decode_splits(const Dims& dm) {
+  if (prefill_chunk(dm) < dm.T) return 1;
+  const int64_t QS = 128 / dm.G < dm.W ? 128 / dm.G : dm.W;
+  const int64_t items = dm.ntiles * dm.Hkv * ((std::min<int64_t>(dm.T, dm.W) + QS - 1) / QS);
+  const int64_t want = (2 * 152 + items - 1) / items;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(kMaxSplit, want));
+}
+void carve_decode(Carve& c, const Dims& dm, PrefillWs* pw, AttnSplitWs* sw) {
+  PrefillWs w = carve_prefill(c, dm, false);
+  if (pw) *pw = w;
+  AttnSplitWs a;
+  a.n = decode_splits(dm);
+  a.opart = a.n > 1 ? c.take<float>((size_t)a.n * dm.T * dm.H * dm.d) : nullptr;
+  a.lpart = a.n > 1 ? c.take<float>((size_t)a.n * dm.H * dm.T) : nullptr;
+  if (sw) *sw = a;
+}
 
 // Element strides between consecutive sequences of a batched call (the
 // batch layout of include/sgqa.h).  A paged cache shares its page pool, so
@@ -371,6 +400,7 @@ SGQA_API size_t sgqa_workspace_bytes(const sgqa_params* p, int which) {
     case SGQA_WS_TOPK_UNION: c.take<int32_t>(topk_union_ws_bytes(dm, dm.T) / 4); break;
     case SGQA_WS_SPARSE_ATTN: carve_attn(c, dm); break;
     case SGQA_WS_PREFILL: carve_prefill(c, dm); break;
+    case SGQA_WS_DECODE: carve_decode(c, dm, nullptr, nullptr); break;
     case SGQA_WS_ATTN_BWD: {
       c.take<__nv_bfloat16>((size_t)kv_pack_elems(dm));
       c.take<__nv_bfloat16>((size_t)kv_pack_elems(dm));
@@ -573,16 +603,38 @@ SGQA_API int sgqa_sparse_attn_bwd(const sgqa_params* p, const void* Q, const voi
 
 namespace {
 
+// A caller-owned block-key cache with a fixed row stride (sgqa_decode):
+// Kbar and its bf16 hi/lo halves, blocks [0, valid) already merged and split.
+struct KeyCache {
+  __nv_bfloat16* khi = nullptr;
+  __nv_bfloat16* klo = nullptr;
+  int64_t rows = 0;  // block rows per group (0: no cache; Kbar rows are nblk)
+};
+
+// Attention split over its union entries (sgqa_decode): partial outputs.
+struct AttnSplit {
+  int n = 1;
+  float* opart = nullptr;
+  float* lpart = nullptr;
+};
+
 // One sequence of sgqa_prefill (arguments validated by the caller).  Qidx
 // (nullable) replaces the mean of each group's query heads as the index
-// query, Kidx (nullable) replaces K as the merge's input.
+// query, Kidx (nullable) replaces K as the merge's input.  With a key cache,
+// Kbar has kc.rows rows per group, only blocks [kbar_valid_blocks, nblk) are
+// merged (and split into the cache), and the indexer reads the cache.
 int prefill_one(const Dims& dm, const void* Q, const void* K, const void* V, const void* Qidx,
                 const void* Kidx, const int32_t* page_table, float* Kbar,
                 int32_t kbar_valid_blocks, void* O, float* lse, void* ws, int32_t* status,
-                cudaStream_t st) {
+                cudaStream_t st, const KeyCache& kc = KeyCache(),
+                const AttnSplit& sp = AttnSplit()) {
   int rc = SGQA_OK;
   Carve c(align_ws(ws));
-  PrefillWs w = carve_prefill(c, dm);
+  PrefillWs w = carve_prefill(c, dm, kc.rows == 0);
+  if (kc.rows > 0) {  // the indexer's key operand is the persistent cache
+    w.ix.khi = kc.khi;
+    w.ix.klo = kc.klo;
+  }
   // the index query's source: Q with G heads per group, or Qidx with one
   Dims qd = dm;
   const void* qsrc = Q;
@@ -593,9 +645,11 @@ int prefill_one(const Dims& dm, const void* Q, const void* K, const void* V, con
   }
 
   // step 1: merge the blocks not yet in the cache (and split all of them for the indexer)
-  cudaError_t e = launch_block_merge(dm, Kidx != nullptr ? Kidx : K, page_table,
+  Dims md = dm;  // the merge writes rows of the cache's stride
+  if (kc.rows > 0) md.nblk = kc.rows;
+  cudaError_t e = launch_block_merge(md, Kidx != nullptr ? Kidx : K, page_table,
                                      kbar_valid_blocks, dm.nblk, Kbar, w.ix.khi, w.ix.klo, st);
-  if (e == cudaSuccess && kbar_valid_blocks > 0) {
+  if (e == cudaSuccess && kbar_valid_blocks > 0 && kc.rows == 0) {
     Dims part = dm;  // split the cached prefix: per group, blocks [0, kbar_valid_blocks)
     for (int g = 0; g < dm.Hkv && e == cudaSuccess; ++g) {
       part.Hkv = 1;
@@ -604,7 +658,8 @@ int prefill_one(const Dims& dm, const void* Q, const void* K, const void* V, con
       e = launch_split_kbar(part, Kbar + o, w.ix.khi + o, w.ix.klo + o, st);
     }
   }
-  if (e == cudaSuccess && w.filt) e = launch_sample_keys(dm, w.ix.khi, w.ix.klo, w.shi, nullptr, st);
+  if (e == cudaSuccess && w.filt)
+    e = launch_sample_keys(dm, w.ix.khi, w.ix.klo, w.shi, nullptr, st, kc.rows);
   const __nv_bfloat16 *q, *k, *v;
   Dims ad;  // the dims the attention reads its K/V with
   if (e == cudaSuccess) e = stage_attn(dm, Q, K, V, page_table, w.at, &q, &k, &v, &ad, st);
@@ -618,6 +673,7 @@ int prefill_one(const Dims& dm, const void* Q, const void* K, const void* V, con
       e = launch_index_query(qd, qsrc, q0, q1, w.ix.qhi, w.ix.qlo, st);
       if (e != cudaSuccess) return SGQA_ERR_CUDA;
       IndexMode mode{};
+      mode.krows = kc.rows;
       if (filt) {  // thresholds from the sampled blocks' scores, then candidates
         IndexMode ms{};
         ms.sample = 1;
@@ -640,6 +696,7 @@ int prefill_one(const Dims& dm, const void* Q, const void* K, const void* V, con
         IndexMode mr{};
         mr.flist = w.flist;
         mr.nflist = w.counters + 1;
+        mr.krows = kc.rows;
         rc = launch_index_scores(dm, w.ix.qhi, w.ix.qlo, w.ix.khi, w.ix.klo, q0, q1, w.scores,
                                  false, status, st, &mr);
         if (rc != SGQA_OK) return rc;
@@ -653,7 +710,7 @@ int prefill_one(const Dims& dm, const void* Q, const void* K, const void* V, con
     rc = launch_sparse_attn_layout(ad, q, k, v, w.at.Kp, w.at.Vp,
                                    ad.ps > 0 ? page_table : nullptr, w.uoff, w.ulen,
                                    w.ublk, w.umask, O, lse, tau0, tau1, tau0, w.chunk_tiles,
-                                   status, st);
+                                   status, st, sp.n, sp.opart, sp.lpart);
     if (rc != SGQA_OK) return rc;
   }
   return SGQA_OK;
@@ -699,6 +756,52 @@ SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, co
                           sgqa_stream_t stream) {
   return sgqa_prefill_ex(p, Q, K, V, nullptr, page_table, Kbar, kbar_valid_blocks, O, lse, ws,
                          ws_bytes, status, stream);
+}
+
+SGQA_API int sgqa_decode(const sgqa_params* p, const void* Q, const void* K, const void* V,
+                         const int32_t* page_table, sgqa_block_key_cache* cache, void* O,
+                         float* lse, void* ws, size_t ws_bytes, int32_t* status,
+                         sgqa_stream_t stream) {
+  Dims dm;
+  int rc = derive(p, &dm);
+  if (rc != SGQA_OK) return rc;
+  if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr || lse == nullptr ||
+      cache == nullptr || cache->Kbar == nullptr || cache->Ksplit == nullptr ||
+      cache->cap_blocks < dm.nblk || cache->valid_blocks < 0 ||
+      ((dm.ps > 0) != (page_table != nullptr)))
+    return SGQA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
+      !aligned16(cache->Kbar) || !aligned16(cache->Ksplit))
+    return SGQA_ERR_ALIGNMENT;
+  if (((int64_t)cache->cap_blocks * dm.d * 2) % 16 != 0) return SGQA_ERR_ALIGNMENT;
+  if (ws == nullptr || ws_bytes < sgqa_workspace_bytes(p, SGQA_WS_DECODE))
+    return SGQA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Carve c(align_ws(ws));
+  AttnSplitWs sw;
+  carve_decode(c, dm, nullptr, &sw);
+  const int64_t cap = cache->cap_blocks;
+  const int32_t valid = std::min<int32_t>(cache->valid_blocks, (int32_t)dm.nblk);
+  KeyCache kc;
+  kc.rows = cap;
+  AttnSplit sp;
+  sp.n = sw.n;
+  sp.opart = sw.opart;
+  sp.lpart = sw.lpart;
+  const SeqStride ss = seq_stride(dm);
+  const int64_t kcache = (int64_t)dm.Hkv * cap * dm.d;  // one sequence's cache rows
+  for (int64_t b = 0; b < dm.batch; ++b) {
+    __nv_bfloat16* hi = static_cast<__nv_bfloat16*>(cache->Ksplit) + b * 2 * kcache;
+    kc.khi = hi;
+    kc.klo = hi + kcache;
+    rc = prefill_one(dm, at_bytes(Q, b, ss.q_bytes), at_bytes(K, b, ss.kv_bytes),
+                     at_bytes(V, b, ss.kv_bytes), nullptr, nullptr, at_b(page_table, b, ss.pt),
+                     cache->Kbar + b * kcache, valid, at_bytes(O, b, ss.q_bytes),
+                     at_b(lse, b, ss.lse), ws, status, st, kc, sp);
+    if (rc != SGQA_OK) return rc;
+  }
+  cache->valid_blocks = (int32_t)dm.nblk;
+  return SGQA_OK;
 }
 
 SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int32_t* launches) {

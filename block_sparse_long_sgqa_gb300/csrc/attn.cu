@@ -98,6 +98,13 @@ struct AttnArgs {
   int H, Hkv, G, B, W, ps, QS, nsub, mode, out_f32, npages;
   float scale_log2;
   int32_t* status;
+  // split work items (few queries over long lists): nsplit > 1 splits each
+  // item's historical union entries into nsplit ranges (the last also takes
+  // the current blocks); each split writes its normalised partial O and its
+  // log-sum-exp, merged by k_attn_combine
+  int nsplit;
+  float* opart;  // [nsplit][T][H][D]
+  float* lpart;  // [nsplit][H][T]
 };
 
 // Gathers one stage's 128 key rows (bf16) of K or V for KV head g into the
@@ -260,8 +267,9 @@ __global__ void __launch_bounds__(384, 1)
   float* xmax = reinterpret_cast<float*>(smem + C::OFF_X);  // [2 group][BM]
   float* xsum = xmax + 2 * C::BM;                            // [2 group][BM]
 
-  // ---- work item
-  const int64_t item = blockIdx.x;
+  // ---- work item (and its split)
+  const int sp = (int)(blockIdx.x % a.nsplit);
+  const int64_t item = blockIdx.x / a.nsplit;
   const int64_t per_tile = (int64_t)a.Hkv * a.nsub;
   const int64_t tau = a.tau_end - 1 - item / per_tile;  // heavy tiles first
   const int g = (int)((item % per_tile) / a.nsub);
@@ -328,6 +336,24 @@ __global__ void __launch_bounds__(384, 1)
     gs.end = gs.cur + a.ulen[lt];
     gs.c0 = (a.off + tq0) / B;
     gs.c_last = (a.off + tq0 + nq_sub - 1) / B;
+    if (a.nsplit > 1) {
+      // the historical entries (those before the first current block; the
+      // entries at or past it are at most the last 64) are divided evenly
+      const int64_t L = gs.end - gs.cur;
+      int64_t trail = 0;
+      for (int r0 = 0; r0 < 64 && r0 < L; r0 += 32) {
+        const bool ge = r0 + lane < L && a.ublk[gs.end - 1 - r0 - lane] >= gs.c0;
+        const uint32_t bal = __ballot_sync(FULL, ge);
+        trail += __popc(bal);
+        if (bal != FULL) break;
+      }
+      const int64_t h0 = gs.cur, lh = L - trail;
+      gs.cur = h0 + lh * sp / a.nsplit;
+      if (sp < a.nsplit - 1) {
+        gs.end = h0 + lh * (sp + 1) / a.nsplit;
+        gs.c_last = gs.c0 - 1;  // the current blocks go to the last split
+      }
+    }
     gs.nd = gs.c0;
     gs.phase = 0;
     gs.pf_at = -1;
@@ -838,7 +864,12 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e)
           ov[e] = __uint_as_float(o0[e]) * g0 + (n1 > 0 ? __uint_as_float(o1[e]) * g1 : 0.0f);
-        if (row_ok) {
+        if (row_ok && a.nsplit > 1) {
+          float* dst = a.opart + ((sp * a.T + t) * a.H + hq) * D + col;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
+        } else if (row_ok) {
           if (a.out_f32) {
             float* dst = static_cast<float*>(a.O) + (t * a.H + hq) * D + col;
 #pragma unroll
@@ -858,7 +889,13 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
-      if (row_ok && grp == 0) a.lse[hq * a.T + t] = (mm + __log2f(lt)) * 0.69314718055994531f;
+      if (row_ok && grp == 0) {
+        const float l_e = (mm + __log2f(lt)) * 0.69314718055994531f;
+        if (a.nsplit > 1)
+          a.lpart[(sp * a.H + hq) * a.T + t] = lt > 0.0f ? l_e : ninf;
+        else
+          a.lse[hq * a.T + t] = l_e;
+      }
     }
     tc_fence_before();
   }
@@ -890,6 +927,44 @@ bool make_kvmap(const Dims& dm, const void* X, CUtensorMap* mx) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Merge of the splits of a work item (fixed order, so the result does not
+// depend on scheduling): lse = log sum_s e^{lse_s}, O = sum_s e^{lse_s - lse}
+// O_s.  One warp per (query, head) row.
+template <int D>
+__global__ void __launch_bounds__(256) k_attn_combine(const float* __restrict__ opart,
+                                                      const float* __restrict__ lpart, int nsplit,
+                                                      int64_t T, int H, void* O, float* lse,
+                                                      int out_f32) {
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= T * H) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t t = row / H, h = row % H;
+  float mx = -__int_as_float(0x7f800000);
+  for (int s2 = 0; s2 < nsplit; ++s2) mx = fmaxf(mx, lpart[(s2 * H + h) * T + t]);
+  float acc[D / 32];
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) acc[i] = 0.0f;
+  float sw = 0.0f;
+  for (int s2 = 0; s2 < nsplit; ++s2) {
+    const float l = lpart[(s2 * H + h) * T + t];
+    const float w = l == mx ? 1.0f : expf(l - mx);  // e^{-inf} = 0 for an empty split
+    sw += w;
+    const float* src = opart + (s2 * T * H + row) * D;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) acc[i] = fmaf(w, src[lane + 32 * i], acc[i]);
+  }
+  const float inv = 1.0f / sw;
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) {
+    const float v = acc[i] * inv;
+    if (out_f32)
+      static_cast<float*>(O)[row * D + lane + 32 * i] = v;
+    else
+      static_cast<__nv_bfloat16*>(O)[row * D + lane + 32 * i] = __float2bfloat16_rn(v);
+  }
+  if (lane == 0) lse[h * T + t] = mx + logf(sw);
+}
+
 template <int D, int B, bool PK>
 int launch_db(const Dims& dm, const AttnArgs& a, const void* Q, int64_t items, cudaStream_t st) {
   using C = AttnCfg<D, B>;
@@ -906,8 +981,16 @@ int launch_db(const Dims& dm, const AttnArgs& a, const void* Q, int64_t items, c
                            C::SMEM) != cudaSuccess)
     return SGQA_ERR_CUDA;
   log_begin(SGQA_K_ATTN, st);
-  k_sparse_attn<D, B, PK><<<(unsigned)items, C::NTHREADS, C::SMEM, st>>>(mq, mk, mv, a);
+  k_sparse_attn<D, B, PK><<<(unsigned)(items * a.nsplit), C::NTHREADS, C::SMEM, st>>>(mq, mk, mv, a);
   log_end(st);
+  if (cudaGetLastError() != cudaSuccess) return SGQA_ERR_CUDA;
+  if (a.nsplit > 1) {
+    const int64_t rows = a.T * a.H;
+    log_begin(SGQA_K_ATTN, st);
+    k_attn_combine<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(a.opart, a.lpart, a.nsplit, a.T,
+                                                                  a.H, a.O, a.lse, a.out_f32);
+    log_end(st);
+  }
   return cudaGetLastError() == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA;
 }
 
@@ -936,8 +1019,12 @@ int launch_sparse_attn_layout(const Dims& dm, const __nv_bfloat16* Q, const __nv
                               const int64_t* union_off, const int32_t* union_len,
                               const int32_t* union_blk, const uint64_t* union_mask, void* O,
                               float* lse, int64_t tau_begin, int64_t tau_end, int64_t lay_tau0,
-                              int64_t lay_ntiles, int32_t* status, cudaStream_t st) {
+                              int64_t lay_ntiles, int32_t* status, cudaStream_t st, int nsplit,
+                              float* opart, float* lpart) {
   if (tau_end <= tau_begin) return SGQA_OK;
+  if (nsplit > 1 && (opart == nullptr || lpart == nullptr || tau_begin != 0 ||
+                     tau_end != dm.ntiles))
+    return SGQA_ERR_INVALID_ARG;
   if (dm.G > 128) return SGQA_ERR_UNSUPPORTED;
   AttnArgs a;
   a.Q = Q;
@@ -974,6 +1061,9 @@ int launch_sparse_attn_layout(const Dims& dm, const __nv_bfloat16* Q, const __nv
   a.out_f32 = dm.dtype == SGQA_FP32;
   a.scale_log2 = dm.scale * 1.4426950408889634f;
   a.status = status;
+  a.nsplit = nsplit > 1 ? nsplit : 1;
+  a.opart = opart;
+  a.lpart = lpart;
   const int64_t items = (tau_end - tau_begin) * dm.Hkv * a.nsub;
   // packed copies given: B >= 8 bulk copies; else key gathers from K and V
   const bool packed = Kp != nullptr && Vp != nullptr;
@@ -991,7 +1081,7 @@ int launch_sparse_attn(const Dims& dm, const __nv_bfloat16* Q, const __nv_bfloat
                        int64_t tau_end, int32_t* status, cudaStream_t st) {
   return launch_sparse_attn_layout(dm, Q, K, V, Kp, Vp, page_table, union_off, union_len, union_blk,
                                    union_mask, O, lse, tau_begin, tau_end, 0, dm.ntiles, status,
-                                   st);
+                                   st, 1, nullptr, nullptr);
 }
 
 }  // namespace sgqa

@@ -74,7 +74,8 @@ struct IdxCfg {
 
 struct IdxArgs {
   int64_t nq, q_begin, q_end, q_offset;
-  int64_t nblk;       // columns of a score row (key rows per group)
+  int64_t nblk;       // columns of a score row
+  int64_t krows;      // block-key rows per group in the B operand arrays
   int64_t nblk_full;  // complete blocks of the call (bounds nh)
   int B, Hkv;
   int sample;      // columns are the sampled blocks: a row has (nh / 64) * 8 of them
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(320, 1)
         // one product: the hi halves only
         mbar_expect_tx(&b_full[s], a.single ? C::B_BYTES : C::STAGE_BYTES);
         uint8_t* sb = smem + C::OFF_B + s * C::STAGE_BYTES;
-        const int32_t brow = (int32_t)(w.g * a.nblk + w.n * C::BN);
+        const int32_t brow = (int32_t)(w.g * a.krows + w.n * C::BN);
         for (int c = 0; c < C::KC; ++c) {
           tma_load_2d(sb + c * C::B_TILE, &mk_hi, &b_full[s], c * 64, brow);
           if (!a.single) tma_load_2d(sb + C::B_BYTES + c * C::B_TILE, &mk_lo, &b_full[s], c * 64, brow);
@@ -507,6 +508,7 @@ int launch_impl(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* q
   a.single = (mode.sample || dm.index_bf16) ? 1 : 0;
   a.round_bf16 = (!mode.sample && dm.index_bf16) ? 1 : 0;
   a.nblk = mode.sample ? sampled_cols(dm) : dm.nblk;
+  a.krows = (!mode.sample && mode.krows > 0) ? mode.krows : a.nblk;
   a.B = dm.B;
   a.Hkv = dm.Hkv;
   a.fill_tail = fill_tail ? 1 : 0;
@@ -536,8 +538,8 @@ int launch_impl(const Dims& dm, const __nv_bfloat16* qhi, const __nv_bfloat16* q
   const uint64_t row_bytes = (uint64_t)D * 2;
   if (!make_tmap_2d_bf16(&m_qhi, qhi, D, (uint64_t)dm.Hkv * a.nq, row_bytes, 64, C::BM) ||
       !make_tmap_2d_bf16(&m_qlo, qlo, D, (uint64_t)dm.Hkv * a.nq, row_bytes, 64, C::BM) ||
-      !make_tmap_2d_bf16(&m_khi, khi, D, (uint64_t)dm.Hkv * a.nblk, row_bytes, 64, C::BN) ||
-      !make_tmap_2d_bf16(&m_klo, klo, D, (uint64_t)dm.Hkv * a.nblk, row_bytes, 64, C::BN))
+      !make_tmap_2d_bf16(&m_khi, khi, D, (uint64_t)dm.Hkv * a.krows, row_bytes, 64, C::BN) ||
+      !make_tmap_2d_bf16(&m_klo, klo, D, (uint64_t)dm.Hkv * a.krows, row_bytes, 64, C::BN))
     return SGQA_ERR_CUDA;
   if (a.tma_store) {
     if (!make_tmap_scores(&m_s, scores, a.nblk, a.nq, dm.Hkv)) return SGQA_ERR_CUDA;

@@ -91,8 +91,10 @@ inline int64_t sampled_cols(const Dims& dm) { return (dm.nblk >> 6) << 3; }
 
 // Gather the sampled blocks' hi keys (and lo keys when slo is not null):
 // [Hkv][sampled_cols][d] each.
+// krows: block-key rows per group of khi/klo (0: dm.nblk).
 cudaError_t launch_sample_keys(const Dims& dm, const __nv_bfloat16* khi, const __nv_bfloat16* klo,
-                               __nv_bfloat16* shi, __nv_bfloat16* slo, cudaStream_t st);
+                               __nv_bfloat16* shi, __nv_bfloat16* slo, cudaStream_t st,
+                               int64_t krows = 0);
 
 // Optional modes of the indexer GEMM (all zero: plain scores).  In filter
 // mode the full score rows are stored only for rows whose threshold is NaN.
@@ -107,6 +109,9 @@ struct IndexMode {
   // entries (g << 20) | (local row / 128), *nflist of them (set on the device)
   const int32_t* flist;
   const int32_t* nflist;
+  // block-key rows per group in khi/klo (0: the call's nblk, or the sampled
+  // columns in sampled mode); a persistent block-key cache has a fixed one
+  int64_t krows;
 };
 
 // scores [Hkv][q_end-q_begin][nblk]; qhi/qlo are [Hkv][q_end-q_begin][d].

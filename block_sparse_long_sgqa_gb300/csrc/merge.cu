@@ -301,14 +301,16 @@ cudaError_t launch_split_kbar(const Dims& dm, const float* Kbar, __nv_bfloat16* 
 }
 
 cudaError_t launch_sample_keys(const Dims& dm, const __nv_bfloat16* khi, const __nv_bfloat16* klo,
-                               __nv_bfloat16* shi, __nv_bfloat16* slo, cudaStream_t st) {
+                               __nv_bfloat16* shi, __nv_bfloat16* slo, cudaStream_t st,
+                               int64_t krows) {
   const int64_t ns = sampled_cols(dm);
   const int c16 = dm.d / 8;
   const int64_t n = (int64_t)dm.Hkv * ns * c16;
   if (n == 0) return cudaSuccess;
   log_begin(SGQA_K_SPLIT, st);
   k_sample_keys<<<grid_for(n), 256, 0, st>>>(reinterpret_cast<const uint4*>(khi),
-                                             reinterpret_cast<const uint4*>(klo), dm.nblk, ns,
+                                             reinterpret_cast<const uint4*>(klo),
+                                             krows > 0 ? krows : dm.nblk, ns,
                                              dm.Hkv, c16, reinterpret_cast<uint4*>(shi),
                                              reinterpret_cast<uint4*>(slo));
   log_end(st);

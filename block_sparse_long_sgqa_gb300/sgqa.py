@@ -28,12 +28,12 @@ ERR_CAPACITY, ERR_TIMEOUT, ERR_BOUNDS = 6, 7, 8
 BF16, FP32 = 0, 1
 UNION_MASKED, UNION_FULL = 0, 1
 INDEX_SPLIT, INDEX_BF16 = 0, 1
-WS_INDEX_SCORES, WS_TOPK_UNION, WS_SPARSE_ATTN, WS_PREFILL, WS_ATTN_BWD = 1, 2, 3, 4, 5
+WS_INDEX_SCORES, WS_TOPK_UNION, WS_SPARSE_ATTN, WS_PREFILL, WS_ATTN_BWD, WS_DECODE = 1, 2, 3, 4, 5, 6
 DEBUG_STALL = 0x5354414C  # SGQA_DEBUG_STALL: written into word 3 of a status buffer
 
 EXPORTED = ("sgqa_workspace_bytes", "sgqa_union_capacity", "sgqa_block_merge", "sgqa_index_scores",
             "sgqa_topk_union", "sgqa_topk_union_noalloc", "sgqa_sparse_attn_fwd",
-            "sgqa_sparse_attn_bwd", "sgqa_prefill",
+            "sgqa_sparse_attn_bwd", "sgqa_prefill", "sgqa_decode",
             "sgqa_prefill_ex", "sgqa_prefill_plan",
             "sgqa_set_launch_log", "sgqa_reset_status", "sgqa_read_status", "sgqa_status_string",
             "sgqa_version")
@@ -57,6 +57,11 @@ class Params(ctypes.Structure):
 
 class IndexInputs(ctypes.Structure):
     _fields_ = [("Qidx", ctypes.c_void_p), ("Kidx", ctypes.c_void_p)]
+
+
+class BlockKeyCache(ctypes.Structure):
+    _fields_ = [("Kbar", ctypes.c_void_p), ("Ksplit", ctypes.c_void_p),
+                ("cap_blocks", ctypes.c_int32), ("valid_blocks", ctypes.c_int32)]
 
 
 class LaunchLog(ctypes.Structure):
@@ -88,6 +93,8 @@ _lib.sgqa_sparse_attn_bwd.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp
 _lib.sgqa_prefill.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp, _vp]
 _lib.sgqa_prefill_ex.argtypes = [_P, _vp, _vp, _vp, ctypes.POINTER(IndexInputs), _vp, _vp, _i32,
                                  _vp, _vp, _vp, _sz, _vp, _vp]
+_lib.sgqa_decode.argtypes = [_P, _vp, _vp, _vp, _vp, ctypes.POINTER(BlockKeyCache), _vp, _vp, _vp,
+                             _sz, _vp, _vp]
 _lib.sgqa_prefill_plan.argtypes = [_P, ctypes.POINTER(_i64), ctypes.POINTER(_i32)]
 _lib.sgqa_set_launch_log.argtypes = [ctypes.POINTER(LaunchLog)]
 _lib.sgqa_reset_status.argtypes = [_vp, _vp]
@@ -97,7 +104,7 @@ _lib.sgqa_status_string.restype = ctypes.c_char_p
 _lib.sgqa_version.restype = ctypes.c_int
 for _f in ("sgqa_block_merge", "sgqa_index_scores", "sgqa_topk_union", "sgqa_topk_union_noalloc",
            "sgqa_sparse_attn_fwd", "sgqa_sparse_attn_bwd",
-           "sgqa_prefill", "sgqa_prefill_ex", "sgqa_prefill_plan", "sgqa_set_launch_log", "sgqa_reset_status",
+           "sgqa_prefill", "sgqa_prefill_ex", "sgqa_decode", "sgqa_prefill_plan", "sgqa_set_launch_log", "sgqa_reset_status",
            "sgqa_read_status"):
     getattr(_lib, _f).restype = ctypes.c_int
 
@@ -235,6 +242,32 @@ def sgqa_prefill_ex(p, Q, K, V, Kbar, O, lse, ws, Qidx=None, Kidx=None, page_tab
                                 _ptr(page_table), _ptr(Kbar), kbar_valid_blocks, _ptr(O), _ptr(lse),
                                 _ptr(ws), ws.numel() * ws.element_size(), _ptr(status),
                                 _stream(stream)), "sgqa_prefill_ex")
+
+
+class KeyCache:
+    """A persistent block-key cache for sgqa_decode (device tensors owned here):
+    Kbar [(batch,) Hkv, cap_blocks, d] fp32 and its hi/lo split [(batch,) 2, Hkv,
+    cap_blocks, d] bf16; valid_blocks follows the calls."""
+
+    def __init__(self, p: Params, cap_blocks: int, device="cuda"):
+        nb = p.batch if p.batch > 1 else 1
+        lead = (nb,) if nb > 1 else ()
+        self.Kbar = torch.zeros(lead + (p.n_kv_heads, cap_blocks, p.head_dim), dtype=torch.float32,
+                                device=device)
+        self.Ksplit = torch.zeros(lead + (2, p.n_kv_heads, cap_blocks, p.head_dim),
+                                  dtype=torch.bfloat16, device=device)
+        self.c = BlockKeyCache(self.Kbar.data_ptr(), self.Ksplit.data_ptr(), cap_blocks, 0)
+
+    @property
+    def valid_blocks(self) -> int:
+        return self.c.valid_blocks
+
+
+def sgqa_decode(p, Q, K, V, cache: KeyCache, O, lse, ws, page_table=None, status=None, stream=None):
+    _check(_lib.sgqa_decode(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(page_table),
+                            ctypes.byref(cache.c), _ptr(O), _ptr(lse), _ptr(ws),
+                            ws.numel() * ws.element_size(), _ptr(status), _stream(stream)),
+           "sgqa_decode")
 
 
 def sgqa_prefill_plan(p):

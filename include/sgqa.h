@@ -153,7 +153,8 @@ enum sgqa_ws_kind {
   SGQA_WS_TOPK_UNION = 2,
   SGQA_WS_SPARSE_ATTN = 3,
   SGQA_WS_PREFILL = 4,
-  SGQA_WS_ATTN_BWD = 5
+  SGQA_WS_ATTN_BWD = 5,
+  SGQA_WS_DECODE = 6
 };
 
 /* Bytes of device workspace the entry point `which` needs for these params
@@ -318,6 +319,39 @@ SGQA_API int sgqa_prefill_ex(const sgqa_params* p, const void* Q, const void* K,
                              const sgqa_index_inputs* idx, const int32_t* page_table,
                              float* Kbar, int32_t kbar_valid_blocks, void* O, float* lse,
                              void* ws, size_t ws_bytes, int32_t* status, sgqa_stream_t stream);
+
+/* A caller-owned block-key cache that persists across decode steps, with a
+ * fixed number of block rows per KV group so that the context can grow:
+ *   Kbar:   [n_kv_heads][cap_blocks][head_dim] fp32 block keys (batch: an
+ *           outer dimension), as sgqa_block_merge computes them;
+ *   Ksplit: [2][n_kv_heads][cap_blocks][head_dim] bf16, the hi and lo halves
+ *           of Kbar that the indexer reads (batch: an outer dimension of the
+ *           pair), kept in step with Kbar by sgqa_decode;
+ *   cap_blocks: rows per group, at least seq_kv / block_size of every call
+ *           (cap_blocks * head_dim * 2 a multiple of 16);
+ *   valid_blocks: blocks [0, valid_blocks) of both are up to date (0 for a
+ *           fresh cache); each call merges and splits only the blocks past it
+ *           and sets it to seq_kv / block_size. */
+typedef struct sgqa_block_key_cache {
+  float* Kbar;
+  void* Ksplit;
+  int32_t cap_blocks;
+  int32_t valid_blocks;
+} sgqa_block_key_cache;
+
+/* Decode steps (the inference side of the layer: a few queries, typically
+ * one, at the end of a long cached context): the same result as sgqa_prefill
+ * on these params, computed with a persistent block-key cache and with each
+ * attention work item split over ranges of its selected blocks when the call
+ * has few work items (the ranges' partial outputs merged in a fixed order, so
+ * results do not depend on scheduling; they may differ from sgqa_prefill's in
+ * the last bits).  The call merges and splits only the blocks that completed
+ * since the previous step.  Workspace: sgqa_workspace_bytes(p,
+ * SGQA_WS_DECODE). */
+SGQA_API int sgqa_decode(const sgqa_params* p, const void* Q, const void* K, const void* V,
+                         const int32_t* page_table, sgqa_block_key_cache* cache, void* O,
+                         float* lse, void* ws, size_t ws_bytes, int32_t* status,
+                         sgqa_stream_t stream);
 
 /* Plan of one sgqa_prefill call: queries per chunk (*chunk_queries) and the
  * number of kernel launches it enqueues (*launches).  Either pointer may be
