@@ -276,9 +276,13 @@ def oracle_sample(wl, inp, budget_s: float):
             n += len(rows)
         return n, time.perf_counter() - t1
 
-    n, dt = run_rows(4, 1)  # probe
-    per_row = dt / max(n, 1)
-    per = max(1, int(budget_s / per_row / 8))
+    # two probes fit a cost per range (the sub-problem's set-up) and per row,
+    # so the sample fills the budget
+    n1, dt1 = run_rows(4, 1)
+    n2, dt2 = run_rows(4, 8)
+    per_row = max((dt2 - dt1) / max(n2 - n1, 1), 1e-6)
+    per_range = max((dt1 - per_row * n1) / 4, 0.0)
+    per = max(1, int((budget_s - 8 * per_range) / per_row / 8))
     n, dt = run_rows(8, per)
     total = t_merge + wl.seq_q * dt / n
     desc = (f"full block merge ({t_merge:.2f} s) + {n} queries in 8 spread ranges "
