@@ -15,6 +15,13 @@ over ranks is reported.  The inputs (several GB) are larger than the 129 MB
 L2, so no flush is needed between steps.  Multi-GPU runs are independent
 replicas (each rank prefills its own copy of the workload; the path has no
 exchange step), so scaling is weak and the value is the total over ranks.
+
+End to end (`e2e`): the same K steps through the C ABI with every step's
+inputs (Q, K, V) copied from pinned host memory and its outputs (O, lse)
+copied back, pipelined as a serving loop would run them: two slots of device
+buffers, the copies on their own streams, so step i's uploads overlap step
+i-1's prefill and step i-2's downloads; events order each slot's reuse.  The
+time runs from the first upload to the last download.
 """
 from __future__ import annotations
 
@@ -692,30 +699,61 @@ def main(argv=None):
         hV = torch.from_numpy(Vh.view(np.int16) if Vh.dtype == np.uint16 else Vh).pin_memory()
         hO = torch.empty(O.numel(), dtype=torch.int16 if O.dtype == torch.bfloat16 else torch.float32).pin_memory()
         hl = torch.empty(lse.numel(), dtype=torch.float32).pin_memory()
-        Qv, Kv, Vv = (Q.view(torch.int16) if Q.dtype == torch.bfloat16 else Q,
-                      K.view(torch.int16) if K.dtype == torch.bfloat16 else K,
-                      V.view(torch.int16) if V.dtype == torch.bfloat16 else V)
-        Ov = O.view(torch.int16) if O.dtype == torch.bfloat16 else O
+        as16 = lambda t: t.view(torch.int16) if t.dtype == torch.bfloat16 else t
+        # A serving loop's pipeline: two slots of device inputs and outputs;
+        # step i's host-to-device copies (copy stream) run while step i-1
+        # computes (the compute stream) and step i-2's results return (a
+        # third stream).  Events order each slot's reuse: its inputs are
+        # overwritten only after the step that read them has computed, its
+        # outputs only after they have been copied back.
+        slots = [(Q, K, V, O, lse),
+                 (torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V),
+                  torch.empty_like(O), torch.empty_like(lse))]
+        hOs = [hO, torch.empty_like(hO).pin_memory()]
+        hls = [hl, torch.empty_like(hl).pin_memory()]
+        s_in = torch.cuda.Stream(dev)
+        s_out = torch.cuda.Stream(dev)
+        in_done = [torch.cuda.Event() for _ in range(2)]
+        comp_done = [torch.cuda.Event() for _ in range(2)]
+        out_done = [torch.cuda.Event() for _ in range(2)]
+        used = [False, False]
 
-        def e2e_step():
-            Qv.view(-1).copy_(hQ.view(-1), non_blocking=True)
-            Kv.view(-1).copy_(hK.view(-1), non_blocking=True)
-            Vv.view(-1).copy_(hV.view(-1), non_blocking=True)
-            step()
-            hO.copy_(Ov.view(-1), non_blocking=True)
-            hl.copy_(lse.view(-1), non_blocking=True)
+        def e2e_step(i):
+            b = i & 1
+            Qb, Kb, Vb, Ob, lb = slots[b]
+            with torch.cuda.stream(s_in):
+                if used[b]:
+                    s_in.wait_event(comp_done[b])
+                as16(Qb).view(-1).copy_(hQ.view(-1), non_blocking=True)
+                as16(Kb).view(-1).copy_(hK.view(-1), non_blocking=True)
+                as16(Vb).view(-1).copy_(hV.view(-1), non_blocking=True)
+                in_done[b].record(s_in)
+            stream.wait_event(in_done[b])
+            if used[b]:
+                stream.wait_event(out_done[b])
+            sgqa.sgqa_prefill(p, Qb, Kb, Vb, Kbar, Ob, lb, ws, page_table=pt,
+                              kbar_valid_blocks=kvalid, status=st, stream=stream)
+            comp_done[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[b])
+                hOs[b].copy_(as16(Ob).view(-1), non_blocking=True)
+                hls[b].copy_(lb.view(-1), non_blocking=True)
+                out_done[b].record(s_out)
+            used[b] = True
 
-        for _ in range(max(1, min(args.warmup, 2))):
-            e2e_step()
+        for i in range(max(2, min(args.warmup, 2))):
+            e2e_step(i)
         barrier()
         torch.cuda.synchronize(dev)
-        ev0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        ev1.record(stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s_in)
+        for i in range(args.steps):
+            e2e_step(i)
+        s_out.wait_event(comp_done[(args.steps - 1) & 1])
+        e1.record(s_out)
         torch.cuda.synchronize(dev)
         barrier()
-        e2e_ms = reduce_max(ev0.elapsed_time(ev1) / args.steps, dev)
+        e2e_ms = reduce_max(e0.elapsed_time(e1) / args.steps, dev)
         h2d = (hQ.numel() + hK.numel() + hV.numel()) * hQ.element_size()
         d2h = hO.numel() * hO.element_size() + hl.numel() * 4
         e2e = {"value": world * wl.seq_q / (e2e_ms * 1e-3), "unit": UNIT,
