@@ -824,8 +824,9 @@ SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int
     // the chunk has rows of more than 16384 blocks), tile union and attention;
     // where some rows select from threshold candidates, the sampled-key gather
     // once and per such chunk the sampled-block GEMM, the thresholds, the
-    // candidate select and the refill GEMM of the row tiles it left (the rows
-    // it leaves then all go through the warp-per-row select)
+    // candidate select (after zeroing its two counters and the row-tile
+    // flags) and the refill GEMM of the row tiles it left (the rows it leaves
+    // then all go through the warp-per-row select)
     const bool any_filt = dm.nblk > 0 && chunk_filtered(dm, 0, dm.T);
     const bool pack = use_pack(dm);
     int64_t n = (dm.nblk > 0 ? 1 : 0) + (dm.dtype == SGQA_FP32 ? (pack ? 1 : 3) : 0) +
@@ -833,7 +834,7 @@ SGQA_API int sgqa_prefill_plan(const sgqa_params* p, int64_t* chunk_queries, int
     for (int64_t q0 = 0; q0 < dm.T; q0 += chunk) {
       const int64_t q1 = std::min<int64_t>(dm.T, q0 + chunk);
       const bool filt = any_filt && chunk_filtered(dm, q0, q1);
-      n += (dm.nblk > 0 ? 2 : 0) + 1 + (filt ? 4 + 2 : topk_union_launches(dm, q0, q1));
+      n += (dm.nblk > 0 ? 2 : 0) + 1 + (filt ? 4 + 2 + 2 : topk_union_launches(dm, q0, q1));
     }
     *launches = (int32_t)(n * dm.batch);
   }

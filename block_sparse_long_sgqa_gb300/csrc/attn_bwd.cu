@@ -1094,9 +1094,14 @@ int launch_attn_bwd(const Dims& dm, const __nv_bfloat16* Q, const __nv_bfloat16*
                                              const_cast<float*>(a.Dl));
   log_end(st);
   if (cudaGetLastError() != cudaSuccess) return SGQA_ERR_CUDA;
-  if (cudaMemsetAsync(w + oB, 0, (size_t)dm.Hkv * a.nks * a.nw * 4, st) != cudaSuccess ||
-      cudaMemsetAsync(w + oF, 0xFF, (size_t)dm.Hkv * dm.ntiles * a.nks * 4, st) != cudaSuccess)
-    return SGQA_ERR_CUDA;
+  log_begin(SGQA_K_STAGE, st);
+  bool filled = fill_u32(w + oB, (int64_t)dm.Hkv * a.nks * a.nw, 0u, st) == cudaSuccess;
+  log_end(st);
+  log_begin(SGQA_K_STAGE, st);
+  filled = filled &&
+           fill_u32(w + oF, (int64_t)dm.Hkv * dm.ntiles * a.nks, 0xFFFFFFFFu, st) == cudaSuccess;
+  log_end(st);
+  if (!filled) return SGQA_ERR_CUDA;
   const int64_t warps = (int64_t)dm.Hkv * dm.ntiles;
   log_begin(SGQA_K_STAGE, st);
   k_bwd_index<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(a, SB);

@@ -414,4 +414,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Fill n 32-bit words with v by a kernel on the stream: a runtime memset can
+// be carried out by a copy engine, where it waits behind large transfers
+// issued on other streams (an overlapped upload of the next inputs).
+namespace {
+__global__ void __launch_bounds__(256) k_fill_u32(uint32_t* p, int64_t n, uint32_t v) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = v;
+}
+}  // namespace
+inline cudaError_t fill_u32(void* p, int64_t n, uint32_t v, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t blocks = (n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024;
+  k_fill_u32<<<(unsigned)blocks, 256, 0, st>>>(static_cast<uint32_t*>(p), n, v);
+  return cudaGetLastError();
+}
+
 }  // namespace sgqa

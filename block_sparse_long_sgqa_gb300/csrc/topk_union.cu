@@ -1264,9 +1264,13 @@ int launch_cand_rows(const Dims& dm, int64_t q_begin, int64_t q_end, int32_t* se
   a.flist = flist;
   a.status = status;
   const int64_t nrt = (nq + 127) / 128;
-  if (cudaMemsetAsync(counters, 0, 2 * sizeof(int32_t), st) != cudaSuccess ||
-      cudaMemsetAsync(tflag, 0, (size_t)dm.Hkv * nrt * sizeof(int32_t), st) != cudaSuccess)
-    return SGQA_ERR_CUDA;
+  log_begin(SGQA_K_TOPK_UNION, st);
+  bool zeroed = fill_u32(counters, 2, 0u, st) == cudaSuccess;
+  log_end(st);
+  log_begin(SGQA_K_TOPK_UNION, st);
+  zeroed = zeroed && fill_u32(tflag, (int64_t)dm.Hkv * nrt, 0u, st) == cudaSuccess;
+  log_end(st);
+  if (!zeroed) return SGQA_ERR_CUDA;
   int dev = 0, nsm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
