@@ -290,7 +290,10 @@ SGQA_API int sgqa_topk_union_noalloc(const sgqa_params* p, const float* scores, 
  * [0, kbar_valid_blocks) are taken as already merged (earlier chunks of a
  * chunked prefill) and the rest are merged here.  Same outputs and numerics
  * as the step-by-step entry points.  Workspace: sgqa_workspace_bytes(p,
- * SGQA_WS_PREFILL). */
+ * SGQA_WS_PREFILL); chunks are sized so that a chunk's fp32 score rows take
+ * up to 8 GiB (4 GiB when rows exceed 16384 blocks), which with the
+ * candidate lists and operand copies comes to about 12 GiB for 131072 queries
+ * over 8 KV groups of 16384 blocks. */
 SGQA_API int sgqa_prefill(const sgqa_params* p, const void* Q, const void* K, const void* V,
                           const int32_t* page_table, float* Kbar, int32_t kbar_valid_blocks,
                           void* O, float* lse, void* ws, size_t ws_bytes, int32_t* status,

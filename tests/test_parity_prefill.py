@@ -216,10 +216,10 @@ def test_prefill_candidates_equal_full_select(s, case):
 @pytest.mark.parametrize("case", ["b8", "filt", "mixed"])
 def test_prefill_plan_counts_launches(s, case):
     """sgqa_prefill_plan's launch count is the number of kernels the call
-    enqueues: chunks without candidates (b8), with them (filt), and both in
-    one call (the 128K shapes at 32K tokens: two chunks of 16384 queries,
-    the first with rows under 2048 blocks)."""
-    mixed = synth.WORKLOADS["step5_128k"].replace(name="mixed", seq_q=32768, seq_kv=32768)
+    enqueues: chunks without candidates (b8), with them (filt), and several
+    chunks in one call (the 128K shapes at 64K tokens: two chunks of 32768
+    queries, the first with rows on both sides of 2048 blocks)."""
+    mixed = synth.WORKLOADS["step5_128k"].replace(name="mixed", seq_q=65536, seq_kv=65536)
     wl = {"b8": SMALL["b8"], "filt": FILT, "mixed": mixed}[case]
     p = s.params_for(wl)
     _, planned = s.sgqa_prefill_plan(p)
