@@ -437,8 +437,8 @@ SGQA_API int sgqa_block_merge(const sgqa_params* p, const void* K, const int32_t
   Dims dm;
   int rc = derive(p, &dm);
   if (rc != SGQA_OK) return rc;
-  if (K == nullptr || Kbar == nullptr || blk_begin < 0 || blk_end < blk_begin ||
-      blk_end > dm.nblk || ((dm.ps > 0) != (page_table != nullptr)))
+  if (K == nullptr || (Kbar == nullptr && blk_end > blk_begin) || blk_begin < 0 ||
+      blk_end < blk_begin || blk_end > dm.nblk || ((dm.ps > 0) != (page_table != nullptr)))
     return SGQA_ERR_INVALID_ARG;
   if (!aligned16(K) || !aligned16(Kbar)) return SGQA_ERR_ALIGNMENT;
   (void)status;
@@ -733,8 +733,8 @@ SGQA_API int sgqa_prefill_ex(const sgqa_params* p, const void* Q, const void* K,
   int rc = derive(p, &dm);
   if (rc != SGQA_OK) return rc;
   if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr || lse == nullptr ||
-      Kbar == nullptr || kbar_valid_blocks < 0 || kbar_valid_blocks > dm.nblk ||
-      ((dm.ps > 0) != (page_table != nullptr)))
+      (Kbar == nullptr && dm.nblk > 0) || kbar_valid_blocks < 0 ||
+      kbar_valid_blocks > dm.nblk || ((dm.ps > 0) != (page_table != nullptr)))
     return SGQA_ERR_INVALID_ARG;
   const void* Qidx = idx ? idx->Qidx : nullptr;
   const void* Kidx = idx ? idx->Kidx : nullptr;

@@ -172,7 +172,8 @@ SGQA_API int64_t sgqa_union_capacity(const sgqa_params* p);
  * summed in fp32 as adjacent pairs level by level (((k0+k1)+(k2+k3))+((k4+k5)+(k6+k7))
  * for B = 8) and then multiplied by 1/B.  K is contiguous or paged (page_table
  * non-NULL iff p->page_size > 0).  Other blocks of Kbar are left untouched, so a
- * chunked prefill can extend a cached Kbar.  0 <= blk_begin <= blk_end <= nblk. */
+ * chunked prefill can extend a cached Kbar.  0 <= blk_begin <= blk_end <= nblk;
+ * Kbar may be NULL for an empty range. */
 SGQA_API int sgqa_block_merge(const sgqa_params* p, const void* K, const int32_t* page_table,
                               int32_t blk_begin, int32_t blk_end, float* Kbar, int32_t* status,
                               sgqa_stream_t stream);
@@ -286,7 +287,8 @@ SGQA_API int sgqa_topk_union_noalloc(const sgqa_params* p, const float* scores, 
 
 /* Steps 1-6 fused into one enqueue: merge -> index scores -> top-k -> union ->
  * attention, chunked over queries so that intermediates stay within the
- * workspace.  Kbar is a caller-owned block-key cache [Hkv][nblk] fp32: blocks
+ * workspace.  Kbar is a caller-owned block-key cache [Hkv][nblk] fp32 (NULL
+ * allowed when seq_kv < block_size, i.e. nblk = 0): blocks
  * [0, kbar_valid_blocks) are taken as already merged (earlier chunks of a
  * chunked prefill) and the rest are merged here.  Same outputs and numerics
  * as the step-by-step entry points.  Workspace: sgqa_workspace_bytes(p,

@@ -82,6 +82,47 @@ def test_prefill_end_to_end(s, name):
     assert frac > 0.9
 
 
+EDGE = {
+    # one query at position 0: no historical block, only itself to attend
+    "one_query_at_0": SMALL["b8"].replace(name="e1", seq_q=1, seq_kv=1, q_offset=0),
+    # a call shorter than one block: every query sees only its own block
+    "under_one_block": SMALL["b8"].replace(name="e2", seq_q=5, seq_kv=5, q_offset=0),
+    # a last tile of one query, rows of at most nine blocks (all selected)
+    "ragged_one_query_tile": SMALL["b8"].replace(name="e3", seq_q=65, seq_kv=65, q_offset=0),
+    # one query at the first position of a block with exactly k/B blocks before it
+    "block_start": SMALL["b8"].replace(name="e4", seq_q=1, seq_kv=257, q_offset=256),
+    # one query whose row just exceeds k/B blocks (the first real selection)
+    "first_selection": SMALL["b8"].replace(name="e5", seq_q=2, seq_kv=271, q_offset=269),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+def test_prefill_edge_shapes(s, name):
+    """Degenerate shapes through the fused call against the oracle: a single
+    query with nothing before it, calls shorter than a block, a one-query
+    last tile, and rows at the edge of the selection (exactly k/B blocks,
+    one more)."""
+    wl = EDGE[name]
+    inp = synth.make_inputs(wl)
+    p = s.params_for(wl)
+    d = dev_inputs(inp)
+    O, lse, Kbar = run_prefill(s, p, d)
+    assert torch.isfinite(O.float()).all() and torch.isfinite(lse).all()
+    rows = np.arange(wl.seq_q, dtype=np.int32)
+    if wl.seq_kv >= wl.block_size:  # R3 and R2 on the standalone selection
+        _, frac = check_end_to_end(s, wl, inp, O, lse, rows, Kbar, d)
+        assert frac >= 0.5
+    else:  # no complete block: nothing to select, R3 on every row
+        Q, K, V = widened(inp)
+        S, _, O64, lse64 = oracle.prefill_rows(Q, K, V, wl.q_offset, wl.block_size, wl.k_blocks,
+                                               rows)
+        G = wl.n_q_heads // wl.n_kv_heads
+        mask = np.repeat(clear_margin(S, wl, rows).T, G, axis=1)
+        assert mask.all()
+        r3_check(O.float().cpu().numpy()[rows], lse.cpu().numpy()[:, rows], O64, lse64, mask,
+                 lse_tol=lse_tol_for(wl, inp, rows))
+
+
 def test_prefill_mode_full(s):
     wl, inp = SMALL["b8"], inputs("b8")
     p = s.params_for(wl, union_mode=1)
