@@ -20,7 +20,7 @@ import torch
 
 import oracle
 from block_sparse_long_sgqa_gb300 import synth
-from helpers import dev_inputs
+from helpers import clear_margin, dev_inputs, lse_tol_for, r3_check, widened
 from test_parity_prefill import check_end_to_end, run_prefill
 
 pytestmark = pytest.mark.gpu
@@ -94,3 +94,37 @@ def test_decode_loop_persistent_cache(s):
     lo = cache.Ksplit[1, :, :nb].float()
     assert torch.equal(hi, cache.Kbar[:, :nb].to(torch.bfloat16).float())
     assert (hi + lo - cache.Kbar[:, :nb]).abs().max().item() <= 2.0 ** -16 * cache.Kbar[:, :nb].abs().max().item()
+
+
+@pytest.mark.parametrize("pos", [0, 5, 256, 300])
+def test_decode_edge_positions(s, pos):
+    """Decode steps at the edges of the selection, on small heads: the first
+    position (no block before it), inside the first block, at the first
+    position after exactly k/B blocks (all of them attended), and past it
+    (a real selection); each step against the oracle, the cache's blocks
+    bit-exact against the oracle's merge."""
+    wl = synth.WORKLOADS["step5_128k"].replace(name="dec_edge", seq_q=1, q_offset=pos,
+                                               seq_kv=pos + 1, n_q_heads=32, n_kv_heads=4,
+                                               topk_tokens=256, needles=0)
+    inp = synth.make_inputs(wl)
+    p = s.params_for(wl)
+    d = dev_inputs(inp)
+    cache = s.KeyCache(p, cap_blocks=64)
+    O, lse = s.alloc_outputs(p)
+    st = s.new_status()
+    s.sgqa_decode(p, d["Q"], d["K"], d["V"], cache, O, lse, s.alloc_workspace(p, s.WS_DECODE),
+                  page_table=d["page_table"], status=st)
+    assert s.read_status(st)[0] == 0
+    nb = (pos + 1) // wl.block_size
+    assert cache.valid_blocks == nb
+    Q, K, V = widened(inp)
+    rows = np.arange(1, dtype=np.int32)
+    S, _, O64, lse64 = oracle.prefill_rows(Q, K, V, wl.q_offset, wl.block_size, wl.k_blocks, rows)
+    G = wl.n_q_heads // wl.n_kv_heads
+    mask = np.repeat(clear_margin(S, wl, rows).T, G, axis=1)
+    assert mask.mean() >= 0.5
+    r3_check(O.float().cpu().numpy(), lse.cpu().numpy(), O64, lse64, mask,
+             lse_tol=lse_tol_for(wl, inp, rows))
+    if nb:
+        ref = oracle.merge_tree_f32(synth.widen(inp["K"]), wl.block_size)[:, :nb]
+        assert np.array_equal(cache.Kbar[:, :nb].cpu().numpy().view(np.uint32), ref.view(np.uint32))
