@@ -495,7 +495,7 @@ SGQA_API int sgqa_topk_union(const sgqa_params* p, const float* scores, int32_t 
       (q_end % dm.W && q_end != dm.T))
     return SGQA_ERR_INVALID_ARG;
   if ((dm.nblk > 0 && scores == nullptr) || union_off == nullptr || union_len == nullptr ||
-      union_blk == nullptr || union_mask == nullptr)
+      ((union_blk == nullptr || union_mask == nullptr) && group_cap(dm) > 0))
     return SGQA_ERR_INVALID_ARG;
   if (scores && !aligned16(scores)) return SGQA_ERR_ALIGNMENT;
   if (union_cap < sgqa_union_capacity(p)) return SGQA_ERR_WORKSPACE;
@@ -529,8 +529,9 @@ SGQA_API int sgqa_sparse_attn_fwd(const sgqa_params* p, const void* Q, const voi
   int rc = derive(p, &dm);
   if (rc != SGQA_OK) return rc;
   if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr || lse == nullptr ||
-      union_off == nullptr || union_len == nullptr || union_blk == nullptr ||
-      union_mask == nullptr || ((dm.ps > 0) != (page_table != nullptr)))
+      union_off == nullptr || union_len == nullptr ||
+      ((union_blk == nullptr || union_mask == nullptr) && group_cap(dm) > 0) ||
+      ((dm.ps > 0) != (page_table != nullptr)))
     return SGQA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
     return SGQA_ERR_ALIGNMENT;
@@ -572,7 +573,8 @@ SGQA_API int sgqa_sparse_attn_bwd(const sgqa_params* p, const void* Q, const voi
   if (rc != SGQA_OK) return rc;
   if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr || lse == nullptr ||
       dO == nullptr || dQ == nullptr || dK == nullptr || dV == nullptr || union_off == nullptr ||
-      union_len == nullptr || union_blk == nullptr || union_mask == nullptr ||
+      union_len == nullptr ||
+      ((union_blk == nullptr || union_mask == nullptr) && group_cap(dm) > 0) ||
       ((dm.ps > 0) != (page_table != nullptr)))
     return SGQA_ERR_INVALID_ARG;
   if (dm.dtype != SGQA_BF16 || dm.B < 8 || (dm.G & (dm.G - 1)) != 0 ||

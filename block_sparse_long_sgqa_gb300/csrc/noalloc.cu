@@ -64,7 +64,7 @@ extern "C" SGQA_API int sgqa_topk_union_noalloc(const sgqa_params* p, const floa
       (q_end % dm.W && q_end != dm.T))
     return SGQA_ERR_INVALID_ARG;
   if ((dm.nblk > 0 && scores == nullptr) || union_off == nullptr || union_len == nullptr ||
-      union_blk == nullptr || union_mask == nullptr)
+      ((union_blk == nullptr || union_mask == nullptr) && sgqa_union_capacity(p) > 0))
     return SGQA_ERR_INVALID_ARG;
   if (scores && (reinterpret_cast<uintptr_t>(scores) & 15u)) return SGQA_ERR_ALIGNMENT;
   if (union_cap < sgqa_union_capacity(p)) return SGQA_ERR_WORKSPACE;

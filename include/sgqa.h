@@ -203,7 +203,9 @@ SGQA_API int sgqa_index_scores(const sgqa_params* p, const void* Q, const float*
  * capacity-based layout), union_len[g][tau] = its length; union_blk[slot] =
  * block ids in ascending order; union_mask[slot] bit i set iff query
  * tau * tile_q + i selected that block.  union_cap = length of union_blk and
- * union_mask, at least sgqa_union_capacity(p).
+ * union_mask, at least sgqa_union_capacity(p) (when that is 0, no query has a
+ * historical block, and union_blk / union_mask may be NULL here and in the
+ * attention calls).
  * Workspace: sgqa_workspace_bytes(p, SGQA_WS_TOPK_UNION). */
 SGQA_API int sgqa_topk_union(const sgqa_params* p, const float* scores, int32_t q_begin,
                              int32_t q_end, int32_t* topk_idx, int64_t* union_off,

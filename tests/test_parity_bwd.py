@@ -185,3 +185,47 @@ def test_attn_bwd_full_size(s, name):
     close(dV[k0:], dV64[k0:], "dV last keys")
     dQ2, dK2, dV2 = run_bwd(s, p, d, u, O, lse, dO, wl)
     assert torch.equal(dQ, dQ2) and torch.equal(dK, dK2) and torch.equal(dV, dV2)
+
+
+BWD_EDGE = {
+    "one_query_at_0": SMALL["b8"].replace(name="be1", seq_q=1, seq_kv=1, q_offset=0),
+    "under_one_block": SMALL["b8"].replace(name="be2", seq_q=5, seq_kv=5, q_offset=0),
+    "ragged_one_query_tile": SMALL["b8"].replace(name="be3", seq_q=65, seq_kv=65, q_offset=0),
+    "first_selection": SMALL["b8"].replace(name="be4", seq_q=2, seq_kv=271, q_offset=269),
+}
+
+
+@pytest.mark.parametrize("name", list(BWD_EDGE))
+def test_attn_bwd_edge_shapes(s, name):
+    """The backward on degenerate shapes (a single query with nothing before
+    it, a call shorter than a block, a one-query last tile, rows just past
+    k/B blocks) against the oracle's fp64 backward on the oracle's lists."""
+    wl = BWD_EDGE[name]
+    inp = synth.make_inputs(wl)
+    p = s.params_for(wl)
+    rows = np.arange(wl.seq_q, dtype=np.int32)
+    Q, K, V = widened(inp)
+    S = oracle.scores(oracle.index_query(Q, wl.n_kv_heads, rows), oracle.merge_f64(K, wl.block_size),
+                      wl.block_size, wl.q_offset, rows)
+    sel = oracle.select(S, wl.block_size, wl.q_offset, rows, wl.k_blocks)
+    csr = oracle.union(sel, wl.tile_q, wl.n_blocks)
+    d = dev_inputs(inp)
+    union = _upload_union(*csr, wl.n_kv_heads, 0)
+    O, lse = s.alloc_outputs(p)
+    st = s.new_status()
+    s.sgqa_sparse_attn_fwd(p, d["Q"], d["K"], d["V"], *union, O, lse, page_table=d["page_table"],
+                           ws=s.alloc_workspace(p, s.WS_SPARSE_ATTN), status=st)
+    assert s.read_status(st)[0] == 0
+    rng = np.random.default_rng(79)
+    dOb = synth.to_bf16_bits(rng.standard_normal((wl.seq_q, wl.n_q_heads, wl.head_dim)).astype(np.float32))
+    dQ, dK, dV = run_bwd(s, p, d, union, O, lse, to_dev(dOb), wl)
+    dQ64, dK64, dV64 = oracle.sparse_attn_bwd(Q, K, V, synth.widen(dOb).astype(np.float64),
+                                              wl.q_offset, wl.block_size, sel, 0, csr, wl.tile_q)
+    for got, ref, nm in ((dQ, dQ64, "dQ"), (dK, dK64, "dK"), (dV, dV64, "dV")):
+        if np.abs(ref).max() == 0.0:
+            # a query that attends only itself has P = 1, so dS = dP - D = 0
+            # and dQ, dK vanish exactly; the GPU's D comes from the bf16 O,
+            # which leaves rounding noise
+            assert np.abs(got.double().cpu().numpy()).max() <= 1e-4, nm
+        else:
+            close(got, ref, nm)
