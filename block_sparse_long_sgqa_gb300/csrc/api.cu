@@ -459,8 +459,8 @@ SGQA_API int sgqa_index_scores(const sgqa_params* p, const void* Q, const float*
   Dims dm;
   int rc = derive(p, &dm);
   if (rc != SGQA_OK) return rc;
-  if (Q == nullptr || Kbar == nullptr || scores == nullptr || q_begin < 0 || q_end < q_begin ||
-      q_end > dm.T)
+  if (Q == nullptr || ((Kbar == nullptr || scores == nullptr) && dm.nblk > 0) || q_begin < 0 ||
+      q_end < q_begin || q_end > dm.T)
     return SGQA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(Kbar) || !aligned16(scores)) return SGQA_ERR_ALIGNMENT;
   if (ws == nullptr || ws_bytes < sgqa_workspace_bytes(p, SGQA_WS_INDEX_SCORES))

@@ -184,7 +184,9 @@ SGQA_API int sgqa_block_merge(const sgqa_params* p, const void* K, const int32_t
  * query heads of group g.  Computed on tcgen05 tensor cores from a two-term
  * bf16 split of both operands (hi*hi + hi*lo + lo*hi, fp32 accumulation), so
  * the error against an fp64 evaluation is about 1e-5 of |qt| |Kbar|.
- * Workspace: sgqa_workspace_bytes(p, SGQA_WS_INDEX_SCORES). */
+ * Workspace: sgqa_workspace_bytes(p, SGQA_WS_INDEX_SCORES).  With no complete
+ * block (seq_kv < block_size) there is nothing to score and Kbar and scores
+ * may be NULL. */
 SGQA_API int sgqa_index_scores(const sgqa_params* p, const void* Q, const float* Kbar,
                                int32_t q_begin, int32_t q_end, float* scores, void* ws,
                                size_t ws_bytes, int32_t* status, sgqa_stream_t stream);

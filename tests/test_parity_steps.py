@@ -43,6 +43,11 @@ SMALL = {
     "f32_paged_b4": synth.WORKLOADS["tiny_2k"].replace(name="f32_paged_b4", seq_q=300, seq_kv=700,
                                                       q_offset=400, block_size=4, topk_tokens=64,
                                                       page_size=64),
+    # degenerate: one query at position 0 (no block, no union) and a query
+    # pair whose rows just exceed k/B blocks (the first real selection)
+    "edge_one": BASE.replace(name="edge_one", seq_q=1, seq_kv=1, q_offset=0, topk_tokens=256),
+    "edge_first_sel": BASE.replace(name="edge_first_sel", seq_q=2, seq_kv=271, q_offset=269,
+                                   topk_tokens=256),
     # Step-5-shaped heads with planted needles: large logit jumps between stages
     # exercise the online-softmax rescale of O in TMEM
     "needles": synth.WORKLOADS["step5_128k"].replace(name="needles", seq_q=1200, seq_kv=1200,
