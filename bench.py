@@ -717,6 +717,16 @@ def main(argv=None):
         comp_done = [torch.cuda.Event() for _ in range(2)]
         out_done = [torch.cuda.Event() for _ in range(2)]
         used = [False, False]
+        # per-step spans of the three streams' work (each starts once its waits
+        # are met): where the end-to-end time goes
+        spans = None
+
+        def mark(s):
+            if spans is None:
+                return None
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(s)
+            return ev
 
         def e2e_step(i):
             b = i & 1
@@ -724,22 +734,30 @@ def main(argv=None):
             with torch.cuda.stream(s_in):
                 if used[b]:
                     s_in.wait_event(comp_done[b])
+                a0 = mark(s_in)
                 as16(Qb).view(-1).copy_(hQ.view(-1), non_blocking=True)
                 as16(Kb).view(-1).copy_(hK.view(-1), non_blocking=True)
                 as16(Vb).view(-1).copy_(hV.view(-1), non_blocking=True)
                 in_done[b].record(s_in)
+                a1 = mark(s_in)
             stream.wait_event(in_done[b])
             if used[b]:
                 stream.wait_event(out_done[b])
+            c0 = mark(stream)
             sgqa.sgqa_prefill(p, Qb, Kb, Vb, Kbar, Ob, lb, ws, page_table=pt,
                               kbar_valid_blocks=kvalid, status=st, stream=stream)
             comp_done[b].record(stream)
+            c1 = mark(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(comp_done[b])
+                d0 = mark(s_out)
                 hOs[b].copy_(as16(Ob).view(-1), non_blocking=True)
                 hls[b].copy_(lb.view(-1), non_blocking=True)
                 out_done[b].record(s_out)
+                d1 = mark(s_out)
             used[b] = True
+            if spans is not None:
+                spans.append((a0, a1, c0, c1, d0, d1))
 
         for i in range(max(2, min(args.warmup, 2))):
             e2e_step(i)
@@ -759,6 +777,18 @@ def main(argv=None):
         e2e = {"value": world * wl.seq_q / (e2e_ms * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms}
+        # a second, untimed pass with per-stream events: the uploads', the
+        # prefill's and the downloads' own durations while the three overlap
+        spans = []
+        for i in range(min(args.steps, 8)):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
+        if spans:
+            mean = lambda j: statistics.mean(x[j].elapsed_time(x[j + 1]) for x in spans)
+            h_ms, c_ms, d_ms = mean(0), mean(2), mean(4)
+            e2e["overlap"] = {"steps": len(spans), "h2d_ms": h_ms, "prefill_ms": c_ms, "d2h_ms": d_ms,
+                              "h2d_gbs": h2d / (h_ms * 1e-3) / 1e9,
+                              "d2h_gbs": d2h / (d_ms * 1e-3) / 1e9}
 
     # ---------------- a chunked prefill's cached prefix: its merge timed alone
     # (the timed steps merge only the chunk's new blocks)
