@@ -53,36 +53,43 @@ __device__ __forceinline__ void split_store8(const float (&v)[8], __nv_bfloat16*
   *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// One thread = 8 consecutive head-dim lanes of one (block, group).
-// Sum of the B rows as adjacent pairs level by level, then times 1/B.
-template <typename T, int B>
+// One unit = one (block, group): CH = d / 8 threads, each 8 consecutive
+// head-dim lanes of the block's B rows (B independent 16- or 32-byte loads).
+// Sum of the B rows as adjacent pairs level by level, then times 1/B.  The
+// unit's rows sit in one page (the page size is a multiple of B), so a paged
+// cache costs one page-table read per unit.
+template <typename T, int B, int CH>
 __global__ void __launch_bounds__(256) k_block_merge(const T* __restrict__ K,
                                                      const int32_t* __restrict__ page_table,
                                                      int64_t blk_begin, int64_t nblocks, int Hkv,
-                                                     int d, int ps, int64_t nblk,
+                                                     int ps, int64_t nblk,
                                                      float* __restrict__ Kbar,
                                                      __nv_bfloat16* __restrict__ khi,
                                                      __nv_bfloat16* __restrict__ klo) {
-  const int chunks = d / 8;
-  const int64_t total = nblocks * Hkv * chunks;
-  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
-       x += (int64_t)gridDim.x * blockDim.x) {
-    const int c = (int)(x % chunks);
-    const int g = (int)((x / chunks) % Hkv);
-    const int64_t j = blk_begin + x / ((int64_t)chunks * Hkv);
+  constexpr int D = CH * 8;
+  constexpr int UPB = 256 / CH;  // units per CTA pass
+  const int c = threadIdx.x % CH;
+  const int64_t units = nblocks * Hkv;
+  // rows of one (position run, group) are D apart in a page, Hkv * D apart
+  // in a contiguous cache
+  const int64_t rstride = ps > 0 ? D : (int64_t)Hkv * D;
+  for (int64_t u = (int64_t)blockIdx.x * UPB + threadIdx.x / CH; u < units;
+       u += (int64_t)gridDim.x * UPB) {
+    const int64_t jr = u / Hkv;
+    const int g = (int)(u - jr * Hkv);
+    const int64_t j = blk_begin + jr;
+    const int64_t p0 = j * B;
+    const T* row;
+    if (ps > 0) {
+      const int64_t lp = p0 / ps;
+      const int64_t phys = page_table[lp];
+      row = K + ((phys * Hkv + g) * ps + (p0 - lp * ps)) * (int64_t)D + c * 8;
+    } else {
+      row = K + (p0 * Hkv + g) * (int64_t)D + c * 8;
+    }
     float v[B][8];
 #pragma unroll
-    for (int r = 0; r < B; ++r) {
-      const int64_t p = j * B + r;
-      const T* row;
-      if (ps > 0) {
-        const int64_t phys = page_table[p / ps];
-        row = K + ((phys * Hkv + g) * ps + (p % ps)) * (int64_t)d;
-      } else {
-        row = K + (p * Hkv + g) * (int64_t)d;
-      }
-      Vec8<T>::load(row + c * 8, v[r]);
-    }
+    for (int r = 0; r < B; ++r) Vec8<T>::load(row + r * rstride, v[r]);
 #pragma unroll
     for (int w = B; w > 1; w /= 2)
 #pragma unroll
@@ -92,7 +99,7 @@ __global__ void __launch_bounds__(256) k_block_merge(const T* __restrict__ K,
     const float inv = 1.0f / (float)B;  // exact: B is a power of two
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[0][i] = __fmul_rn(v[0][i], inv);
-    const int64_t o = ((int64_t)g * nblk + j) * d + c * 8;
+    const int64_t o = ((int64_t)g * nblk + j) * D + c * 8;
     float4* dst = reinterpret_cast<float4*>(Kbar + o);
     dst[0] = make_float4(v[0][0], v[0][1], v[0][2], v[0][3]);
     dst[1] = make_float4(v[0][4], v[0][5], v[0][6], v[0][7]);
@@ -178,6 +185,18 @@ __global__ void __launch_bounds__(256) k_to_bf16_paged(const float* __restrict__
   }
 }
 
+// Eight consecutive elements as bf16 (16 bytes): copied as they are from a
+// bf16 cache, rounded to nearest from an fp32 one.
+__device__ __forceinline__ uint4 load_bf16x8(const __nv_bfloat16* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ uint4 load_bf16x8(const float* p) {
+  float v[8];
+  Vec8<float>::load(p, v);
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
+}
+
 // Block-packed K/V for the attention gathers: block j of KV head g becomes
 // B/8 groups of 8 positions; each group holds its d/64 head-dim halves as
 // 1 KB atoms of 8 rows x 128 B with the 128-byte swizzle (16-byte unit u of
@@ -185,43 +204,53 @@ __global__ void __launch_bounds__(256) k_to_bf16_paged(const float* __restrict__
 // lands directly in the layout the tensor cores read.  Positions at or past
 // Tkv (a partial last block) and the extra block at index nblkp are zero.
 // Output [Hkv][nblkp + 1][B * d] bf16, nblkp = ceil(Tkv / B).
-template <typename T>
+// One (group, block) = CH = d / 8 threads, each one 16-byte unit of the
+// block's B rows (loaded up to eight rows at a time, then stored); the
+// block's rows sit in one page (the page size is a multiple of B).
+template <typename T, int B, int CH>
 __global__ void __launch_bounds__(256) k_kv_pack(const T* __restrict__ X,
                                                  const int32_t* __restrict__ page_table,
-                                                 int64_t Tkv, int Hkv, int d, int B, int ps,
-                                                 int64_t nblkp, __nv_bfloat16* __restrict__ out) {
-  const int units = d / 8;  // 16-byte units of a row
-  const int KC = d / 64;
-  const int64_t per_g = (nblkp + 1) * B * units;
-  const int64_t total = (int64_t)Hkv * per_g;
-  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
-       x += (int64_t)gridDim.x * blockDim.x) {
-    const int g = (int)(x / per_g);
-    const int64_t rem = x % per_g;
-    const int64_t j = rem / ((int64_t)B * units);
-    const int rr = (int)((rem / units) % B);
-    const int u = (int)(rem % units);
-    const int64_t p = j * B + rr;
-    float v[8];
-    if (j < nblkp && p < Tkv) {
-      const T* row;
+                                                 int64_t Tkv, int Hkv, int ps, int64_t nblkp,
+                                                 __nv_bfloat16* __restrict__ out) {
+  constexpr int D = CH * 8, KC = D / 64;
+  constexpr int UPB = 256 / CH;      // (group, block) pairs per CTA pass
+  constexpr int RB = B < 8 ? B : 8;  // rows in flight per thread
+  const int u = threadIdx.x % CH, c = u >> 3, uu = u & 7;
+  const int64_t nbp = nblkp + 1;
+  const int64_t pairs = (int64_t)Hkv * nbp;
+  const int64_t rstride = ps > 0 ? D : (int64_t)Hkv * D;
+  for (int64_t x = (int64_t)blockIdx.x * UPB + threadIdx.x / CH; x < pairs;
+       x += (int64_t)gridDim.x * UPB) {
+    const int64_t gq = x / nbp;
+    const int g = (int)gq;
+    const int64_t j = x - gq * nbp;
+    const int64_t p0 = j * B;
+    const T* row = nullptr;
+    if (j < nblkp) {
       if (ps > 0) {
-        const int64_t phys = page_table[p / ps];
-        row = X + ((phys * Hkv + g) * ps + (p % ps)) * (int64_t)d;
+        const int64_t lp = p0 / ps;
+        const int64_t phys = page_table[lp];
+        row = X + ((phys * Hkv + g) * ps + (p0 - lp * ps)) * (int64_t)D + u * 8;
       } else {
-        row = X + (p * Hkv + g) * (int64_t)d;
+        row = X + (p0 * Hkv + g) * (int64_t)D + u * 8;
       }
-      Vec8<T>::load(row + u * 8, v);
-    } else {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = 0.0f;
     }
-    const int r8 = rr & 7, grp = rr >> 3, c = u >> 3, uu = u & 7;
-    const int64_t o = ((int64_t)g * (nblkp + 1) + j) * B * d +  // element offset of the block
-                      ((int64_t)grp * KC * 1024 + c * 1024 + r8 * 128 + ((uu ^ r8) << 4)) / 2;
-    const uint4 w = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                               pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-    *reinterpret_cast<uint4*>(out + o) = w;
+    // rows of the block that exist (a partial last block, the zero block)
+    const int nval = row == nullptr ? 0 : (Tkv - p0 < B ? (int)(Tkv - p0) : B);
+    __nv_bfloat16* blk = out + x * (int64_t)(B * D);  // x = g * nbp + j
+#pragma unroll
+    for (int r0 = 0; r0 < B; r0 += RB) {
+      uint4 w[RB];
+#pragma unroll
+      for (int k = 0; k < RB; ++k)
+        w[k] = r0 + k < nval ? load_bf16x8(row + (r0 + k) * rstride) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int k = 0; k < RB; ++k) {
+        const int rr = r0 + k, r8 = rr & 7, grp = rr >> 3;
+        const int o = (grp * KC * 1024 + c * 1024 + r8 * 128 + ((uu ^ r8) << 4)) / 2;
+        *reinterpret_cast<uint4*>(blk + o) = w[k];
+      }
+    }
   }
 }
 
@@ -254,12 +283,18 @@ int grid_for(int64_t work) {
 template <typename T>
 cudaError_t merge_dispatch(const Dims& dm, const T* K, const int32_t* pt, int64_t b0, int64_t nb,
                            float* Kbar, __nv_bfloat16* khi, __nv_bfloat16* klo, cudaStream_t st) {
+  if (dm.d != 128 && dm.d != 64) return cudaErrorInvalidValue;
   const int grid = grid_for(nb * dm.Hkv * (dm.d / 8));
   log_begin(SGQA_K_MERGE, st);
+  bool known = true;
 #define SGQA_MERGE_CASE(BB)                                                                   \
   case BB:                                                                                    \
-    k_block_merge<T, BB><<<grid, 256, 0, st>>>(K, pt, b0, nb, dm.Hkv, dm.d, dm.ps, dm.nblk,  \
-                                               Kbar, khi, klo);                               \
+    if (dm.d == 128)                                                                          \
+      k_block_merge<T, BB, 16><<<grid, 256, 0, st>>>(K, pt, b0, nb, dm.Hkv, dm.ps, dm.nblk,   \
+                                                     Kbar, khi, klo);                         \
+    else                                                                                      \
+      k_block_merge<T, BB, 8><<<grid, 256, 0, st>>>(K, pt, b0, nb, dm.Hkv, dm.ps, dm.nblk,    \
+                                                    Kbar, khi, klo);                          \
     break;
   switch (dm.B) {
     SGQA_MERGE_CASE(1)
@@ -268,11 +303,11 @@ cudaError_t merge_dispatch(const Dims& dm, const T* K, const int32_t* pt, int64_
     SGQA_MERGE_CASE(8)
     SGQA_MERGE_CASE(16)
     default:
-      log_end(st);
-      return cudaErrorInvalidValue;
+      known = false;
   }
 #undef SGQA_MERGE_CASE
   log_end(st);
+  if (!known) return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
@@ -333,19 +368,42 @@ cudaError_t launch_index_query(const Dims& dm, const void* Q, int64_t q_begin, i
   return cudaGetLastError();
 }
 
+namespace {
+
+template <typename T>
+cudaError_t kv_pack_dispatch(const Dims& dm, const T* X, const int32_t* pt, int64_t nblkp,
+                             __nv_bfloat16* out, cudaStream_t st) {
+  if (dm.d != 128 && dm.d != 64) return cudaErrorInvalidValue;
+  const int grid = grid_for((int64_t)dm.Hkv * (nblkp + 1) * (dm.d / 8));
+  bool known = true;
+  log_begin(SGQA_K_STAGE, st);
+#define SGQA_PACK_CASE(BB)                                                                      \
+  case BB:                                                                                      \
+    if (dm.d == 128)                                                                            \
+      k_kv_pack<T, BB, 16><<<grid, 256, 0, st>>>(X, pt, dm.Tkv, dm.Hkv, dm.ps, nblkp, out);     \
+    else                                                                                        \
+      k_kv_pack<T, BB, 8><<<grid, 256, 0, st>>>(X, pt, dm.Tkv, dm.Hkv, dm.ps, nblkp, out);      \
+    break;
+  switch (dm.B) {
+    SGQA_PACK_CASE(8)
+    SGQA_PACK_CASE(16)
+    default:
+      known = false;
+  }
+#undef SGQA_PACK_CASE
+  log_end(st);
+  if (!known) return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_kv_pack(const Dims& dm, const void* X, const int32_t* page_table,
                            __nv_bfloat16* out, cudaStream_t st) {
   const int64_t nblkp = (dm.Tkv + dm.B - 1) / dm.B;
-  const int64_t total = (int64_t)dm.Hkv * (nblkp + 1) * dm.B * (dm.d / 8);
-  log_begin(SGQA_K_STAGE, st);
   if (dm.dtype == SGQA_BF16)
-    k_kv_pack<<<grid_for(total), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(X), page_table,
-                                                 dm.Tkv, dm.Hkv, dm.d, dm.B, dm.ps, nblkp, out);
-  else
-    k_kv_pack<<<grid_for(total), 256, 0, st>>>(static_cast<const float*>(X), page_table, dm.Tkv,
-                                                 dm.Hkv, dm.d, dm.B, dm.ps, nblkp, out);
-  log_end(st);
-  return cudaGetLastError();
+    return kv_pack_dispatch(dm, static_cast<const __nv_bfloat16*>(X), page_table, nblkp, out, st);
+  return kv_pack_dispatch(dm, static_cast<const float*>(X), page_table, nblkp, out, st);
 }
 
 cudaError_t launch_to_bf16(const float* in, __nv_bfloat16* out, int64_t n, cudaStream_t st) {
