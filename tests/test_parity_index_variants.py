@@ -58,8 +58,8 @@ def test_index_scores_bf16_vs_oracle(s, name):
     # one bf16 ulp (<= 2^-7 |s|), plus an operand that rounded the other way
     prod = np.einsum("rgi,gji->grj", np.abs(qt32.astype(np.float64)), np.abs(kb32.astype(np.float64)))
     bound = 2.0 ** -7 * np.abs(ref.astype(np.float64)) + 2.0 ** -8 * prod + 1e-30
-    err = np.abs(got.astype(np.float64) - ref)
-    assert (err[fin] <= bound[fin]).all(), float((err[fin] / bound[fin]).max())
+    err = np.abs(got[fin].astype(np.float64) - ref[fin])
+    assert (err <= bound[fin]).all(), float((err / bound[fin]).max())
     assert (got[fin] == ref[fin]).mean() > 0.98
 
 
