@@ -30,7 +30,7 @@ def _worker(rank, world, port, out):
 
 def test_reductions_two_ranks_gloo():
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
         assert dict(out) == {0: (2.5, 30.0), 1: (2.5, 30.0)}
