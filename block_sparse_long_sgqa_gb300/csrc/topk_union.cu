@@ -849,12 +849,19 @@ __device__ void finish_tile(const TUArgs& a, int g, int64_t tau, int64_t base, i
         const int64_t x = xb + u * 32 + lane;
         jj[u] = x < need ? lst[x] : -1;
       }
+      // every slot first, then the updates (an update between two slot reads
+      // would hold the second back)
+      uint32_t sl[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int32_t j = jj[u];
-        if (j < 0) continue;
+        const int32_t j = jj[u] < 0 ? 0 : jj[u];
         const int w = j >> 5;
-        const int64_t slot = wprefix[w] + __popc(tile_bits[w] & ((1u << (j & 31)) - 1u));
+        sl[u] = wprefix[w] + __popc(tile_bits[w] & ((1u << (j & 31)) - 1u));
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (jj[u] < 0) continue;
+        const int64_t slot = sl[u];
         if (in_smem) {
           atomicOr(i < 32 ? &mlo[slot] : &mhi[slot], 1u << (i & 31));
         } else {
@@ -953,18 +960,27 @@ __global__ void __launch_bounds__(UNION_THREADS) k_tile_union(TUArgs a, int64_t 
     if (nh > a.nblk) nh = a.nblk;
     const int need = (int)(nh < a.Ks ? nh : a.Ks);
     const int32_t* lst = a.sel + ((int64_t)g * a.nq + (t - a.q_begin)) * a.Ks;
-    // each lane ORs a contiguous piece of the ascending list, one atomic per word run
+    // each lane ORs a contiguous piece of the ascending list, one atomic per
+    // word run; the piece's entries are loaded 16 at a time ahead of the
+    // updates (an update between two loads would hold the second back)
     const int per = (need + 31) / 32;
     const int xa = lane * per, x1 = min(need, xa + per);
     uint32_t word = 0xffffffffu, bits = 0;
-    for (int x = xa; x < x1; ++x) {
-      const int32_t j = lst[x];
-      if ((uint32_t)(j >> 5) != word) {
-        if (bits) atomicOr(&tile_bits[word], bits);
-        word = (uint32_t)(j >> 5);
-        bits = 0;
+    for (int x0 = xa; x0 < x1; x0 += 16) {
+      int32_t jj[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) jj[u] = x0 + u < x1 ? lst[x0 + u] : -1;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int32_t j = jj[u];
+        if (j < 0) continue;
+        if ((uint32_t)(j >> 5) != word) {
+          if (bits) atomicOr(&tile_bits[word], bits);
+          word = (uint32_t)(j >> 5);
+          bits = 0;
+        }
+        bits |= 1u << (j & 31);
       }
-      bits |= 1u << (j & 31);
     }
     if (bits) atomicOr(&tile_bits[word], bits);
   }
