@@ -322,7 +322,7 @@ def run_reference(args, wl, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(wl, args),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": desc},
+                             "sample": desc, "extrapolated": True},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     return line
@@ -866,7 +866,7 @@ def main(argv=None):
     if rank == 0 and world == 1 and not args.no_cpu and args.union_mode == "masked":
         v, desc, _ = oracle_sample(wl, inp, args.cpu_seconds)
         cpu = {"value": v, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-               "sample": desc}
+               "sample": desc, "extrapolated": True}
 
     if rank == 0:
         line = {"metric": METRIC, "value": world * wl.seq_q / (ms_max * 1e-3), "unit": UNIT,
